@@ -1,0 +1,401 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test ties one step of the oracle to a closed form, an invariant, a
+brute-force search, a library routine (math.fsum, torch SDPA in float64) or
+the accuracy the pages report for the FP8-PV path (cosine >= 0.99926 against
+float64 attention on the SageAttention 2.2.0 sm_120a wheel page, accuracy
+table).  They are chosen so that a plausible slip in the oracle (a dropped
+rescale, a wrong block index, a transposed operand, a wrong mean axis, a
+wrong rounding tie) fails at least one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from quantized_attention_smooth_gb300 import workloads as wl
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# ------------------------------------------------------------------ e4m3
+def _e4m3_table(orc):
+    return orc.e4m3_value(np.arange(256, dtype=np.uint8))
+
+
+def test_e4m3_decode_known_values(orc):
+    t = _e4m3_table(orc)
+    # values fixed by the e4m3 format: bias 7, 3 mantissa bits, no inf
+    assert t[0x00] == 0.0 and t[0x80] == 0.0 and math.copysign(1, t[0x80]) < 0
+    assert t[0x01] == 2.0 ** -9          # smallest subnormal
+    assert t[0x07] == 7 * 2.0 ** -9      # largest subnormal
+    assert t[0x08] == 2.0 ** -6          # smallest normal
+    assert t[0x38] == 1.0
+    assert t[0x3C] == 1.5
+    assert t[0x7E] == 448.0              # largest finite
+    assert np.isnan(t[0x7F]) and np.isnan(t[0xFF])
+    assert t[0xB8] == -1.0
+    pos = t[:0x7F]
+    assert np.all(np.diff(pos) > 0)      # strictly increasing codes 0..126
+
+
+def _brute_force_encode(x, table):
+    """Nearest finite e4m3 value, ties to the even code, saturating."""
+    pos = table[:0x7F].astype(np.float64)           # codes 0..126
+    a = np.abs(x.astype(np.float64))
+    d = np.abs(a[:, None] - pos[None, :])
+    best = d.min(axis=1, keepdims=True)
+    cand = (d == best)
+    codes = np.arange(0x7F)
+    # ties: prefer the even code
+    even = cand & (codes[None, :] % 2 == 0)
+    pick = np.where(even.any(axis=1), np.argmax(even, axis=1), np.argmax(cand, axis=1))
+    pick = np.where(a >= 448.0, 0x7E, pick)
+    sign = np.signbit(x).astype(np.uint8) << 7
+    return (pick.astype(np.uint8) | sign)
+
+
+def test_e4m3_encode_matches_brute_force(orc):
+    t = _e4m3_table(orc)
+    pos = t[:0x7F].astype(np.float32)
+    mids = ((pos[:-1].astype(np.float64) + pos[1:]) / 2).astype(np.float32)
+    up = np.nextafter(mids, np.float32(np.inf))
+    dn = np.nextafter(mids, np.float32(0))
+    rng = np.random.default_rng(7)
+    rand = (rng.standard_normal(200000) * np.exp2(rng.uniform(-14, 10, 200000))).astype(np.float32)
+    big = np.array([447.9, 448.0, 449.0, 463.9, 464.0, 465.0, 479.0, 480.0, 1e6, 3e38], np.float32)
+    x = np.concatenate([pos, mids, up, dn, rand, big, -pos, -mids, -rand, -big])
+    got = orc.e4m3_encode(x)
+    ref = _brute_force_encode(x, t)
+    # -0.0 style zeros: compare magnitudes and signs separately
+    np.testing.assert_array_equal(got, ref)
+    assert orc.e4m3_encode(np.array([np.inf], np.float32))[0] == 0x7E
+    assert orc.e4m3_encode(np.array([-np.inf], np.float32))[0] == 0xFE
+
+
+# ----------------------------------------------------------------- helpers
+def _rand_bits(rng, shape, dtype, scale=1.0, offset=None):
+    x = rng.standard_normal(shape, dtype=np.float32) * np.float32(scale)
+    if offset is not None:
+        x += offset
+    return wl.to_bits(x.astype(np.float32), dtype)
+
+
+def _cos(a, b):
+    a = a.astype(np.float64).ravel()
+    b = b.astype(np.float64).ravel()
+    return float(a @ b / (np.linalg.norm(a) * np.linalg.norm(b)))
+
+
+def _rel_l2(a, b):
+    a = a.astype(np.float64)
+    b = b.astype(np.float64)
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+# ---------------------------------------------------------------- prologue
+def test_k_mean_is_exact_sum(orc):
+    """Mean = fp32(fsum / L): math.fsum gives the correctly rounded exact sum."""
+    rng = np.random.default_rng(11)
+    # bf16 values spanning 2^-30 .. 2^12 so that a plain fp64 running sum
+    # is inexact (exact sum needs far more than 53 bits)
+    mags = np.exp2(rng.uniform(-30, 12, size=5000)).astype(np.float32)
+    vals = wl.bits_to_float(wl.to_bits(mags * rng.choice([-1, 1], 5000).astype(np.float32),
+                                       wl.BF16), wl.BF16)
+    ref = np.float32(math.fsum(vals.astype(np.float64).tolist()) / len(vals))
+    assert orc.exact_mean(vals) == ref
+    # a sum a running fp64 accumulator gets wrong: 2^40, 1000 x 2^-20, -2^40
+    hard = np.concatenate([[2.0 ** 40], np.full(1000, 2.0 ** -20), [-2.0 ** 40]]).astype(np.float32)
+    ref = np.float32(math.fsum(hard.astype(np.float64).tolist()) / len(hard))
+    naive = np.float64(0)
+    for x in hard:
+        naive += np.float64(x)
+    assert np.float32(naive / len(hard)) != ref
+    assert orc.exact_mean(hard) == ref
+
+
+def test_prologue_k_mean_axis_and_value(orc):
+    rng = np.random.default_rng(12)
+    Hq, Hkv, L, D = 2, 2, 300, 40
+    off = rng.normal(0, 3, D).astype(np.float32)
+    q = _rand_bits(rng, (Hq, L, D), wl.F16)
+    k = _rand_bits(rng, (Hkv, L, D), wl.F16, offset=off)
+    v = _rand_bits(rng, (Hkv, L, D), wl.F16)
+    p = orc.prologue(q, k, v, wl.F16)
+    kf = wl.bits_to_float(k, wl.F16)
+    for h in range(Hkv):
+        for c in range(D):
+            ref = np.float32(math.fsum(kf[h, :, c].astype(np.float64).tolist()) / L)
+            assert p["k_mean"][h, c] == ref
+    assert np.all(p["k_mean"][:, D:] == 0)
+
+
+def test_prologue_q_codes_and_ties(orc):
+    rng = np.random.default_rng(13)
+    Hq, L, D = 1, 64, 64
+    qf = rng.standard_normal((Hq, L, D)).astype(np.float32) * \
+        np.exp2(rng.integers(-3, 4, size=(Hq, L, 1))).astype(np.float32)
+    # row 0: amax exactly 127 so the multiplier is 1 and x.5 values are ties
+    qf[0, 0, :] = 0
+    qf[0, 0, :6] = [127.0, 2.5, 3.5, -2.5, -0.5, 0.5]
+    q = wl.to_bits(qf, wl.F16)
+    k = _rand_bits(rng, (1, 8, D), wl.F16)
+    v = _rand_bits(rng, (1, 8, D), wl.F16)
+    p = orc.prologue(q, k, v, wl.F16)
+    q8, s_q = p["q8"].astype(np.int32), p["s_q"]
+    assert list(q8[0, 0, :6]) == [127, 2, 4, -2, 0, 0]          # ties to even
+    assert s_q[0, 0] == np.float32(1.0)
+    x = wl.bits_to_float(q, wl.F16)
+    assert np.all(np.abs(q8) <= 127)
+    assert np.all(np.abs(q8).max(axis=-1) == 127)                # amax -> 127
+    err = np.abs(x - q8 * s_q[..., None])
+    assert np.all(err <= s_q[..., None] * (0.5 + 1e-5))           # round trip
+
+
+def test_prologue_k_block_scales(orc):
+    rng = np.random.default_rng(14)
+    Hkv, L, D = 2, 300, 128                       # 3 blocks, ragged last one
+    scale = np.ones((1, L, 1), np.float32)
+    scale[:, 128:256] = 4.0
+    scale[:, 256:] = 0.25
+    k = wl.to_bits(rng.standard_normal((Hkv, L, D)).astype(np.float32) * scale + 5.0, wl.F16)
+    q = _rand_bits(rng, (Hkv, 4, D), wl.F16)
+    v = _rand_bits(rng, (Hkv, L, D), wl.F16)
+    p = orc.prologue(q, k, v, wl.F16)
+    kf = wl.bits_to_float(k, wl.F16)
+    khat = kf - p["k_mean"][:, None, :]
+    k8 = p["k8"].astype(np.int32)
+    assert p["s_k"].shape == (Hkv, 3)
+    for h in range(Hkv):
+        for b in range(3):
+            sl = slice(b * 128, min(L, b * 128 + 128))
+            s = p["s_k"][h, b]
+            assert np.abs(k8[h, sl]).max() == 127
+            assert np.all(np.abs(khat[h, sl] - k8[h, sl] * s) <= s * (0.5 + 1e-5))
+    # block scales follow the token magnitudes: 4x and 1/4x blocks
+    assert np.all(p["s_k"][:, 1] > 2.5 * p["s_k"][:, 0])
+    assert np.all(p["s_k"][:, 2] < 0.5 * p["s_k"][:, 0])
+
+
+def test_prologue_v_fp8_per_channel(orc):
+    rng = np.random.default_rng(15)
+    Hkv, L, D = 1, 200, 80
+    cs = np.exp2(np.arange(D) % 7 - 3).astype(np.float32)
+    vf = rng.standard_normal((Hkv, L, D)).astype(np.float32) * cs
+    v = wl.to_bits(vf, wl.F16)
+    q = _rand_bits(rng, (1, 4, D), wl.F16)
+    k = _rand_bits(rng, (1, L, D), wl.F16)
+    p = orc.prologue(q, k, v, wl.F16)
+    x = wl.bits_to_float(v, wl.F16)
+    dec = orc.e4m3_value(p["v8"])[:, :, :D]
+    s_v = p["s_v"][:, :D]
+    assert np.all(p["v_amax"][:, :D] == np.abs(x).max(axis=1))
+    assert np.all(np.abs(dec).max(axis=1) == 448.0)
+    err = np.abs(x - dec * s_v[:, None, :])
+    normal = np.abs(dec) >= 2.0 ** -6
+    assert np.all(err[normal] <= np.abs(x[normal]) * 2.0 ** -4 * (1 + 1e-5))
+    assert np.all(err[~normal] <= (2.0 ** -10 * np.broadcast_to(s_v[:, None, :], err.shape))[~normal] * (1 + 1e-5))
+    # padded channels are zero with zero scale
+    assert np.all(p["v8"][:, :, D:] == 0) and np.all(p["s_v"][:, D:] == 0)
+
+
+# ------------------------------------------------------ exact attention
+def _sdpa64(q, k, v, dtype, causal, scale):
+    qf = torch.from_numpy(wl.bits_to_float(q, dtype).astype(np.float64))
+    kf = torch.from_numpy(wl.bits_to_float(k, dtype).astype(np.float64))
+    vf = torch.from_numpy(wl.bits_to_float(v, dtype).astype(np.float64))
+    g = qf.shape[0] // kf.shape[0]
+    kf = kf.repeat_interleave(g, dim=0)
+    vf = vf.repeat_interleave(g, dim=0)
+    o = torch.nn.functional.scaled_dot_product_attention(
+        qf[None], kf[None], vf[None], is_causal=causal, scale=scale)
+    return o[0].numpy()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_exact_attention_matches_sdpa(orc, causal):
+    rng = np.random.default_rng(21)
+    Hq, Hkv, Lq, Lk, D = 4, 2, 70, 90, 40
+    q = _rand_bits(rng, (Hq, Lq, D), wl.BF16)
+    k = _rand_bits(rng, (Hkv, Lk, D), wl.BF16)
+    v = _rand_bits(rng, (Hkv, Lk, D), wl.BF16, scale=3.0)
+    # v differs strongly between kv heads so a wrong GQA map shows
+    v[1] = wl.to_bits(wl.bits_to_float(v[1], wl.BF16) + 10.0, wl.BF16)
+    scale = 0.3
+    got = orc.attn_exact(q, k, v, wl.BF16, causal, scale)
+    ref = _sdpa64(q, k, v, wl.BF16, causal, scale)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------- quantized attention
+def _hetero_case(rng, Hq, Hkv, Lq, Lk, D, dtype):
+    qs = np.exp2(rng.integers(-1, 2, size=(Hq, Lq, 1))).astype(np.float32)
+    ks = np.array([0.5, 1.0, 1.5, 2.0], np.float32)[(np.arange(Lk) // 128) % 4][None, :, None]
+    vs = np.exp2(np.arange(D) % 5 - 2).astype(np.float32)
+    off = rng.normal(0, 3, D).astype(np.float32)
+    q = wl.to_bits(rng.standard_normal((Hq, Lq, D)).astype(np.float32) * qs, dtype)
+    k = wl.to_bits(rng.standard_normal((Hkv, Lk, D)).astype(np.float32) * ks + off, dtype)
+    v = wl.to_bits(rng.standard_normal((Hkv, Lk, D)).astype(np.float32) * vs
+                   + np.arange(Hkv, dtype=np.float32)[:, None, None], dtype)
+    return q, k, v
+
+
+@pytest.mark.parametrize("causal,Hq,Hkv,Lq,Lk,D,dtype", [
+    (False, 2, 2, 200, 700, 64, wl.F16),
+    (True, 4, 2, 300, 300, 128, wl.BF16),
+    (False, 4, 1, 130, 513, 40, wl.F16),
+    (True, 2, 2, 100, 260, 80, wl.F16),     # Lq != Lk, top-left causal
+])
+def test_quantized_attention_accuracy(orc, causal, Hq, Hkv, Lq, Lk, D, dtype):
+    """Within the pages' FP8-PV accuracy (cos >= 0.99926 vs float64)."""
+    rng = np.random.default_rng(31 + D + Lk)
+    q, k, v = _hetero_case(rng, Hq, Hkv, Lq, Lk, D, dtype)
+    scale = 1.0 / math.sqrt(D)
+    p = orc.prologue(q, k, v, dtype)
+    got = orc.attn(p, causal, scale)
+    ref = orc.attn_exact(q, k, v, dtype, causal, scale)
+    ref_t = _sdpa64(q, k, v, dtype, causal, scale)
+    np.testing.assert_allclose(ref, ref_t, atol=1e-10)
+    c = _cos(got, ref)
+    r = _rel_l2(got, ref)
+    assert c >= 0.9992, c
+    assert r <= 0.05, r
+    assert np.all(np.isfinite(got))
+
+
+def test_single_key_gives_dequantized_v(orc):
+    """Lk = 1: softmax is exactly 1, P~ = 448, output = v~ * s_v."""
+    rng = np.random.default_rng(41)
+    q = _rand_bits(rng, (2, 5, 64), wl.F16)
+    k = _rand_bits(rng, (2, 1, 64), wl.F16)
+    v = _rand_bits(rng, (2, 1, 64), wl.F16, scale=2.0)
+    p = orc.prologue(q, k, v, wl.F16)
+    got = orc.attn(p, False, 0.125)
+    vdq = orc.e4m3_value(p["v8"])[:, 0, :] * p["s_v"]
+    for h in range(2):
+        # (448 v s_v) / 448 differs from v s_v only by fp32 rounding (<= 2 ulp)
+        np.testing.assert_allclose(got[h], np.broadcast_to(vdq[h], (5, 64)), rtol=2.5e-7, atol=0)
+
+
+def test_identical_keys_average_values(orc):
+    """All keys equal: uniform softmax, output = token mean of v~ * s_v."""
+    rng = np.random.default_rng(42)
+    L, D = 300, 64
+    q = _rand_bits(rng, (1, 7, D), wl.F16)
+    krow = rng.standard_normal(D).astype(np.float32)
+    k = wl.to_bits(np.broadcast_to(krow, (1, L, D)).copy(), wl.F16)
+    v = _rand_bits(rng, (1, L, D), wl.F16)
+    p = orc.prologue(q, k, v, wl.F16)
+    got = orc.attn(p, False, 0.125)
+    vdq = orc.e4m3_value(p["v8"])[0].astype(np.float64) * p["s_v"][0]
+    ref = vdq.mean(axis=0)
+    np.testing.assert_allclose(got[0], np.broadcast_to(ref, (7, D)), rtol=1e-5, atol=1e-6)
+
+
+def test_causal_mask_hides_future(orc):
+    """Changing codes of future keys leaves earlier rows bit-identical."""
+    rng = np.random.default_rng(43)
+    Hq, L, D = 2, 400, 64
+    q, k, v = _hetero_case(rng, Hq, Hq, L, L, D, wl.F16)
+    p = orc.prologue(q, k, v, wl.F16)
+    base = orc.attn(p, True, 0.125)
+    cut = 200
+    p2 = dict(p)
+    p2["k8"] = p["k8"].copy()
+    p2["v8"] = p["v8"].copy()
+    p2["k8"][:, cut:] = rng.integers(-127, 128, size=p["k8"][:, cut:].shape).astype(np.int8)
+    p2["v8"][:, cut:] = rng.integers(0, 0x7E, size=p["v8"][:, cut:].shape).astype(np.uint8)
+    p2["s_k"] = p["s_k"].copy()
+    p2["s_k"][:, 3] *= 3.0                       # block 3 = keys 384..399, all future of rows < 200
+    alt = orc.attn(p2, True, 0.125)
+    np.testing.assert_array_equal(alt[:, :cut], base[:, :cut])
+    assert not np.array_equal(alt[:, cut:], base[:, cut:])
+    # non-causal rows do see them
+    nb = orc.attn(p, False, 0.125)
+    na = orc.attn(p2, False, 0.125)
+    assert not np.array_equal(na[:, :cut], nb[:, :cut])
+
+
+def test_late_maximum_is_rescaled(orc):
+    """A dominant key in the last tile must dominate the output."""
+    rng = np.random.default_rng(44)
+    L, D = 512, 64
+    qf = np.zeros((1, 1, D), np.float32)
+    qf[0, 0, 0] = 1.0
+    kf = rng.standard_normal((1, L, D)).astype(np.float32) * 0.1
+    kf[0, 500, 0] = 60.0                         # key 500 (tile 3) wins
+    vf = rng.standard_normal((1, L, D)).astype(np.float32)
+    q, k, v = (wl.to_bits(a, wl.F16) for a in (qf, kf, vf))
+    p = orc.prologue(q, k, v, wl.F16)
+    got = orc.attn(p, False, 1.0)
+    ref = orc.attn_exact(q, k, v, wl.F16, False, 1.0)
+    vdq = orc.e4m3_value(p["v8"])[0, 500] * p["s_v"][0]
+    assert _cos(got[0, 0], vdq) > 0.9999
+    assert _cos(got, ref) > 0.999
+
+
+def test_padding_is_output_neutral(orc):
+    """D=40 padded to 64 equals the exact unpadded attention closely."""
+    rng = np.random.default_rng(45)
+    q, k, v = _hetero_case(rng, 2, 2, 150, 150, 40, wl.F16)
+    p = orc.prologue(q, k, v, wl.F16)
+    assert p["Dp"] == 64
+    assert np.all(p["q8"][..., 40:] == 0) and np.all(p["k8"][..., 40:] == 0)
+    got = orc.attn(p, False, 1 / math.sqrt(40))
+    assert got.shape == (2, 150, 40)
+    ref = _sdpa64(q, k, v, wl.F16, False, 1 / math.sqrt(40))
+    assert _cos(got, ref) >= 0.9992
+
+
+def test_smoothing_is_output_neutral_in_exact_arithmetic(orc):
+    """softmax(q (k - mean)^T) == softmax(q k^T): the mean runs over tokens."""
+    rng = np.random.default_rng(46)
+    q = _rand_bits(rng, (1, 20, 64), wl.F16)
+    k = _rand_bits(rng, (1, 50, 64), wl.F16, offset=rng.normal(0, 4, 64).astype(np.float32))
+    v = _rand_bits(rng, (1, 50, 64), wl.F16)
+    p = orc.prologue(q, k, v, wl.F16)
+    qf, kf, vf = (torch.from_numpy(wl.bits_to_float(a, wl.F16).astype(np.float64)) for a in (q, k, v))
+    mean = torch.from_numpy(p["k_mean"][:, :64].astype(np.float64))[:, None, :]
+    a = torch.nn.functional.scaled_dot_product_attention(qf[None], kf[None], vf[None])
+    b = torch.nn.functional.scaled_dot_product_attention(qf[None], (kf - mean)[None], vf[None])
+    np.testing.assert_allclose(a.numpy(), b.numpy(), atol=1e-12)
+    # and the smoothed codes are much better balanced than the raw keys
+    assert np.abs(wl.bits_to_float(k, wl.F16).mean(axis=1)).max() > 1.0
+    kh = wl.bits_to_float(k, wl.F16) - p["k_mean"][:, None, :64]
+    assert np.abs(kh.mean(axis=1)).max() < 1e-3
+
+
+def test_smoothing_improves_accuracy(orc):
+    """With a large shared key offset the quantized output stays accurate."""
+    rng = np.random.default_rng(47)
+    D = 128
+    off = np.zeros(D, np.float32)
+    off[[7, 42, 77, 119]] = 15.0
+    q = _rand_bits(rng, (2, 256, D), wl.BF16)
+    k = _rand_bits(rng, (2, 512, D), wl.BF16, offset=off)
+    v = _rand_bits(rng, (2, 512, D), wl.BF16)
+    p = orc.prologue(q, k, v, wl.BF16)
+    got = orc.attn(p, False, 1 / math.sqrt(D))
+    ref = orc.attn_exact(q, k, v, wl.BF16, False, 1 / math.sqrt(D))
+    assert _cos(got, ref) >= 0.9992
+
+
+def test_empty_keys_give_zeros(orc):
+    q = np.zeros((1, 3, 64), np.uint16)
+    k = np.zeros((1, 0, 64), np.uint16)
+    v = np.zeros((1, 0, 64), np.uint16)
+    p = orc.prologue(q, k, v, wl.F16)
+    out = orc.attn(p, False, 0.125)
+    assert np.all(out == 0)
+
+
+def test_large_magnitude_causal_inputs_stay_finite(orc):
+    """Masked positions use real -inf: no NaN or Inf with huge logits."""
+    rng = np.random.default_rng(48)
+    q = _rand_bits(rng, (1, 256, 64), wl.BF16, scale=300.0)
+    k = _rand_bits(rng, (1, 256, 64), wl.BF16, scale=300.0)
+    v = _rand_bits(rng, (1, 256, 64), wl.BF16)
+    p = orc.prologue(q, k, v, wl.BF16)
+    out = orc.attn(p, True, 0.125)
+    assert np.all(np.isfinite(out))
