@@ -1,0 +1,193 @@
+/*
+ * sage.h - C ABI of the GB300 (sm_103a) smoothed quantized attention library.
+ *
+ * The method (SageAttention2/2++-style quantized attention) is described on
+ * these pages, cited below by title and section:
+ *   [SD] stable-diffusion.cpp, docs "SageAttention": kernel-selection table
+ *        (per-thread INT8 Q/K, FP8 PV, FP32 buffer), FP8-path paragraph
+ *        (smooth K, per-channel V, pad and permute V, FP32 output), "Use"
+ *        section (head_dim 1..128 zero-padded to 64/128, original softmax
+ *        scale, cropped output, GQA, different q/kv lengths, batches) and
+ *        the error convention (an unavailable feature reports an error).
+ *   [OV] "SageAttention: Quantized Attention Library", Core features
+ *        (INT8 QK^T per token/thread, FP8 PV, K smoothing, varlen, GQA).
+ *   [RM] SageAttention README translation, usage section (q, k, v fp16/bf16,
+ *        tensor_layout "HND" (B,H,L,D) or "NHD" (B,L,H,D), is_causal).
+ *   [RD] SageAttention-RDNA4 releases, v0.4.0 (hand-written prologue, key
+ *        mean summed in fp64, 64-bit offsets) and v0.3.0 (a refusal carries
+ *        its reason).
+ *
+ * Conventions shared by every call:
+ *  - All tensor pointers are DEVICE pointers of the current CUDA device and
+ *    are owned by the caller.  The library allocates no memory, never
+ *    synchronises the host and enqueues all work on the caller's stream.
+ *  - Arguments are validated on the host before anything is enqueued; a bad
+ *    argument returns an error and launches nothing.  The reason is kept in
+ *    a thread-local string returned by sage_last_error().
+ *  - Inputs q, k, v are fp16 or bf16, densely packed (no strided views).
+ *    Dense calls take HND (B,H,L,D) or NHD (B,L,H,D); varlen calls take
+ *    packed (T,H,D) with int32 cumulative sequence offsets.
+ *  - The output is fp32 in the same layout as q, with the caller's D
+ *    (padding channels are never written).
+ *  - D is 1..128; Hq must be a multiple of Hkv (query head h reads kv head
+ *    h / (Hq/Hkv)).  sm_scale <= 0 selects 1/sqrt(D).
+ *  - is_causal masks key j for query i when j > i (top-left alignment).
+ *  - Failures detected on the device (a bounded wait that ran out, an
+ *    inconsistent cu_seqlens array) are recorded in a status word at the
+ *    start of the workspace; sage_device_status() reads it.
+ */
+#ifndef SAGE_H_
+#define SAGE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SAGE_API __attribute__((visibility("default")))
+#else
+#define SAGE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* sage_stream_t;
+
+typedef enum {
+  SAGE_OK = 0,
+  SAGE_ERR_INVALID_ARG = 1,    /* bad pointer, size, enum or alignment      */
+  SAGE_ERR_UNSUPPORTED = 2,    /* valid request this build does not serve   */
+  SAGE_ERR_WORKSPACE = 3,      /* workspace too small or misaligned         */
+  SAGE_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed         */
+  SAGE_ERR_DEVICE_TIMEOUT = 5  /* a device-side bounded wait ran out        */
+} sage_status;
+
+enum { SAGE_HND = 0, SAGE_NHD = 1 };
+enum { SAGE_F16 = 0, SAGE_BF16 = 1 };
+
+/* Quantised operands produced by the prologue; every pointer points into
+ * the caller's workspace.  Layout (Dp = 64 if D <= 64 else 128; all token
+ * counts padded to multiples of 128 per (segment, head), padding zeroed):
+ *   q16  : [q_rows][Dp] fp16 holding the int8 codes of Q (exact integers)
+ *   k16  : [k_rows][Dp] fp16 holding the int8 codes of smoothed K
+ *   v8   : [v_rows][v_cols] e4m3 codes of V, channel-major ("permuted"):
+ *          row = (segment base) + kv_head*Dp + channel, column = token
+ *   s_q  : [q_rows] fp32, one scale per query token
+ *   s_k  : [k_rows/128] fp32, one scale per 128-token key block
+ *   s_v  : [nseg][Hkv][Dp] fp32, one scale per value channel
+ *   k_mean: [nseg][Hkv][Dp] fp32, the per-channel token mean of K
+ * Row of token t of head h in segment s: dense  (s*H + h)*L_pad + t,
+ *                                        varlen h*T_pad + base(s) + t with
+ * base(s) = 128*(s + cu[s]/128) and T_pad = 128*(nseg + total/128).       */
+typedef struct {
+  int64_t nseg, Hq, Hkv, Lq, Lk, D, Dp;
+  int32_t dtype, varlen;
+  int64_t total_q, total_k;         /* varlen packed token totals        */
+  int32_t max_q, max_k;             /* varlen length upper bounds        */
+  int64_t q_head_rows, k_head_rows; /* L_pad (dense) or T_pad (varlen)   */
+  int64_t q_rows, k_rows, v_rows, v_cols;
+  const int32_t* cu_q;              /* varlen only (device), else NULL   */
+  const int32_t* cu_k;
+  void* q16;
+  void* k16;
+  void* v8;
+  float* s_q;
+  float* s_k;
+  float* s_v;
+  float* k_mean;
+  void* stats;                      /* per-channel accumulators          */
+  uint32_t* status;                 /* device status word (workspace+0)  */
+} sage_quantized;
+
+/* Workspace bytes for a dense call (HND or NHD).  Returns 0 for invalid
+ * sizes.  The workspace must be 256-byte aligned. */
+SAGE_API size_t sage_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq,
+                            int64_t Lk, int64_t D);
+
+/* Workspace bytes for a packed varlen call with nseq sequences and total_q
+ * query / total_k key tokens. */
+SAGE_API size_t sage_workspace_bytes_varlen(int64_t nseq, int64_t total_q,
+                                   int64_t total_k, int64_t Hq, int64_t Hkv,
+                                   int64_t D);
+
+/* Quantisation prologue ([SD] FP8-path paragraph; [OV] Core features; [RD]
+ * v0.4.0): pads D to Dp, smooths K by its exact per-channel token mean
+ * (the sum is exact, rounded once to fp64), quantises Q to int8 per token
+ * and smoothed K per 128-token block, V to e4m3 per channel (largest
+ * magnitude -> 448), and writes V channel-major for the tensor cores.
+ * Fills *qt with pointers into ws.  q,k,v: dense tensors in `layout`. */
+SAGE_API sage_status sage_quant_prologue(const void* q, const void* k, const void* v,
+                                int dtype, int layout, int64_t B, int64_t Hq,
+                                int64_t Hkv, int64_t Lq, int64_t Lk, int64_t D,
+                                void* ws, size_t ws_bytes, sage_quantized* qt,
+                                sage_stream_t stream);
+
+/* Varlen prologue: q (total_q,Hq,D), k/v (total_k,Hkv,D); cu_seqlens_q/k are
+ * device int32 arrays of nseq+1 non-decreasing offsets starting at 0 and
+ * ending at total_q/total_k; max_q/max_k bound every sequence length. */
+SAGE_API sage_status sage_quant_prologue_varlen(
+    const void* q, const void* k, const void* v, int dtype,
+    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int64_t nseq,
+    int64_t total_q, int64_t total_k, int max_q, int max_k, int64_t Hq,
+    int64_t Hkv, int64_t D, void* ws, size_t ws_bytes, sage_quantized* qt,
+    sage_stream_t stream);
+
+/* Fused attention on quantised operands ([SD] kernel table: INT8 QK^T,
+ * FP8 PV with an fp32 accumulator; [OV] Core features): per 128x128 tile,
+ * exact integer S = q8 k8^T on the tensor cores, logits S*s_q*s_k*sm_scale
+ * in base 2, -inf masking, online softmax in fp32, P quantised to e4m3 as
+ * 448*P, O += P~ V~ accumulated in fp32 tensor memory, and
+ * out = O * s_v / (448 * l) in fp32.  `layout` is the dense output layout
+ * (ignored for varlen, which writes packed (total_q,Hq,D)). */
+SAGE_API sage_status sage_attn_quantized(const sage_quantized* qt, float* out,
+                                int layout, int is_causal, float sm_scale,
+                                sage_stream_t stream);
+
+/* Prologue + attention in one call (dense). */
+SAGE_API sage_status sage_attn_fwd(const void* q, const void* k, const void* v,
+                          float* out, int64_t B, int64_t Hq, int64_t Hkv,
+                          int64_t Lq, int64_t Lk, int64_t D, int layout,
+                          int is_causal, float sm_scale, int dtype, void* ws,
+                          size_t ws_bytes, sage_stream_t stream);
+
+/* Prologue + attention in one call (packed varlen, [OV] "variable-length
+ * sequences via sageattn_varlen"). */
+SAGE_API sage_status sage_attn_fwd_varlen(
+    const void* q, const void* k, const void* v, float* out,
+    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int64_t nseq,
+    int64_t total_q, int64_t total_k, int max_q, int max_k, int64_t Hq,
+    int64_t Hkv, int64_t D, int is_causal, float sm_scale, int dtype,
+    void* ws, size_t ws_bytes, sage_stream_t stream);
+
+/* Debug: the exact INT32 QK^T tile (128x128, row-major) of query tile
+ * `qtile` and key tile `ktile` of head `hq` in segment `seg`, computed with
+ * the attention kernel's own tensor-core path and converted from the fp32
+ * accumulator with round-toward-zero.  out: device int32[128*128]. */
+SAGE_API sage_status sage_debug_qk_int32(const sage_quantized* qt, int64_t seg,
+                                int64_t hq, int64_t qtile, int64_t ktile,
+                                int32_t* out, sage_stream_t stream);
+
+/* Debug: the attention kernel's fp32 -> e4m3 conversion (round to nearest
+ * even, saturating to +-448) applied to n device floats. */
+SAGE_API sage_status sage_debug_e4m3(const float* in, uint8_t* out, int64_t n,
+                            sage_stream_t stream);
+
+/* Debug hook for failure-detection tests: the next attention launches skip
+ * loading key/value tile `skip_kv_tile` (-1: off) so that the consumer's
+ * bounded wait runs out after `timeout_ns` (0: default of one second). */
+SAGE_API void sage_debug_set_fault(int skip_kv_tile, uint64_t timeout_ns);
+
+/* Reads (synchronising `stream`) the device status word of workspace ws:
+ * SAGE_OK, SAGE_ERR_DEVICE_TIMEOUT or SAGE_ERR_INVALID_ARG.  The prologue
+ * clears it; the kernels only set bits. */
+SAGE_API sage_status sage_device_status(const void* ws, sage_stream_t stream);
+
+/* Reason of the last failure on this thread ("" if none). */
+SAGE_API const char* sage_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SAGE_H_ */

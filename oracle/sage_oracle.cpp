@@ -180,7 +180,11 @@ uint8_t oracle_e4m3_encode(float x) { return e4m3_encode(x); }
 float oracle_e4m3_value(uint8_t code) { return e4m3_value(code); }
 
 void oracle_e4m3_encode_array(const float* x, uint8_t* out, int64_t n) {
-  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_encode(x[i]);
+  const int64_t block = 1 << 16;
+  parallel_for((n + block - 1) / block, 0, [&](int64_t b) {
+    const int64_t end = std::min(n, (b + 1) * block);
+    for (int64_t i = b * block; i < end; ++i) out[i] = e4m3_encode(x[i]);
+  });
 }
 
 // Exact mean of n values: fp32(fp64(exact sum) / n).  Returns 0 on success.

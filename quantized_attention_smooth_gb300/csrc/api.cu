@@ -1,0 +1,506 @@
+// C ABI of the library: argument validation, workspace layout, TMA tensor
+// maps and kernel launches.  The library allocates nothing and never
+// synchronises the host (sage_device_status excepted, which exists to read
+// the device status word back).
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "sage.h"
+#include "sage_geom.h"
+#include "sage_kernels.h"
+
+using namespace sage;
+
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<int> g_skip_kv_tile{-1};
+std::atomic<unsigned long long> g_timeout_ns{0};
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;   // 1 s
+
+sage_status fail(sage_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+sage_status ok() {
+  g_last_error.clear();
+  return SAGE_OK;
+}
+
+sage_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(SAGE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int64_t padded_dim(int64_t D) { return D <= 64 ? 64 : 128; }
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Byte offsets of every workspace buffer.
+struct WsLayout {
+  size_t status, ksum, vmax, zero_end, k_mean, s_v, v_inv, s_q, s_k, q16, k16,
+      v8, total;
+};
+
+WsLayout ws_layout(const SegGeo& g) {
+  const int64_t nstat = g.nseg * g.Hkv * g.Dp;
+  const int64_t q_rows = (g.varlen ? 1 : g.nseg) * g.Hq * g.q_head_rows;
+  const int64_t k_rows = (g.varlen ? 1 : g.nseg) * g.Hkv * g.k_head_rows;
+  const int64_t v_rows = (g.varlen ? 1 : g.nseg) * g.Hkv * g.Dp;
+  WsLayout w{};
+  size_t o = 0;
+  w.status = o; o += 256;
+  w.ksum = o; o = align256(o + nstat * 8);
+  w.vmax = o; o = align256(o + nstat * 4);
+  w.zero_end = o;
+  w.k_mean = o; o = align256(o + nstat * 4);
+  w.s_v = o; o = align256(o + nstat * 4);
+  w.v_inv = o; o = align256(o + nstat * 4);
+  w.s_q = o; o = align256(o + q_rows * 4);
+  w.s_k = o; o = align256(o + (k_rows / 128) * 4);
+  w.q16 = o; o = align256(o + q_rows * g.Dp * 2);
+  w.k16 = o; o = align256(o + k_rows * g.Dp * 2);
+  w.v8 = o; o = align256(o + v_rows * g.v_cols);
+  w.total = o;
+  return w;
+}
+
+bool check_dims(int64_t Hq, int64_t Hkv, int64_t D, sage_status* st) {
+  if (D < 1 || D > 128) {
+    *st = fail(SAGE_ERR_UNSUPPORTED, "head_dim D=%lld outside 1..128", (long long)D);
+    return false;
+  }
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0) {
+    *st = fail(SAGE_ERR_INVALID_ARG, "Hq=%lld must be a positive multiple of Hkv=%lld",
+               (long long)Hq, (long long)Hkv);
+    return false;
+  }
+  return true;
+}
+
+// Geometry of a dense call.
+SegGeo dense_geo(int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk,
+                 int64_t D, int dtype, int layout) {
+  SegGeo g{};
+  g.nseg = B; g.Hq = Hq; g.Hkv = Hkv; g.Lq = Lq; g.Lk = Lk; g.D = D;
+  g.Dp = padded_dim(D);
+  g.dtype = dtype; g.varlen = 0;
+  g.max_q = static_cast<int32_t>(Lq > INT32_MAX ? INT32_MAX : Lq);
+  g.max_k = static_cast<int32_t>(Lk > INT32_MAX ? INT32_MAX : Lk);
+  if (layout == SAGE_HND) {
+    g.q_seg_stride = Hq * Lq * D; g.q_head_stride = Lq * D; g.q_tok_stride = D;
+    g.k_seg_stride = Hkv * Lk * D; g.k_head_stride = Lk * D; g.k_tok_stride = D;
+  } else {
+    g.q_seg_stride = Lq * Hq * D; g.q_head_stride = D; g.q_tok_stride = Hq * D;
+    g.k_seg_stride = Lk * Hkv * D; g.k_head_stride = D; g.k_tok_stride = Hkv * D;
+  }
+  g.q_head_rows = round_up(Lq, 128);
+  g.k_head_rows = round_up(Lk, 128);
+  g.v_cols = g.k_head_rows;
+  return g;
+}
+
+SegGeo varlen_geo(int64_t nseq, int64_t total_q, int64_t total_k, int max_q,
+                  int max_k, int64_t Hq, int64_t Hkv, int64_t D, int dtype,
+                  const int32_t* cu_q, const int32_t* cu_k) {
+  SegGeo g{};
+  g.nseg = nseq; g.Hq = Hq; g.Hkv = Hkv; g.Lq = 0; g.Lk = 0; g.D = D;
+  g.Dp = padded_dim(D);
+  g.dtype = dtype; g.varlen = 1;
+  g.cu_q = cu_q; g.cu_k = cu_k;
+  g.total_q = total_q; g.total_k = total_k;
+  g.max_q = max_q; g.max_k = max_k;
+  g.q_seg_stride = 0; g.q_head_stride = D; g.q_tok_stride = Hq * D;
+  g.k_seg_stride = 0; g.k_head_stride = D; g.k_tok_stride = Hkv * D;
+  g.q_head_rows = 128 * (nseq + total_q / 128);
+  g.k_head_rows = 128 * (nseq + total_k / 128);
+  g.v_cols = g.k_head_rows;
+  return g;
+}
+
+bool aligned(const void* p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+sage_status check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3)
+    return fail(SAGE_ERR_UNSUPPORTED,
+                "device %d is sm_%d%d; this build runs on sm_103 (GB300) only", dev,
+                major, minor);
+  return SAGE_OK;
+}
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  }
+  return fn;
+}
+
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, void* base,
+               uint64_t inner, uint64_t outer, uint64_t row_bytes,
+               uint32_t box_inner, uint32_t box_outer) {
+  EncodeFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+sage_status make_maps(const sage_quantized* qt, AttnMaps* maps) {
+  if (!encode_2d(&maps->q, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qt->q16, qt->Dp, qt->q_rows,
+                 qt->Dp * 2, 64, 128) ||
+      !encode_2d(&maps->k, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qt->k16, qt->Dp, qt->k_rows,
+                 qt->Dp * 2, 64, 128) ||
+      !encode_2d(&maps->v, CU_TENSOR_MAP_DATA_TYPE_UINT8, qt->v8, qt->v_cols, qt->v_rows,
+                 qt->v_cols, 128, static_cast<uint32_t>(qt->Dp)))
+    return fail(SAGE_ERR_CUDA, "cuTensorMapEncodeTiled failed or unavailable");
+  return SAGE_OK;
+}
+
+SegGeo geo_of(const sage_quantized* qt) {
+  SegGeo g{};
+  g.nseg = qt->nseg; g.Hq = qt->Hq; g.Hkv = qt->Hkv; g.Lq = qt->Lq; g.Lk = qt->Lk;
+  g.D = qt->D; g.Dp = qt->Dp; g.dtype = qt->dtype; g.varlen = qt->varlen;
+  g.cu_q = qt->cu_q; g.cu_k = qt->cu_k; g.total_q = qt->total_q; g.total_k = qt->total_k;
+  g.max_q = qt->max_q; g.max_k = qt->max_k;
+  g.q_head_rows = qt->q_head_rows; g.k_head_rows = qt->k_head_rows; g.v_cols = qt->v_cols;
+  return g;
+}
+
+void fill_quantized(const SegGeo& g, const WsLayout& w, uint8_t* ws, sage_quantized* qt) {
+  std::memset(qt, 0, sizeof(*qt));
+  qt->nseg = g.nseg; qt->Hq = g.Hq; qt->Hkv = g.Hkv; qt->Lq = g.Lq; qt->Lk = g.Lk;
+  qt->D = g.D; qt->Dp = g.Dp; qt->dtype = g.dtype; qt->varlen = g.varlen;
+  qt->total_q = g.total_q; qt->total_k = g.total_k; qt->max_q = g.max_q; qt->max_k = g.max_k;
+  qt->q_head_rows = g.q_head_rows; qt->k_head_rows = g.k_head_rows;
+  qt->q_rows = (g.varlen ? 1 : g.nseg) * g.Hq * g.q_head_rows;
+  qt->k_rows = (g.varlen ? 1 : g.nseg) * g.Hkv * g.k_head_rows;
+  qt->v_rows = (g.varlen ? 1 : g.nseg) * g.Hkv * g.Dp;
+  qt->v_cols = g.v_cols;
+  qt->cu_q = g.cu_q; qt->cu_k = g.cu_k;
+  qt->q16 = ws + w.q16; qt->k16 = ws + w.k16; qt->v8 = ws + w.v8;
+  qt->s_q = reinterpret_cast<float*>(ws + w.s_q);
+  qt->s_k = reinterpret_cast<float*>(ws + w.s_k);
+  qt->s_v = reinterpret_cast<float*>(ws + w.s_v);
+  qt->k_mean = reinterpret_cast<float*>(ws + w.k_mean);
+  qt->stats = ws + w.ksum;
+  qt->status = reinterpret_cast<uint32_t*>(ws + w.status);
+}
+
+// Shared tail of both prologue entry points (arguments already validated).
+sage_status run_prologue(const SegGeo& g, const void* q, const void* k, const void* v,
+                         void* ws, size_t ws_bytes, sage_quantized* qt,
+                         cudaStream_t st) {
+  const WsLayout w = ws_layout(g);
+  if (ws == nullptr || !aligned(ws, 256))
+    return fail(SAGE_ERR_WORKSPACE, "workspace must be a 256-byte aligned device pointer");
+  if (ws_bytes < w.total)
+    return fail(SAGE_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, w.total);
+  if (g.q_head_rows * g.Hq * (g.varlen ? 1 : g.nseg) >= (int64_t(1) << 31) ||
+      g.k_head_rows * g.Hkv * (g.varlen ? 1 : g.nseg) >= (int64_t(1) << 31) ||
+      g.v_cols >= (int64_t(1) << 31))
+    return fail(SAGE_ERR_UNSUPPORTED, "problem exceeds 2^31 workspace rows");
+  sage_status s = check_device();
+  if (s != SAGE_OK) return s;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  fill_quantized(g, w, wsb, qt);
+  cudaError_t e = cudaMemsetAsync(wsb, 0, w.zero_end, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  PrologueBuffers b{};
+  b.q = static_cast<const uint16_t*>(q);
+  b.k = static_cast<const uint16_t*>(k);
+  b.v = static_cast<const uint16_t*>(v);
+  b.q16 = reinterpret_cast<uint16_t*>(wsb + w.q16);
+  b.k16 = reinterpret_cast<uint16_t*>(wsb + w.k16);
+  b.v8 = wsb + w.v8;
+  b.s_q = reinterpret_cast<float*>(wsb + w.s_q);
+  b.s_k = reinterpret_cast<float*>(wsb + w.s_k);
+  b.s_v = reinterpret_cast<float*>(wsb + w.s_v);
+  b.k_mean = reinterpret_cast<float*>(wsb + w.k_mean);
+  b.v_inv = reinterpret_cast<float*>(wsb + w.v_inv);
+  b.ksum = wsb + w.ksum;
+  b.vmax = reinterpret_cast<uint32_t*>(wsb + w.vmax);
+  b.status = reinterpret_cast<uint32_t*>(wsb + w.status);
+  const bool vec = (g.D % 8 == 0) && aligned(q, 16) && aligned(k, 16) && aligned(v, 16);
+  e = launch_prologue(g, b, vec, st);
+  if (e != cudaSuccess) return cuda_fail(e, "prologue launch");
+  return ok();
+}
+
+sage_status check_common(const void* q, const void* k, const void* v, int dtype) {
+  if (dtype != SAGE_F16 && dtype != SAGE_BF16)
+    return fail(SAGE_ERR_INVALID_ARG, "dtype %d is neither SAGE_F16 nor SAGE_BF16", dtype);
+  if (q == nullptr || k == nullptr || v == nullptr)
+    return fail(SAGE_ERR_INVALID_ARG, "q, k and v must be non-null device pointers");
+  if (!aligned(q, 2) || !aligned(k, 2) || !aligned(v, 2))
+    return fail(SAGE_ERR_INVALID_ARG, "q, k and v must be 2-byte aligned");
+  return SAGE_OK;
+}
+
+float resolve_scale(float sm_scale, int64_t D) {
+  return sm_scale > 0.0f ? sm_scale : 1.0f / sqrtf(static_cast<float>(D));
+}
+
+sage_status launch_attn(const sage_quantized* qt, float* out, int layout, int is_causal,
+                        float sm_scale, cudaStream_t st) {
+  AttnMaps maps;
+  sage_status s = make_maps(qt, &maps);
+  if (s != SAGE_OK) return s;
+  AttnParams p{};
+  p.g = geo_of(qt);
+  p.s_q = qt->s_q; p.s_k = qt->s_k; p.s_v = qt->s_v;
+  p.out = out;
+  if (qt->varlen) {
+    p.out_seg_stride = 0; p.out_head_stride = qt->D; p.out_tok_stride = qt->Hq * qt->D;
+  } else if (layout == SAGE_HND) {
+    p.out_seg_stride = qt->Hq * qt->Lq * qt->D; p.out_head_stride = qt->Lq * qt->D;
+    p.out_tok_stride = qt->D;
+  } else {
+    p.out_seg_stride = qt->Lq * qt->Hq * qt->D; p.out_head_stride = qt->D;
+    p.out_tok_stride = qt->Hq * qt->D;
+  }
+  p.scale_log2 = resolve_scale(sm_scale, qt->D) * 1.44269504088896340736f;
+  p.causal = is_causal ? 1 : 0;
+  p.skip_kv_tile = g_skip_kv_tile.load();
+  const unsigned long long t = g_timeout_ns.load();
+  p.timeout_ns = t ? t : kDefaultTimeoutNs;
+  p.status = qt->status;
+  cudaError_t e = launch_attention(maps, p, st);
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return ok();
+}
+
+int64_t out_elems_dense(int64_t B, int64_t Hq, int64_t Lq, int64_t D) {
+  return B * Hq * Lq * D;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t sage_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk,
+                            int64_t D) {
+  if (B < 0 || Lq < 0 || Lk < 0 || D < 1 || D > 128 || Hq < 1 || Hkv < 1 || Hq % Hkv)
+    return 0;
+  return ws_layout(dense_geo(B, Hq, Hkv, Lq, Lk, D, 0, SAGE_HND)).total;
+}
+
+size_t sage_workspace_bytes_varlen(int64_t nseq, int64_t total_q, int64_t total_k,
+                                   int64_t Hq, int64_t Hkv, int64_t D) {
+  if (nseq < 0 || total_q < 0 || total_k < 0 || D < 1 || D > 128 || Hq < 1 || Hkv < 1 ||
+      Hq % Hkv)
+    return 0;
+  return ws_layout(varlen_geo(nseq, total_q, total_k, 0, 0, Hq, Hkv, D, 0, nullptr,
+                              nullptr)).total;
+}
+
+sage_status sage_quant_prologue(const void* q, const void* k, const void* v, int dtype,
+                                int layout, int64_t B, int64_t Hq, int64_t Hkv,
+                                int64_t Lq, int64_t Lk, int64_t D, void* ws,
+                                size_t ws_bytes, sage_quantized* qt,
+                                sage_stream_t stream) {
+  if (qt == nullptr) return fail(SAGE_ERR_INVALID_ARG, "qt must not be null");
+  sage_status s = SAGE_OK;
+  if (layout != SAGE_HND && layout != SAGE_NHD)
+    return fail(SAGE_ERR_INVALID_ARG, "layout %d is neither SAGE_HND nor SAGE_NHD", layout);
+  if (B < 0 || Lq < 0 || Lk < 0)
+    return fail(SAGE_ERR_INVALID_ARG, "negative size (B=%lld Lq=%lld Lk=%lld)",
+                (long long)B, (long long)Lq, (long long)Lk);
+  if (!check_dims(Hq, Hkv, D, &s)) return s;
+  if ((s = check_common(q, k, v, dtype)) != SAGE_OK) return s;
+  if (B == 0 || Lq == 0 || Lk == 0)
+    return fail(SAGE_ERR_INVALID_ARG, "the prologue needs B, Lq and Lk > 0");
+  return run_prologue(dense_geo(B, Hq, Hkv, Lq, Lk, D, dtype, layout), q, k, v, ws,
+                      ws_bytes, qt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sage_status sage_quant_prologue_varlen(const void* q, const void* k, const void* v,
+                                       int dtype, const int32_t* cu_seqlens_q,
+                                       const int32_t* cu_seqlens_k, int64_t nseq,
+                                       int64_t total_q, int64_t total_k, int max_q,
+                                       int max_k, int64_t Hq, int64_t Hkv, int64_t D,
+                                       void* ws, size_t ws_bytes, sage_quantized* qt,
+                                       sage_stream_t stream) {
+  if (qt == nullptr) return fail(SAGE_ERR_INVALID_ARG, "qt must not be null");
+  sage_status s = SAGE_OK;
+  if (!check_dims(Hq, Hkv, D, &s)) return s;
+  if ((s = check_common(q, k, v, dtype)) != SAGE_OK) return s;
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr || !aligned(cu_seqlens_q, 4) ||
+      !aligned(cu_seqlens_k, 4))
+    return fail(SAGE_ERR_INVALID_ARG, "cu_seqlens_q/k must be aligned device pointers");
+  if (nseq < 1 || total_q < 1 || total_k < 1 || max_q < 1 || max_k < 1)
+    return fail(SAGE_ERR_INVALID_ARG,
+                "varlen prologue needs nseq, totals and maxima > 0 (nseq=%lld)",
+                (long long)nseq);
+  if (nseq > 65535) return fail(SAGE_ERR_UNSUPPORTED, "nseq=%lld > 65535", (long long)nseq);
+  return run_prologue(varlen_geo(nseq, total_q, total_k, max_q, max_k, Hq, Hkv, D, dtype,
+                                 cu_seqlens_q, cu_seqlens_k),
+                      q, k, v, ws, ws_bytes, qt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sage_status sage_attn_quantized(const sage_quantized* qt, float* out, int layout,
+                                int is_causal, float sm_scale, sage_stream_t stream) {
+  if (qt == nullptr || qt->q16 == nullptr || qt->status == nullptr)
+    return fail(SAGE_ERR_INVALID_ARG, "qt is null or was not filled by the prologue");
+  if (out == nullptr || !aligned(out, 4))
+    return fail(SAGE_ERR_INVALID_ARG, "out must be a 4-byte aligned device pointer");
+  if (!qt->varlen && layout != SAGE_HND && layout != SAGE_NHD)
+    return fail(SAGE_ERR_INVALID_ARG, "layout %d is neither SAGE_HND nor SAGE_NHD", layout);
+  if (qt->nseg > 65535 || qt->Hq > 65535)
+    return fail(SAGE_ERR_UNSUPPORTED, "more than 65535 segments or heads");
+  sage_status s = check_device();
+  if (s != SAGE_OK) return s;
+  return launch_attn(qt, out, layout, is_causal, sm_scale,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+sage_status sage_attn_fwd(const void* q, const void* k, const void* v, float* out,
+                          int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk,
+                          int64_t D, int layout, int is_causal, float sm_scale, int dtype,
+                          void* ws, size_t ws_bytes, sage_stream_t stream) {
+  sage_status s = SAGE_OK;
+  if (layout != SAGE_HND && layout != SAGE_NHD)
+    return fail(SAGE_ERR_INVALID_ARG, "layout %d is neither SAGE_HND nor SAGE_NHD", layout);
+  if (B < 0 || Lq < 0 || Lk < 0)
+    return fail(SAGE_ERR_INVALID_ARG, "negative size (B=%lld Lq=%lld Lk=%lld)",
+                (long long)B, (long long)Lq, (long long)Lk);
+  if (!check_dims(Hq, Hkv, D, &s)) return s;
+  if (B == 0 || Lq == 0) return ok();                 // nothing to compute
+  if ((s = check_common(q, k, v, dtype)) != SAGE_OK) return s;
+  if (out == nullptr || !aligned(out, 4))
+    return fail(SAGE_ERR_INVALID_ARG, "out must be a 4-byte aligned device pointer");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (Lk == 0) {                                      // empty softmax: zeros
+    if ((s = check_device()) != SAGE_OK) return s;
+    cudaError_t e = cudaMemsetAsync(out, 0, out_elems_dense(B, Hq, Lq, D) * 4, st);
+    return e == cudaSuccess ? ok() : cuda_fail(e, "cudaMemsetAsync");
+  }
+  sage_quantized qt;
+  s = run_prologue(dense_geo(B, Hq, Hkv, Lq, Lk, D, dtype, layout), q, k, v, ws, ws_bytes,
+                   &qt, st);
+  if (s != SAGE_OK) return s;
+  if (qt.nseg > 65535 || qt.Hq > 65535)
+    return fail(SAGE_ERR_UNSUPPORTED, "more than 65535 segments or heads");
+  return launch_attn(&qt, out, layout, is_causal, sm_scale, st);
+}
+
+sage_status sage_attn_fwd_varlen(const void* q, const void* k, const void* v, float* out,
+                                 const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                 int64_t nseq, int64_t total_q, int64_t total_k, int max_q,
+                                 int max_k, int64_t Hq, int64_t Hkv, int64_t D,
+                                 int is_causal, float sm_scale, int dtype, void* ws,
+                                 size_t ws_bytes, sage_stream_t stream) {
+  sage_status s = SAGE_OK;
+  if (!check_dims(Hq, Hkv, D, &s)) return s;
+  if (nseq < 0 || total_q < 0 || total_k < 0)
+    return fail(SAGE_ERR_INVALID_ARG, "negative varlen size");
+  if (nseq == 0 || total_q == 0) return ok();
+  if (out == nullptr || !aligned(out, 4))
+    return fail(SAGE_ERR_INVALID_ARG, "out must be a 4-byte aligned device pointer");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (total_k == 0) {
+    if ((s = check_common(q, q, q, dtype)) != SAGE_OK) return s;
+    if ((s = check_device()) != SAGE_OK) return s;
+    cudaError_t e = cudaMemsetAsync(out, 0, total_q * Hq * D * 4, st);
+    return e == cudaSuccess ? ok() : cuda_fail(e, "cudaMemsetAsync");
+  }
+  sage_quantized qt;
+  s = sage_quant_prologue_varlen(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, nseq, total_q,
+                                 total_k, max_q, max_k, Hq, Hkv, D, ws, ws_bytes, &qt,
+                                 stream);
+  if (s != SAGE_OK) return s;
+  return launch_attn(&qt, out, SAGE_NHD, is_causal, sm_scale, st);
+}
+
+sage_status sage_debug_qk_int32(const sage_quantized* qt, int64_t seg, int64_t hq,
+                                int64_t qtile, int64_t ktile, int32_t* out,
+                                sage_stream_t stream) {
+  if (qt == nullptr || qt->q16 == nullptr || out == nullptr)
+    return fail(SAGE_ERR_INVALID_ARG, "null argument");
+  if (qt->varlen) return fail(SAGE_ERR_UNSUPPORTED, "debug tiles are for dense calls only");
+  if (seg < 0 || seg >= qt->nseg || hq < 0 || hq >= qt->Hq || qtile < 0 ||
+      qtile * 128 >= qt->q_head_rows || ktile < 0 || ktile * 128 >= qt->k_head_rows)
+    return fail(SAGE_ERR_INVALID_ARG, "tile index out of range");
+  sage_status s = check_device();
+  if (s != SAGE_OK) return s;
+  AttnMaps maps;
+  if ((s = make_maps(qt, &maps)) != SAGE_OK) return s;
+  AttnParams p{};
+  p.g = geo_of(qt);
+  p.status = qt->status;
+  p.timeout_ns = kDefaultTimeoutNs;
+  const int64_t hk = hq / (qt->Hq / qt->Hkv);
+  const int64_t q_row0 = (seg * qt->Hq + hq) * qt->q_head_rows + qtile * 128;
+  const int64_t k_row0 = (seg * qt->Hkv + hk) * qt->k_head_rows + ktile * 128;
+  cudaError_t e = launch_debug_qk(maps, p, q_row0, k_row0, out,
+                                  reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "debug qk launch");
+  return ok();
+}
+
+sage_status sage_debug_e4m3(const float* in, uint8_t* out, int64_t n, sage_stream_t stream) {
+  if (n < 0 || (n > 0 && (in == nullptr || out == nullptr)))
+    return fail(SAGE_ERR_INVALID_ARG, "bad buffers");
+  if (n == 0) return ok();
+  sage_status s = check_device();
+  if (s != SAGE_OK) return s;
+  cudaError_t e = launch_debug_e4m3(in, out, n, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "debug e4m3 launch");
+}
+
+void sage_debug_set_fault(int skip_kv_tile, uint64_t timeout_ns) {
+  g_skip_kv_tile.store(skip_kv_tile);
+  g_timeout_ns.store(timeout_ns);
+}
+
+sage_status sage_device_status(const void* ws, sage_stream_t stream) {
+  if (ws == nullptr) return fail(SAGE_ERR_INVALID_ARG, "null workspace");
+  uint32_t word = 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&word, ws, 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+  if (word & kStatusTimeout)
+    return fail(SAGE_ERR_DEVICE_TIMEOUT, "a device-side wait ran out (status 0x%x)", word);
+  if (word & kStatusBadSeqlens)
+    return fail(SAGE_ERR_INVALID_ARG, "cu_seqlens inconsistent with totals/maxima");
+  return ok();
+}
+
+const char* sage_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,61 @@
+// Host-side launch interface of the kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sage_geom.h"
+
+namespace sage {
+
+struct PrologueBuffers {
+  const uint16_t* q;
+  const uint16_t* k;
+  const uint16_t* v;
+  uint16_t* q16;
+  uint16_t* k16;
+  uint8_t* v8;
+  float* s_q;
+  float* s_k;
+  float* s_v;
+  float* k_mean;
+  float* v_inv;
+  void* ksum;        // int64 (fp16 inputs) or double (bf16), [nseg][Hkv][Dp]
+  uint32_t* vmax;    // float bits, [nseg][Hkv][Dp]
+  uint32_t* status;
+};
+
+cudaError_t launch_prologue(const SegGeo& g, const PrologueBuffers& b,
+                            bool vec, cudaStream_t st);
+
+struct AttnParams {
+  SegGeo g;
+  const float* s_q;
+  const float* s_k;
+  const float* s_v;
+  float* out;
+  // output addressing in elements; varlen segments start at cu_q[s]*tok
+  int64_t out_seg_stride, out_head_stride, out_tok_stride;
+  float scale_log2;          // sm_scale * log2(e)
+  int32_t causal;
+  int32_t skip_kv_tile;      // failure-injection hook, -1 = off
+  uint64_t timeout_ns;
+  uint32_t* status;
+};
+
+struct AttnMaps {
+  CUtensorMap q, k, v;
+};
+
+cudaError_t launch_attention(const AttnMaps& maps, const AttnParams& p,
+                             cudaStream_t st);
+
+cudaError_t launch_debug_qk(const AttnMaps& maps, const AttnParams& p,
+                            int64_t q_row0, int64_t k_row0, int32_t* out,
+                            cudaStream_t st);
+
+cudaError_t launch_debug_e4m3(const float* in, uint8_t* out, int64_t n,
+                              cudaStream_t st);
+
+}  // namespace sage

@@ -1,0 +1,265 @@
+"""Thin ctypes binding of libsage.so (the C ABI declared in include/sage.h).
+
+Argument marshalling only: every step of the quantized attention runs in the
+library's CUDA kernels.  torch supplies device memory and the current stream.
+There is no fallback: if the library is missing or cannot load, importing
+this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+F16, BF16 = 0, 1
+HND, NHD = 0, 1
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_TIMEOUT = range(6)
+STATUS_NAMES = ["OK", "INVALID_ARG", "UNSUPPORTED", "WORKSPACE", "CUDA", "DEVICE_TIMEOUT"]
+
+# Every entry point declared in include/sage.h.
+EXPORTS = (
+    "sage_workspace_bytes", "sage_workspace_bytes_varlen", "sage_quant_prologue",
+    "sage_quant_prologue_varlen", "sage_attn_quantized", "sage_attn_fwd",
+    "sage_attn_fwd_varlen", "sage_debug_qk_int32", "sage_debug_e4m3",
+    "sage_debug_set_fault", "sage_device_status", "sage_last_error",
+)
+
+
+class SageError(RuntimeError):
+    def __init__(self, status: int, where: str, reason: str):
+        name = STATUS_NAMES[status] if 0 <= status < len(STATUS_NAMES) else str(status)
+        super().__init__(f"{where}: SAGE_ERR_{name}: {reason}")
+        self.status = status
+
+
+class Quantized(ctypes.Structure):
+    """Mirror of sage_quantized (pointers into the workspace)."""
+    _fields_ = [
+        ("nseg", ctypes.c_int64), ("Hq", ctypes.c_int64), ("Hkv", ctypes.c_int64),
+        ("Lq", ctypes.c_int64), ("Lk", ctypes.c_int64), ("D", ctypes.c_int64),
+        ("Dp", ctypes.c_int64), ("dtype", ctypes.c_int32), ("varlen", ctypes.c_int32),
+        ("total_q", ctypes.c_int64), ("total_k", ctypes.c_int64),
+        ("max_q", ctypes.c_int32), ("max_k", ctypes.c_int32),
+        ("q_head_rows", ctypes.c_int64), ("k_head_rows", ctypes.c_int64),
+        ("q_rows", ctypes.c_int64), ("k_rows", ctypes.c_int64),
+        ("v_rows", ctypes.c_int64), ("v_cols", ctypes.c_int64),
+        ("cu_q", ctypes.c_void_p), ("cu_k", ctypes.c_void_p),
+        ("q16", ctypes.c_void_p), ("k16", ctypes.c_void_p), ("v8", ctypes.c_void_p),
+        ("s_q", ctypes.c_void_p), ("s_k", ctypes.c_void_p), ("s_v", ctypes.c_void_p),
+        ("k_mean", ctypes.c_void_p), ("stats", ctypes.c_void_p),
+        ("status", ctypes.c_void_p),
+    ]
+
+
+def _load():
+    path = _build.LIB
+    if not _build.up_to_date():
+        path = _build.build()
+    lib = ctypes.CDLL(path)
+    P, I64, I, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    F = ctypes.c_float
+    QP = ctypes.POINTER(Quantized)
+    sig = {
+        "sage_workspace_bytes": ([I64] * 6, SZ),
+        "sage_workspace_bytes_varlen": ([I64] * 6, SZ),
+        "sage_quant_prologue": ([P, P, P, I, I, I64, I64, I64, I64, I64, I64, P, SZ, QP, P], I),
+        "sage_quant_prologue_varlen": ([P, P, P, I, P, P, I64, I64, I64, I, I, I64, I64, I64,
+                                        P, SZ, QP, P], I),
+        "sage_attn_quantized": ([QP, P, I, I, F, P], I),
+        "sage_attn_fwd": ([P, P, P, P, I64, I64, I64, I64, I64, I64, I, I, F, I, P, SZ, P], I),
+        "sage_attn_fwd_varlen": ([P, P, P, P, P, P, I64, I64, I64, I, I, I64, I64, I64, I, F,
+                                  I, P, SZ, P], I),
+        "sage_debug_qk_int32": ([QP, I64, I64, I64, I64, P, P], I),
+        "sage_debug_e4m3": ([P, P, I64, P], I),
+        "sage_debug_set_fault": ([I, ctypes.c_uint64], None),
+        "sage_device_status": ([P, P], I),
+        "sage_last_error": ([], ctypes.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+_lib = _load()
+lib = _lib
+
+
+def last_error() -> str:
+    return _lib.sage_last_error().decode()
+
+
+def _check(rc: int, where: str):
+    if rc != OK:
+        raise SageError(rc, where, last_error())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return F16
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"q/k/v must be float16 or bfloat16, got {t.dtype}")
+
+
+def _layout_code(layout) -> int:
+    if layout in (HND, "HND"):
+        return HND
+    if layout in (NHD, "NHD"):
+        return NHD
+    raise ValueError(f"layout must be 'HND' or 'NHD', got {layout!r}")
+
+
+def _dims(q, k, layout):
+    if layout == HND:
+        B, Hq, Lq, D = q.shape
+        _, Hkv, Lk, _ = k.shape
+    else:
+        B, Lq, Hq, D = q.shape
+        _, Lk, Hkv, _ = k.shape
+    return B, Hq, Hkv, Lq, Lk, D
+
+
+def workspace_bytes(B, Hq, Hkv, Lq, Lk, D) -> int:
+    return int(_lib.sage_workspace_bytes(B, Hq, Hkv, Lq, Lk, D))
+
+
+def workspace_bytes_varlen(nseq, total_q, total_k, Hq, Hkv, D) -> int:
+    return int(_lib.sage_workspace_bytes_varlen(nseq, total_q, total_k, Hq, Hkv, D))
+
+
+def alloc_workspace(nbytes: int, device="cuda"):
+    import torch
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def quant_prologue(q, k, v, layout="HND", ws=None, stream=None) -> Quantized:
+    lay = _layout_code(layout)
+    B, Hq, Hkv, Lq, Lk, D = _dims(q, k, lay)
+    if ws is None:
+        ws = alloc_workspace(workspace_bytes(B, Hq, Hkv, Lq, Lk, D), q.device)
+    qt = Quantized()
+    rc = _lib.sage_quant_prologue(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), lay, B, Hq,
+                                  Hkv, Lq, Lk, D, _ptr(ws), ws.numel(), ctypes.byref(qt),
+                                  _stream(stream))
+    _check(rc, "sage_quant_prologue")
+    qt._ws = ws
+    return qt
+
+
+def quant_prologue_varlen(q, k, v, cu_q, cu_k, max_q, max_k, ws=None, stream=None):
+    total_q, Hq, D = q.shape
+    total_k, Hkv, _ = k.shape
+    nseq = cu_q.numel() - 1
+    if ws is None:
+        ws = alloc_workspace(workspace_bytes_varlen(nseq, total_q, total_k, Hq, Hkv, D),
+                             q.device)
+    qt = Quantized()
+    rc = _lib.sage_quant_prologue_varlen(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q),
+                                         _ptr(cu_q), _ptr(cu_k), nseq, total_q, total_k,
+                                         int(max_q), int(max_k), Hq, Hkv, D, _ptr(ws),
+                                         ws.numel(), ctypes.byref(qt), _stream(stream))
+    _check(rc, "sage_quant_prologue_varlen")
+    qt._ws = ws
+    return qt
+
+
+def attn_quantized(qt: Quantized, out, layout="HND", is_causal=False, sm_scale=None,
+                   stream=None):
+    rc = _lib.sage_attn_quantized(ctypes.byref(qt), _ptr(out), _layout_code(layout),
+                                  int(bool(is_causal)), float(sm_scale or 0.0),
+                                  _stream(stream))
+    _check(rc, "sage_attn_quantized")
+    return out
+
+
+def attn_fwd(q, k, v, out, layout="HND", is_causal=False, sm_scale=None, ws=None,
+             stream=None):
+    lay = _layout_code(layout)
+    B, Hq, Hkv, Lq, Lk, D = _dims(q, k, lay)
+    if ws is None:
+        ws = alloc_workspace(workspace_bytes(B, Hq, Hkv, Lq, Lk, D), q.device)
+    rc = _lib.sage_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, Lq, Lk, D,
+                            lay, int(bool(is_causal)), float(sm_scale or 0.0),
+                            _dtype_code(q), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "sage_attn_fwd")
+    return out
+
+
+def attn_fwd_varlen(q, k, v, out, cu_q, cu_k, max_q, max_k, is_causal=False,
+                    sm_scale=None, ws=None, stream=None):
+    total_q, Hq, D = q.shape
+    total_k, Hkv, _ = k.shape
+    nseq = cu_q.numel() - 1
+    if ws is None:
+        ws = alloc_workspace(workspace_bytes_varlen(nseq, total_q, total_k, Hq, Hkv, D),
+                             q.device)
+    rc = _lib.sage_attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(cu_q),
+                                   _ptr(cu_k), nseq, total_q, total_k, int(max_q),
+                                   int(max_k), Hq, Hkv, D, int(bool(is_causal)),
+                                   float(sm_scale or 0.0), _dtype_code(q), _ptr(ws),
+                                   ws.numel(), _stream(stream))
+    _check(rc, "sage_attn_fwd_varlen")
+    return out
+
+
+def sageattn(q, k, v, tensor_layout="HND", is_causal=False, sm_scale=None):
+    """Drop-in style call: fp16/bf16 q, k, v on the GPU -> fp32 output."""
+    import torch
+    out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    return attn_fwd(q, k, v, out, tensor_layout, is_causal, sm_scale)
+
+
+def debug_qk_int32(qt: Quantized, seg, hq, qtile, ktile, out=None, stream=None):
+    import torch
+    if out is None:
+        out = torch.empty(128 * 128, dtype=torch.int32, device="cuda")
+    rc = _lib.sage_debug_qk_int32(ctypes.byref(qt), seg, hq, qtile, ktile, _ptr(out),
+                                  _stream(stream))
+    _check(rc, "sage_debug_qk_int32")
+    return out.view(128, 128)
+
+
+def debug_e4m3(x, out=None, stream=None):
+    import torch
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    rc = _lib.sage_debug_e4m3(_ptr(x), _ptr(out), x.numel(), _stream(stream))
+    _check(rc, "sage_debug_e4m3")
+    return out
+
+
+def set_fault(skip_kv_tile: int = -1, timeout_ns: int = 0):
+    _lib.sage_debug_set_fault(int(skip_kv_tile), int(timeout_ns))
+
+
+def device_status(ws, stream=None) -> int:
+    return int(_lib.sage_device_status(_ptr(ws), _stream(stream)))
+
+
+def ws_view(qt: Quantized, field: str, dtype, shape):
+    """A torch view of one workspace buffer (for tests and inspection)."""
+    import torch
+    ws = qt._ws
+    off = getattr(qt, field) - ws.data_ptr()
+    n = 1
+    for s in shape:
+        n *= s
+    nbytes = n * torch.tensor([], dtype=dtype).element_size()
+    return ws[off:off + nbytes].view(dtype).view(*shape)

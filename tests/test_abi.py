@@ -1,0 +1,108 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side
+validation rejects bad arguments before touching the GPU (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from quantized_attention_smooth_gb300 import sage
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "sage.h")).read()
+    return set(re.findall(r"SAGE_API\s+[\w\s\*]+?\b(sage_\w+)\s*\(", src))
+
+
+def test_header_declares_the_binding_exports():
+    assert _declared() == set(sage.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(sage._build.LIB)
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_workspace_sizes():
+    n = sage.workspace_bytes(2, 24, 24, 4096, 4096, 128)
+    # q16 + k16 (2 B) + v8 (1 B) per padded element dominate
+    assert 2 * 24 * 4096 * 128 * 5 <= n <= 2 * 24 * 4096 * 128 * 5 * 1.05
+    assert sage.workspace_bytes(1, 3, 2, 10, 10, 64) == 0      # Hq % Hkv
+    assert sage.workspace_bytes(1, 2, 2, 10, 10, 0) == 0       # D = 0
+    assert sage.workspace_bytes(1, 2, 2, 10, 10, 129) == 0     # D > 128
+    assert sage.workspace_bytes(1, 2, 2, 100, 100, 40) > 0
+    # padded D: 40 -> 64, 80 -> 128
+    assert (sage.workspace_bytes(1, 2, 2, 128, 128, 40) ==
+            sage.workspace_bytes(1, 2, 2, 128, 128, 64))
+    assert (sage.workspace_bytes(1, 2, 2, 128, 128, 80) ==
+            sage.workspace_bytes(1, 2, 2, 128, 128, 128))
+    assert sage.workspace_bytes_varlen(8, 1000, 1000, 16, 16, 80) > 0
+    assert sage.workspace_bytes_varlen(8, 1000, 1000, 16, 3, 80) == 0
+
+
+FAKE = ctypes.c_void_p(0x10000)   # never dereferenced: validation fails first
+
+
+def _fwd(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, B=1, Hq=2, Hkv=2, Lq=128, Lk=128,
+             D=64, layout=0, causal=0, scale=0.0, dtype=0, ws=FAKE, ws_bytes=1 << 30)
+    a.update(kw)
+    return sage.lib.sage_attn_fwd(a["q"], a["k"], a["v"], a["out"], a["B"], a["Hq"],
+                                  a["Hkv"], a["Lq"], a["Lk"], a["D"], a["layout"],
+                                  a["causal"], a["scale"], a["dtype"], a["ws"],
+                                  a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(D=129), sage.ERR_UNSUPPORTED, "head_dim"),
+    (dict(D=0), sage.ERR_UNSUPPORTED, "head_dim"),
+    (dict(Hq=3, Hkv=2), sage.ERR_INVALID_ARG, "multiple"),
+    (dict(Hkv=0), sage.ERR_INVALID_ARG, "multiple"),
+    (dict(dtype=7), sage.ERR_INVALID_ARG, "dtype"),
+    (dict(layout=5), sage.ERR_INVALID_ARG, "layout"),
+    (dict(q=ctypes.c_void_p(0)), sage.ERR_INVALID_ARG, "non-null"),
+    (dict(k=ctypes.c_void_p(0x10001)), sage.ERR_INVALID_ARG, "aligned"),
+    (dict(out=ctypes.c_void_p(0)), sage.ERR_INVALID_ARG, "out"),
+    (dict(out=ctypes.c_void_p(0x10002)), sage.ERR_INVALID_ARG, "out"),
+    (dict(B=-1), sage.ERR_INVALID_ARG, "negative"),
+    (dict(ws=ctypes.c_void_p(0x10010)), sage.ERR_WORKSPACE, "256-byte"),
+    (dict(ws_bytes=1000), sage.ERR_WORKSPACE, "needs"),
+])
+def test_bad_arguments_are_rejected_on_the_host(kw, status, needle):
+    rc = _fwd(**kw)
+    assert rc == status
+    assert needle in sage.last_error()
+
+
+def test_empty_problem_is_a_no_op():
+    assert _fwd(B=0) == sage.OK
+    assert _fwd(Lq=0) == sage.OK
+    assert sage.last_error() == ""
+
+
+def test_varlen_rejects_bad_arguments():
+    lib = sage.lib
+    rc = lib.sage_attn_fwd_varlen(FAKE, FAKE, FAKE, FAKE, ctypes.c_void_p(0), FAKE, 2, 10,
+                                  10, 5, 5, 2, 2, 64, 0, 0.0, 0, FAKE, 1 << 30, None)
+    assert rc == sage.ERR_INVALID_ARG and "cu_seqlens" in sage.last_error()
+    rc = lib.sage_attn_fwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 10, 10, 5, 5, 2,
+                                  2, 300, 0, 0.0, 0, FAKE, 1 << 30, None)
+    assert rc == sage.ERR_UNSUPPORTED
+    assert lib.sage_attn_fwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, 0, 1, 1, 2, 2,
+                                    64, 0, 0.0, 0, FAKE, 0, None) == sage.OK
+
+
+def test_quantized_call_rejects_unfilled_struct():
+    qt = sage.Quantized()
+    rc = sage.lib.sage_attn_quantized(ctypes.byref(qt), FAKE, 0, 0, 0.0, None)
+    assert rc == sage.ERR_INVALID_ARG
+    rc = sage.lib.sage_debug_qk_int32(ctypes.byref(qt), 0, 0, 0, 0, FAKE, None)
+    assert rc == sage.ERR_INVALID_ARG
+
+
+def test_sage_error_carries_reason():
+    with pytest.raises(sage.SageError, match="head_dim"):
+        sage._check(_fwd(D=200), "sage_attn_fwd")

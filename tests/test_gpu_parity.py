@@ -1,0 +1,271 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+* quantized tensors (int8 codes, e4m3 codes, every scale, the K mean) and the
+  INT32 QK^T tiles: bit-exact;
+* fp32 outputs: max-abs <= 2e-3 against the oracle and cosine >= 0.999
+  against fp64 exact attention, on every row for small shapes and on sampled
+  rows (first, middle and ragged last query tiles of several heads) for the
+  full-size workloads.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from quantized_attention_smooth_gb300 import workloads as wl
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def sage():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantized_attention_smooth_gb300 import sage as s
+    return s
+
+
+def _small(name, **kw):
+    base = dict(B=1, Hq=2, Hkv=2, Lq=256, Lk=256, D=64, dtype=wl.F16, layout=wl.HND,
+                causal=False, seed=77, k_offset_sigma=2.0)
+    base.update(kw)
+    return wl.Workload(name, **base)
+
+
+SMALL = [
+    wl.WORKLOADS["small_d64"],
+    _small("d128_ragged", Lq=300, Lk=333, D=128, seed=1),
+    _small("d1", D=1, Lq=130, Lk=129, seed=2),
+    _small("d16", D=16, seed=3),
+    _small("d40", D=40, Lq=200, Lk=200, seed=4, k_outliers=(3, 17), k_outlier_value=20.0),
+    _small("d65", D=65, seed=5),
+    _small("d80", D=80, Lq=129, Lk=257, seed=6, dtype=wl.BF16),
+    _small("d100_odd", D=100, Lq=77, Lk=391, seed=7),
+    _small("d127", D=127, seed=8),
+    _small("lk1", Lq=64, Lk=1, seed=9),
+    _small("lq1", Lq=1, Lk=700, seed=10, D=128),
+    _small("cross_lq_gt_lk", Lq=600, Lk=150, seed=11, D=128),
+    _small("causal_square", Lq=384, Lk=384, causal=True, seed=12, D=128),
+    _small("causal_lq_gt_lk", Lq=500, Lk=260, causal=True, seed=13, D=128, dtype=wl.BF16),
+    _small("causal_lq_lt_lk", Lq=200, Lk=450, causal=True, seed=14, D=64),
+    _small("gqa_nhd", B=2, Hq=8, Hkv=2, Lq=200, Lk=300, D=128, layout=wl.NHD, seed=15,
+           dtype=wl.BF16, k_outliers=(7, 42), k_outlier_value=15.0, k_offset_sigma=0.0),
+    _small("gqa_causal_nhd", B=2, Hq=4, Hkv=1, Lq=256, Lk=256, D=128, layout=wl.NHD,
+           causal=True, seed=16),
+    _small("batch3_hnd", B=3, Hq=3, Hkv=3, Lq=140, Lk=140, D=96, seed=17),
+    _small("varlen_small", B=0, Hq=4, Hkv=2, Lq=0, Lk=0, D=80, layout=wl.NHD, seed=18,
+           seqlens_q=(1, 130, 257, 128), seqlens_k=(5, 128, 300, 1)),
+    _small("varlen_causal", B=0, Hq=2, Hkv=2, Lq=0, Lk=0, D=40, layout=wl.NHD, seed=19,
+           causal=True, seqlens_q=(200, 64, 333), seqlens_k=(200, 64, 333)),
+]
+
+
+def _check_prologue(sage, orc, w, inp, d):
+    qt = H.run_prologue(sage, w, d)
+    torch.cuda.synchronize()
+    ws = H.Workspace(sage, qt, w, inp)
+    bad = {}
+    for s in range(w.nseg):
+        q, k, v = wl.segment(w, inp, s)
+        ref = orc.prologue(q, k, v, w.dtype)
+        got = ws.segment(s)
+        mism = H.compare_prologue(ref, got, w.D)
+        if any(mism.values()):
+            bad[s] = mism
+        assert ws.padding_is_zero(s), f"segment {s}: padding not zeroed"
+    assert not bad, f"bit mismatches per segment: {bad}"
+    assert sage.device_status(qt._ws) == sage.OK
+    return qt, ws
+
+
+def _check_rows(orc, w, inp, out_np, samples):
+    """samples: list of (segment, (h0, h1), (r0, r1))."""
+    worst, cos_min = 0.0, 1.0
+    pros = {}
+    for s, heads, rows in samples:
+        q, k, v = wl.segment(w, inp, s)
+        if s not in pros:
+            pros[s] = orc.prologue(q, k, v, w.dtype)
+        scale = wl.default_sm_scale(w)
+        ref = orc.attn(pros[s], w.causal, scale, heads=heads, rows=rows)
+        ex = orc.attn_exact(q, k, v, w.dtype, w.causal, scale, heads=heads, rows=rows)
+        got = wl.out_segment(w, out_np, s, inp.get("cu_q"))
+        sl = (slice(*heads), slice(*rows))
+        g, r, e = got[sl], ref[sl], ex[sl]
+        assert np.all(np.isfinite(g)), f"non-finite output in segment {s}"
+        worst = max(worst, float(np.max(np.abs(g.astype(np.float64) - r))))
+        if np.linalg.norm(e) > 0:
+            cos_min = min(cos_min, H.cosine(g, e))
+    return worst, cos_min
+
+
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+def test_small_shapes_bit_exact_and_all_rows(sage, orc, w):
+    inp = wl.make_inputs(w)
+    d = H.device_inputs(w, inp)
+    _check_prologue(sage, orc, w, inp, d)
+    out = H.run_attention(sage, w, d).cpu().numpy()
+    samples = []
+    for s, (lq, lk) in enumerate(w.seg_lengths()):
+        if lq > 0:
+            samples.append((s, (0, w.Hq), (0, lq)))
+    worst, cmin = _check_rows(orc, w, inp, out, samples)
+    assert worst <= H.ATOL_ORACLE, worst
+    assert cmin >= H.COS_EXACT, cmin
+
+
+FULL = ["small_d64", "b2_h24_l4096_d128", "gqa_causal_b4_l8192", "dit_self_l32768",
+        "dit_cross_l32768x512", "varlen_d80", "varlen_d40"]
+
+
+def _samples(w):
+    out = []
+    for s, (lq, lk) in enumerate(w.seg_lengths()):
+        if s not in (0, w.nseg - 1) and w.nseg > 2 and not w.varlen:
+            continue
+        last = max(0, lq - 200)
+        mid = max(0, (lq // 2) // 128 * 128)
+        for h in sorted({0, w.Hq - 1}):
+            for r0 in sorted({0, mid, last}):
+                out.append((s, (h, h + 1), (r0, min(lq, r0 + 200))))
+    return out
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workloads(sage, orc, name):
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w)
+    d = H.device_inputs(w, inp)
+    _check_prologue(sage, orc, w, inp, d)
+    ws = H.workspace_for(sage, w)
+    out = H.run_attention(sage, w, d, ws=ws)
+    assert sage.device_status(ws) == sage.OK
+    out_np = out.cpu().numpy()
+    worst, cmin = _check_rows(orc, w, inp, out_np, _samples(w))
+    assert worst <= H.ATOL_ORACLE, worst
+    assert cmin >= H.COS_EXACT, cmin
+    # property that holds at any size: every written output is finite
+    assert bool(torch.isfinite(out).all())
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_qk_int32_tiles_bit_exact(sage, orc, D):
+    w = _small("tiles", B=2, Hq=4, Hkv=2, Lq=300, Lk=520, D=D, seed=40 + D)
+    inp = wl.make_inputs(w)
+    d = H.device_inputs(w, inp)
+    qt, ws = _check_prologue(sage, orc, w, inp, d)
+    for s in range(2):
+        q, k, v = wl.segment(w, inp, s)
+        ref = orc.prologue(q, k, v, w.dtype)
+        for hq in (0, 3):
+            hk = hq // 2
+            for qtile, ktile in ((0, 0), (2, 4), (1, 3)):
+                tile = sage.debug_qk_int32(qt, s, hq, qtile, ktile).cpu().numpy()
+                qa = np.zeros((128, ref["q8"].shape[-1]), np.int64)
+                ka = np.zeros((128, ref["k8"].shape[-1]), np.int64)
+                qrows = ref["q8"][hq, qtile * 128:(qtile + 1) * 128]
+                krows = ref["k8"][hk, ktile * 128:(ktile + 1) * 128]
+                qa[:len(qrows)] = qrows
+                ka[:len(krows)] = krows
+                np.testing.assert_array_equal(tile, (qa @ ka.T).astype(np.int32))
+
+
+def test_qk_int32_extreme_codes_exact(sage):
+    """All codes +-127 along D=128: row sums reach 2,064,512 and stay exact."""
+    Lq = Lk = 128
+    q = torch.full((1, 1, Lq, 128), 1.0, dtype=torch.float16, device="cuda")
+    q[0, 0, ::2] = -1.0
+    k = torch.full((1, 1, Lk, 128), 1.0, dtype=torch.float16, device="cuda")
+    k[0, 0, :, 1::3] = -1.0
+    k[0, 0, :64] *= 3.0        # smoothing leaves +-c patterns; amax maps to 127
+    v = torch.randn(1, 1, Lk, 128, dtype=torch.float16, device="cuda")
+    qt = sage.quant_prologue(q, k, v, "HND")
+    tile = sage.debug_qk_int32(qt, 0, 0, 0, 0).cpu().numpy().astype(np.int64)
+    q8 = sage.ws_view(qt, "q16", torch.float16, (128, 128)).float().cpu().numpy()
+    k8 = sage.ws_view(qt, "k16", torch.float16, (128, 128)).float().cpu().numpy()
+    ref = q8.astype(np.int64) @ k8.astype(np.int64).T
+    np.testing.assert_array_equal(tile, ref)
+    assert np.abs(ref).max() > 1_000_000
+
+
+def test_e4m3_conversion_matches_oracle_on_all_floats(sage, orc):
+    """The kernel's fp32 -> e4m3 conversion over every fp32 bit pattern."""
+    chunk = 1 << 28
+    for c in range((1 << 32) // chunk):
+        bits = np.arange(chunk, dtype=np.uint32) + np.uint32(c * chunk)
+        x = bits.view(np.float32)
+        gpu = sage.debug_e4m3(torch.from_numpy(x.view(np.int32)).cuda().view(torch.float32))
+        g = gpu.cpu().numpy()
+        ref = orc.e4m3_encode(x)
+        nan = np.isnan(x)
+        assert np.all((g[nan] & 0x7F) == 0x7F), "NaN must stay NaN"
+        diff = np.nonzero((g != ref) & ~nan)[0]
+        assert diff.size == 0, (f"chunk {c}: {diff.size} mismatches, first input "
+                                f"{x[diff[0]]!r} bits {bits[diff[0]]:#x}: gpu {g[diff[0]]:#x} "
+                                f"oracle {ref[diff[0]]:#x}")
+
+
+def test_large_magnitude_causal_inputs_stay_finite(sage, orc):
+    w = _small("huge", Lq=512, Lk=512, D=128, causal=True, seed=50, dtype=wl.BF16)
+    inp = wl.make_inputs(w)
+    scale = np.float32(300.0)
+    for key in ("q", "k"):
+        inp[key] = wl.to_bits(wl.bits_to_float(inp[key], w.dtype) * scale, w.dtype)
+    d = H.device_inputs(w, inp)
+    out = H.run_attention(sage, w, d)
+    assert bool(torch.isfinite(out).all())
+    worst, cmin = _check_rows(orc, w, inp, out.cpu().numpy(), [(0, (0, 2), (0, 512))])
+    assert worst <= H.ATOL_ORACLE
+
+
+def test_prologue_is_deterministic(sage):
+    w = wl.WORKLOADS["gqa_causal_b4_l8192"].replace(B=1, Lq=1000, Lk=1000)
+    inp = wl.make_inputs(w)
+    d = H.device_inputs(w, inp)
+    a = H.run_prologue(sage, w, d)
+    wa = a._ws.clone()
+    b = H.run_prologue(sage, w, d)
+    assert torch.equal(wa, b._ws)
+
+
+def test_quantized_entry_points_match_fused_call(sage):
+    w = _small("split", B=2, Hq=4, Hkv=2, Lq=300, Lk=400, D=128, layout=wl.NHD, seed=60,
+               causal=True)
+    inp = wl.make_inputs(w)
+    d = H.device_inputs(w, inp)
+    fused = H.run_attention(sage, w, d)
+    qt = sage.quant_prologue(d["q"], d["k"], d["v"], "NHD")
+    out = torch.empty_like(fused)
+    sage.attn_quantized(qt, out, "NHD", True, wl.default_sm_scale(w))
+    assert torch.equal(out, fused)
+
+
+def test_default_scale_is_inverse_sqrt_d(sage):
+    w = _small("scale", D=80, seed=61)
+    inp = wl.make_inputs(w)
+    d = H.device_inputs(w, inp)
+    a = torch.empty(d["q"].shape, dtype=torch.float32, device="cuda")
+    b = torch.empty_like(a)
+    sage.attn_fwd(d["q"], d["k"], d["v"], a, "HND", False, None)
+    sage.attn_fwd(d["q"], d["k"], d["v"], b, "HND", False, float(np.float32(1) / np.sqrt(np.float32(80))))
+    assert torch.equal(a, b)
+
+
+def test_empty_keys_give_zeros(sage):
+    q = torch.randn(1, 2, 10, 64, dtype=torch.float16, device="cuda")
+    k = torch.randn(1, 2, 0, 64, dtype=torch.float16, device="cuda")
+    out = torch.full((1, 2, 10, 64), 7.0, device="cuda")
+    sage.attn_fwd(q, k, k, out, "HND")
+    assert bool((out == 0).all())
+
+
+def test_inconsistent_cu_seqlens_reported(sage):
+    q = torch.randn(300, 2, 64, dtype=torch.float16, device="cuda")
+    cu = torch.tensor([0, 200, 100], dtype=torch.int32, device="cuda")   # not monotonic
+    out = torch.zeros(300, 2, 64, device="cuda")
+    ws = sage.alloc_workspace(sage.workspace_bytes_varlen(2, 300, 300, 2, 2, 64))
+    sage.attn_fwd_varlen(q, q, q, out, cu, cu, 200, 200, ws=ws)
+    assert sage.device_status(ws) == sage.ERR_INVALID_ARG
