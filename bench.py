@@ -1,0 +1,367 @@
+"""Benchmark of the smoothed INT8/FP8 quantized attention forward on GB300.
+
+One step = the whole hot path over one batch: the quantisation prologue
+(K smoothing, INT8 Q/K, FP8 V) followed by the fused attention kernel, for
+the workload B=2, H=24, L=4096, D=128, fp16, HND, non-causal (the shape of the
+pages' RTX 5070 measurement).  Inputs are seeded synthetic tensors already
+resident in HBM; L2 is flushed (256 MiB write) between timed steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--workload NAME]
+
+Prints one JSON line.  `--impl reference` times the plain CPU oracle (the
+reference arm) on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from quantized_attention_smooth_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "attention TOPS (4*B*H*Lq*Lk*D / device time)"
+DEFAULT_WORKLOAD = "b2_h24_l4096_d128"
+L2_FLUSH_BYTES = 256 << 20
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM bytes per attention-kernel launch from the ncu capture summarised in
+# profiles/ (None until a capture of the current kernel exists).
+ATTN_NCU_DRAM_BYTES = None
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_ops(w: wl.Workload, dim=None) -> float:
+    return w.ops(dim=dim)
+
+
+def prologue_bytes(w: wl.Workload) -> float:
+    """Algorithmic HBM bytes of the prologue: read q, k, v (2 B each); write
+    the fp16 code copies of Q and K (2 B each) and the e4m3 V (1 B) per padded
+    element; the second pass over K and V is an L2 re-read and counts 0."""
+    Dp = 64 if w.D <= 64 else 128
+    nq = nk = 0
+    for lq, lk in w.seg_lengths():
+        nq += lq
+        nk += lk
+    read = 2 * w.D * (nq * w.Hq + 2 * nk * w.Hkv)
+    write = Dp * (2 * nq * w.Hq + 3 * nk * w.Hkv)
+    scales = 4 * (nq * w.Hq + nk * w.Hkv // 128 + 2 * w.Hkv * Dp * w.nseg)
+    return float(read + write + scales)
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- GPU arm
+def to_device(torch, bits, dtype):
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch.float16 if dtype == wl.F16 else torch.bfloat16)
+
+
+def run_gpu(args, w: wl.Workload, rank: int, world: int):
+    import torch
+    import torch.distributed as dist
+    from quantized_attention_smooth_gb300 import sage
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    inp = wl.make_inputs(w)
+    host = {k: to_device(torch, inp[k], w.dtype).pin_memory() for k in ("q", "k", "v")}
+    d = {k: host[k].to(dev) for k in host}
+    if w.varlen:
+        d["cu_q"] = torch.from_numpy(inp["cu_q"]).to(dev)
+        d["cu_k"] = torch.from_numpy(inp["cu_k"]).to(dev)
+        nbytes = sage.workspace_bytes_varlen(w.nseg, sum(w.seqlens_q), sum(w.seqlens_k),
+                                             w.Hq, w.Hkv, w.D)
+    else:
+        nbytes = sage.workspace_bytes(w.B, w.Hq, w.Hkv, w.Lq, w.Lk, w.D)
+    ws = sage.alloc_workspace(nbytes, dev)
+    out = torch.empty(d["q"].shape, dtype=torch.float32, device=dev)
+    out_host = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    scale = wl.default_sm_scale(w)
+
+    def fwd():
+        if w.varlen:
+            sage.attn_fwd_varlen(d["q"], d["k"], d["v"], out, d["cu_q"], d["cu_k"],
+                                 max(w.seqlens_q), max(w.seqlens_k), w.causal, scale, ws=ws)
+        else:
+            sage.attn_fwd(d["q"], d["k"], d["v"], out, w.layout, w.causal, scale, ws=ws)
+
+    def prologue():
+        if w.varlen:
+            return sage.quant_prologue_varlen(d["q"], d["k"], d["v"], d["cu_q"], d["cu_k"],
+                                              max(w.seqlens_q), max(w.seqlens_k), ws=ws)
+        return sage.quant_prologue(d["q"], d["k"], d["v"], w.layout, ws=ws)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        fwd()
+        flush.zero_()
+    torch.cuda.synchronize()
+    assert sage.device_status(ws) == sage.OK, sage.last_error()
+
+    # ---- timed region: whole step (prologue + attention), device events
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    t_end = time.perf_counter() + 0.4          # keep the GPU busy while the sampler starts
+    while time.perf_counter() < t_end:
+        fwd()
+        flush.zero_()
+        torch.cuda.synchronize()
+    barrier()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+    barrier()
+    clock_info = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    assert sage.device_status(ws) == sage.OK, sage.last_error()
+
+    # ---- per-kernel split: prologue alone and attention kernel alone
+    qt = prologue()
+    pro_ev, att_ev = [], []
+    for i in range(max(10, args.steps)):
+        flush.zero_()
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record(stream)
+        qt = prologue()
+        b.record(stream)
+        sage.attn_quantized(qt, out, w.layout, w.causal, scale)
+        c.record(stream)
+        pro_ev.append((a, b))
+        att_ev.append((b, c))
+    torch.cuda.synchronize()
+    pro_ms = statistics.mean(a.elapsed_time(b) for a, b in pro_ev)
+    att_ms = statistics.mean(a.elapsed_time(b) for a, b in att_ev)
+
+    # ---- end to end: host buffers, copies inside the timed region
+    e2e_ev = []
+    for i in range(max(5, min(args.steps, 50))):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k in ("q", "k", "v"):
+            d[k].copy_(host[k], non_blocking=True)
+        fwd()
+        out_host.copy_(out, non_blocking=True)
+        b.record(stream)
+        e2e_ev.append((a, b))
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in ("q", "k", "v"))
+    d2h = out_host.numel() * 4
+
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ops = workload_ops(w)
+    Dp = 64 if w.D <= 64 else 128
+    return dict(total_ms=total_ms, step_ms=step_ms, pro_ms=pro_ms, att_ms=att_ms,
+                e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, ops=ops, ops_padded=workload_ops(w, Dp),
+                clocks=clock_info)
+
+
+# ---------------------------------------------------------- CPU oracle arm
+def oracle_sample(w: wl.Workload, inp: dict, rows: int, heads: int = 1):
+    """Times the oracle (prologue + attention) on `heads` query heads of segment 0
+    and its first `rows` query rows; returns (ops, seconds, threads)."""
+    import oracle
+    q, k, v = wl.segment(w, inp, 0)
+    # query head 0 reads kv head 0 for every GQA grouping
+    qs = np.ascontiguousarray(q[:1])
+    ks = np.ascontiguousarray(k[:1])
+    vs = np.ascontiguousarray(v[:1])
+    lq, lk = w.seg_lengths()[0]
+    rows = min(rows, lq)
+    t0 = time.perf_counter()
+    pro = oracle.prologue(qs, ks, vs, w.dtype)
+    oracle.attn(pro, w.causal, wl.default_sm_scale(w), rows=(0, rows))
+    dt = time.perf_counter() - t0
+    if w.causal:
+        pairs = sum(min(i + 1, lk) for i in range(rows))
+    else:
+        pairs = rows * lk
+    ops = 4.0 * qs.shape[0] * pairs * w.D
+    return ops, dt, os.cpu_count()
+
+
+def reference_arm(args, w: wl.Workload, rank: int, world: int):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    inp = wl.make_inputs(w)
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_sample(w, inp, min(rows, 128))
+    tot_ops, tot_s = 0.0, 0.0
+    for _ in range(args.steps):
+        ops, dt, cores = oracle_sample(w, inp, rows)
+        tot_ops += ops
+        tot_s += dt
+    tops = tot_ops / tot_s / 1e12
+    sample = (f"segment 0, query head 0, rows [0,{rows}) of {w.name}: prologue of that "
+              f"head plus attention, per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tops, "unit": "TOPS",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_s / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8+e4m3 (fp32 softmax)",
+        "data": "synthetic", "config": config_of(w),
+        "cpu_baseline": {"value": tops, "unit": "TOPS", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": tops, "unit": "TOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w: wl.Workload) -> dict:
+    c = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Lq": w.Lq, "Lk": w.Lk,
+         "D": w.D, "input_dtype": "fp16" if w.dtype == wl.F16 else "bf16",
+         "layout": "HND" if w.layout == wl.HND else "NHD", "causal": w.causal,
+         "l2": "flushed between timed steps (256 MiB write)"}
+    if w.varlen:
+        c["seqlens"] = list(w.seqlens_q)
+    return c
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="sage", choices=["sage", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--ref-rows", type=int, default=512)
+    ap.add_argument("--cpu-rows", type=int, default=4096)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    w = wl.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        reference_arm(args, w, rank, world)
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    r = run_gpu(args, w, rank, world)
+    if rank != 0:
+        return
+    peaks, src = load_peaks()
+    # attention kernel roofline: QK^T on the 16-bit tensor pipe (exact int8
+    # emulation) and PV on the FP8 pipe (2x rate) => ceiling 4/3 x bf16 peak
+    bf16 = peaks["bf16_tflops"]
+    mix_peak = bf16 * 4.0 / 3.0
+    fp8_peak = bf16 * 2.0
+    att_tflops = r["ops_padded"] / (r["att_ms"] * 1e-3) / 1e12
+    tops = r["ops"] * world * args.steps / (r["total_ms"] * 1e-3) / 1e12
+    pro_gbs = prologue_bytes(w) / (r["pro_ms"] * 1e-3) / 1e9
+    inp = wl.make_inputs(w)
+    cpu_ops, cpu_s, cores = oracle_sample(w, inp, args.cpu_rows)
+    line = {
+        "metric": METRIC, "value": tops, "unit": "TOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": r["total_ms"] / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8+e4m3 (fp32 softmax/accumulate)", "data": "synthetic",
+        "config": config_of(w),
+        "roofline": {"bound": "tensor", "achieved": att_tflops, "peak": mix_peak,
+                     "unit": "TFLOP/s", "frac": att_tflops / mix_peak,
+                     "traffic": ATTN_NCU_DRAM_BYTES,
+                     "kernel": "attn_kernel (fused QK^T/softmax/PV)",
+                     "peak_note": f"4/3 x {src} bf16 burst {bf16} (QK^T at the 16-bit "
+                                  "rate, PV at the FP8 rate)",
+                     "fp8_peak": fp8_peak, "frac_of_fp8_peak": att_tflops / fp8_peak},
+        "attention_ms": r["att_ms"], "attention_tops": att_tflops,
+        "prologue_ms": r["pro_ms"], "prologue_gbs": pro_gbs,
+        "prologue_hbm_frac": pro_gbs / peaks["hbm_gbs"],
+        "e2e": {"value": r["ops"] / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TOPS",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": 5 * args.steps,
+        "clocks": r["clocks"],
+        "cpu_baseline": {"value": cpu_ops / cpu_s / 1e12, "unit": "TOPS", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"segment 0, query head 0, rows [0,{args.cpu_rows}): "
+                                   "prologue of that head plus attention"},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -7,8 +7,6 @@
   rows (first, middle and ragged last query tiles of several heads) for the
   full-size workloads.
 """
-import math
-
 import numpy as np
 import pytest
 
@@ -68,9 +66,11 @@ def _check_prologue(sage, orc, w, inp, d):
     torch.cuda.synchronize()
     ws = H.Workspace(sage, qt, w, inp)
     bad = {}
+    ws.oracle = {}
     for s in range(w.nseg):
         q, k, v = wl.segment(w, inp, s)
         ref = orc.prologue(q, k, v, w.dtype)
+        ws.oracle[s] = ref
         got = ws.segment(s)
         mism = H.compare_prologue(ref, got, w.D)
         if any(mism.values()):
@@ -81,10 +81,10 @@ def _check_prologue(sage, orc, w, inp, d):
     return qt, ws
 
 
-def _check_rows(orc, w, inp, out_np, samples):
+def _check_rows(orc, w, inp, out_np, samples, pros=None):
     """samples: list of (segment, (h0, h1), (r0, r1))."""
     worst, cos_min = 0.0, 1.0
-    pros = {}
+    pros = {} if pros is None else pros
     for s, heads, rows in samples:
         q, k, v = wl.segment(w, inp, s)
         if s not in pros:
@@ -106,13 +106,13 @@ def _check_rows(orc, w, inp, out_np, samples):
 def test_small_shapes_bit_exact_and_all_rows(sage, orc, w):
     inp = wl.make_inputs(w)
     d = H.device_inputs(w, inp)
-    _check_prologue(sage, orc, w, inp, d)
+    _, ws = _check_prologue(sage, orc, w, inp, d)
     out = H.run_attention(sage, w, d).cpu().numpy()
     samples = []
     for s, (lq, lk) in enumerate(w.seg_lengths()):
         if lq > 0:
             samples.append((s, (0, w.Hq), (0, lq)))
-    worst, cmin = _check_rows(orc, w, inp, out, samples)
+    worst, cmin = _check_rows(orc, w, inp, out, samples, ws.oracle)
     assert worst <= H.ATOL_ORACLE, worst
     assert cmin >= H.COS_EXACT, cmin
 
@@ -139,12 +139,12 @@ def test_full_size_workloads(sage, orc, name):
     w = wl.WORKLOADS[name]
     inp = wl.make_inputs(w)
     d = H.device_inputs(w, inp)
-    _check_prologue(sage, orc, w, inp, d)
+    _, wsh = _check_prologue(sage, orc, w, inp, d)
     ws = H.workspace_for(sage, w)
     out = H.run_attention(sage, w, d, ws=ws)
     assert sage.device_status(ws) == sage.OK
     out_np = out.cpu().numpy()
-    worst, cmin = _check_rows(orc, w, inp, out_np, _samples(w))
+    worst, cmin = _check_rows(orc, w, inp, out_np, _samples(w), wsh.oracle)
     assert worst <= H.ATOL_ORACLE, worst
     assert cmin >= H.COS_EXACT, cmin
     # property that holds at any size: every written output is finite
@@ -174,21 +174,25 @@ def test_qk_int32_tiles_bit_exact(sage, orc, D):
 
 
 def test_qk_int32_extreme_codes_exact(sage):
-    """All codes +-127 along D=128: row sums reach 2,064,512 and stay exact."""
-    Lq = Lk = 128
-    q = torch.full((1, 1, Lq, 128), 1.0, dtype=torch.float16, device="cuda")
-    q[0, 0, ::2] = -1.0
-    k = torch.full((1, 1, Lk, 128), 1.0, dtype=torch.float16, device="cuda")
-    k[0, 0, :, 1::3] = -1.0
-    k[0, 0, :64] *= 3.0        # smoothing leaves +-c patterns; amax maps to 127
-    v = torch.randn(1, 1, Lk, 128, dtype=torch.float16, device="cuda")
+    """All codes +-127 along D=128 with matching sign rows: |S| reaches
+    128 * 127^2 = 2,064,512 and stays exact in the fp32 accumulator."""
+    rng = np.random.default_rng(5)
+    # +-1 keys with every channel balanced over the 128 tokens: the channel
+    # mean is exactly 0, smoothing leaves +-1 and every code is +-127
+    signs = np.ones((128, 128), np.float32)
+    for c in range(128):
+        signs[rng.permutation(128)[:64], c] = -1.0
+    k = torch.from_numpy(signs).to(torch.float16).cuda().view(1, 1, 128, 128)
+    q = k.clone()                               # row i of Q equals key i
+    v = torch.randn(1, 1, 128, 128, dtype=torch.float16, device="cuda")
     qt = sage.quant_prologue(q, k, v, "HND")
     tile = sage.debug_qk_int32(qt, 0, 0, 0, 0).cpu().numpy().astype(np.int64)
     q8 = sage.ws_view(qt, "q16", torch.float16, (128, 128)).float().cpu().numpy()
     k8 = sage.ws_view(qt, "k16", torch.float16, (128, 128)).float().cpu().numpy()
+    assert np.all(np.abs(q8) == 127) and np.all(np.abs(k8) == 127)
     ref = q8.astype(np.int64) @ k8.astype(np.int64).T
     np.testing.assert_array_equal(tile, ref)
-    assert np.abs(ref).max() > 1_000_000
+    assert np.abs(ref).max() == 128 * 127 * 127
 
 
 def test_e4m3_conversion_matches_oracle_on_all_floats(sage, orc):
