@@ -184,6 +184,29 @@ SAGE_API void sage_debug_set_fault(int skip_kv_tile, uint64_t timeout_ns);
  * clears it; the kernels only set bits. */
 SAGE_API sage_status sage_device_status(const void* ws, sage_stream_t stream);
 
+/* Allocation-free smoothing statistics (the pages have no counterpart: an
+ * addition of this library).  For callers that may not allocate device
+ * memory at all, not even a workspace: code running inside a host framework
+ * that owns every device allocation and forbids its extensions to allocate,
+ * or a latency-critical loop that cannot afford cudaMalloc's implicit device
+ * synchronisation and unbounded cost.  Computes, for a dense K and V (HND
+ * or NHD, fp16/bf16), the same per-channel K token mean and V scale
+ * (max |v| / 448) as sage_quant_prologue, into caller-owned k_mean and s_v,
+ * each [B][Hkv][Dp] fp32 (Dp = 64 if D <= 64 else 128; padded channels 0).
+ * Its scratch accumulators live in one static device array inside the
+ * library, sized for B*Hkv*Dp <= 16384 channel slots (about 256 KB, held by
+ * every GPU that loads the library until the process exits); larger
+ * problems return SAGE_ERR_UNSUPPORTED.  The first call on each device looks
+ * up the array's device address (a one-time set-up); make that first call
+ * before any stream capture.  Every call clears and reuses the same array,
+ * so calls that overlap on the GPU (other streams, other host threads)
+ * race and must be serialised by the caller.  It calls no cudaMalloc or
+ * cudaFree. */
+SAGE_API sage_status sage_kv_stats_noalloc(const void* k, const void* v, int dtype,
+                                           int layout, int64_t B, int64_t Hkv,
+                                           int64_t Lk, int64_t D, float* k_mean,
+                                           float* s_v, sage_stream_t stream);
+
 /* Reason of the last failure on this thread ("" if none). */
 SAGE_API const char* sage_last_error(void);
 

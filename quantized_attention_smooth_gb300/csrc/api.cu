@@ -501,6 +501,34 @@ sage_status sage_device_status(const void* ws, sage_stream_t stream) {
   return ok();
 }
 
+sage_status sage_kv_stats_noalloc(const void* k, const void* v, int dtype, int layout,
+                                  int64_t B, int64_t Hkv, int64_t Lk, int64_t D,
+                                  float* k_mean, float* s_v, sage_stream_t stream) {
+  sage_status s = SAGE_OK;
+  if (layout != SAGE_HND && layout != SAGE_NHD)
+    return fail(SAGE_ERR_INVALID_ARG, "layout %d is neither SAGE_HND nor SAGE_NHD", layout);
+  if (!check_dims(Hkv, Hkv, D, &s)) return s;
+  if ((s = check_common(k, k, v, dtype)) != SAGE_OK) return s;
+  if (B < 1 || Lk < 1)
+    return fail(SAGE_ERR_INVALID_ARG, "B and Lk must be positive (B=%lld Lk=%lld)",
+                (long long)B, (long long)Lk);
+  if (k_mean == nullptr || s_v == nullptr || !aligned(k_mean, 4) || !aligned(s_v, 4))
+    return fail(SAGE_ERR_INVALID_ARG, "k_mean and s_v must be 4-byte aligned device pointers");
+  const int64_t entries = B * Hkv * padded_dim(D);
+  if (entries > kStaticStatEntries)
+    return fail(SAGE_ERR_UNSUPPORTED,
+                "B*Hkv*Dp = %lld exceeds the %lld channel slots of the static scratch",
+                (long long)entries, (long long)kStaticStatEntries);
+  if ((s = check_device()) != SAGE_OK) return s;
+  const SegGeo g = dense_geo(B, Hkv, Hkv, 1, Lk, D, dtype, layout);
+  const bool vec = (D % 8 == 0) && aligned(k, 16) && aligned(v, 16);
+  cudaError_t e = launch_kv_stats_static(g, static_cast<const uint16_t*>(k),
+                                         static_cast<const uint16_t*>(v), k_mean, s_v, vec,
+                                         reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "static-scratch statistics");
+  return ok();
+}
+
 const char* sage_last_error(void) { return g_last_error.c_str(); }
 
 }  // extern "C"

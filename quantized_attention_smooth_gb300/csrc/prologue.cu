@@ -29,6 +29,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "sage_device.cuh"
 #include "sage_geom.h"
 #include "sage_kernels.h"
@@ -363,6 +365,76 @@ cudaError_t launch_prologue(const SegGeo& g, const PrologueBuffers& b,
                        : launch_prologue_t<true, false>(g, b, st);
   return bf16 ? launch_prologue_t<false, true>(g, b, st)
               : launch_prologue_t<false, false>(g, b, st);
+}
+
+// ------------------------------------------- statistics without allocation
+// Scratch of the allocation-free statistics entry point: the status word,
+// then per-channel K sums (8 B), V maxima (4 B) and V multipliers (4 B) for
+// at most kStaticStatEntries (segment, kv head, channel) triples.  It lives
+// in the module image, so every device that loads this library holds it
+// until the process exits; concurrent calls share it.
+namespace {
+constexpr size_t kStaticHeader = 256;
+__device__ __align__(256) unsigned char g_stats_scratch[
+    kStaticHeader + kStaticStatEntries * (8 + 4 + 4)];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+template <bool kVec, bool kBf16>
+void launch_stats_only(const SegGeo& g, const uint16_t* k, const uint16_t* v,
+                       void* ksum, uint32_t* vmax, float* k_mean, float* s_v,
+                       float* v_inv, uint32_t* status, cudaStream_t st) {
+  if (g.Lk > 0) {
+    dim3 gs(static_cast<unsigned>((g.Lk + kStatsChunk - 1) / kStatsChunk),
+            static_cast<unsigned>(g.Hkv), static_cast<unsigned>(g.nseg));
+    kv_stats_kernel<kVec, kBf16><<<gs, kThreads, 0, st>>>(g, k, v, ksum, vmax, status);
+  }
+  const int64_t nstat = g.nseg * g.Hkv * g.Dp;
+  kv_finalize_kernel<<<static_cast<unsigned>((nstat + 255) / 256), 256, 0, st>>>(
+      g, ksum, vmax, k_mean, s_v, v_inv);
+}
+}  // namespace
+
+cudaError_t launch_kv_stats_static(const SegGeo& g, const uint16_t* k,
+                                   const uint16_t* v, float* k_mean, float* s_v,
+                                   bool vec, cudaStream_t st) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  unsigned char* base = nullptr;
+  {
+    // one-time set-up per device, with that device current: the host-side
+    // name of the array is not a device address, so look the address up
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_stats_scratch);
+      if (e != cudaSuccess) return e;
+      g_scratch_addr[dev] = p;
+    }
+    base = static_cast<unsigned char*>(g_scratch_addr[dev]);
+  }
+  const int64_t n = g.nseg * g.Hkv * g.Dp;
+  if (n > kStaticStatEntries) return cudaErrorInvalidValue;
+  uint32_t* status = reinterpret_cast<uint32_t*>(base);
+  void* ksum = base + kStaticHeader;
+  uint32_t* vmax = reinterpret_cast<uint32_t*>(base + kStaticHeader + kStaticStatEntries * 8);
+  float* v_inv = reinterpret_cast<float*>(base + kStaticHeader + kStaticStatEntries * 12);
+  // the previous call's sums and maxima are still there: clear them
+  e = cudaMemsetAsync(base, 0, kStaticHeader + kStaticStatEntries * 12, st);
+  if (e != cudaSuccess) return e;
+  const bool bf16 = g.dtype == 1;
+  if (vec) {
+    if (bf16) launch_stats_only<true, true>(g, k, v, ksum, vmax, k_mean, s_v, v_inv, status, st);
+    else launch_stats_only<true, false>(g, k, v, ksum, vmax, k_mean, s_v, v_inv, status, st);
+  } else {
+    if (bf16) launch_stats_only<false, true>(g, k, v, ksum, vmax, k_mean, s_v, v_inv, status, st);
+    else launch_stats_only<false, false>(g, k, v, ksum, vmax, k_mean, s_v, v_inv, status, st);
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace sage

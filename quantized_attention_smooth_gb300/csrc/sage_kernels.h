@@ -29,6 +29,15 @@ struct PrologueBuffers {
 cudaError_t launch_prologue(const SegGeo& g, const PrologueBuffers& b,
                             bool vec, cudaStream_t st);
 
+// Largest nseg * Hkv * Dp served by the allocation-free statistics call.
+constexpr int64_t kStaticStatEntries = 16384;
+
+// K channel means and V channel scales of a dense call, with the scratch
+// accumulators in a static device array instead of a caller workspace.
+cudaError_t launch_kv_stats_static(const SegGeo& g, const uint16_t* k,
+                                   const uint16_t* v, float* k_mean, float* s_v,
+                                   bool vec, cudaStream_t st);
+
 struct AttnParams {
   SegGeo g;
   const float* s_q;

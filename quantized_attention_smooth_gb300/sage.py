@@ -23,6 +23,7 @@ EXPORTS = (
     "sage_quant_prologue_varlen", "sage_attn_quantized", "sage_attn_fwd",
     "sage_attn_fwd_varlen", "sage_debug_qk_int32", "sage_debug_e4m3",
     "sage_debug_set_fault", "sage_device_status", "sage_last_error",
+    "sage_kv_stats_noalloc",
 )
 
 
@@ -75,6 +76,7 @@ def _load():
         "sage_debug_set_fault": ([I, ctypes.c_uint64], None),
         "sage_device_status": ([P, P], I),
         "sage_last_error": ([], ctypes.c_char_p),
+        "sage_kv_stats_noalloc": ([P, P, I, I, I64, I64, I64, I64, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -243,6 +245,21 @@ def debug_e4m3(x, out=None, stream=None):
     rc = _lib.sage_debug_e4m3(_ptr(x), _ptr(out), x.numel(), _stream(stream))
     _check(rc, "sage_debug_e4m3")
     return out
+
+
+def kv_stats_noalloc(k, v, layout, k_mean, s_v, stream=None):
+    """K channel means and V channel scales with no device allocation at all:
+    the scratch is a static array inside the library (B*Hkv*Dp <= 16384).
+    k_mean and s_v are caller-owned fp32 tensors of B*Hkv*Dp elements."""
+    lay = _layout_code(layout)
+    if lay == HND:
+        B, Hkv, Lk, D = k.shape
+    else:
+        B, Lk, Hkv, D = k.shape
+    rc = _lib.sage_kv_stats_noalloc(_ptr(k), _ptr(v), _dtype_code(k), lay, B, Hkv, Lk, D,
+                                    _ptr(k_mean), _ptr(s_v), _stream(stream))
+    _check(rc, "sage_kv_stats_noalloc")
+    return k_mean, s_v
 
 
 def set_fault(skip_kv_tile: int = -1, timeout_ns: int = 0):
