@@ -400,7 +400,8 @@ sage_status sage_attn_fwd(const void* q, const void* k, const void* v, float* ou
                 (long long)B, (long long)Lq, (long long)Lk);
   if (!check_dims(Hq, Hkv, D, &s)) return s;
   if (B == 0 || Lq == 0) return ok();                 // nothing to compute
-  if ((s = check_common(q, k, v, dtype)) != SAGE_OK) return s;
+  // an empty key tensor may legitimately have null data pointers
+  if ((s = check_common(q, Lk == 0 ? q : k, Lk == 0 ? q : v, dtype)) != SAGE_OK) return s;
   if (out == nullptr || !aligned(out, 4))
     return fail(SAGE_ERR_INVALID_ARG, "out must be a 4-byte aligned device pointer");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
