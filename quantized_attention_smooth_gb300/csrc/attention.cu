@@ -8,18 +8,30 @@
 //   m'  = max(m, rowmax x);  P = 2^(x - m');  l = l * 2^(m - m') + sum P
 //   O   = O * 2^(m - m') + e4m3(448 P) . v~
 // and finally out = O * s_v / (448 l) in fp32 for the caller's D channels.
+// The kernel carries 448 P directly (2^(x - m' + log2 448)) and 448 l.
 //
 // GB300 mapping.  sm_103a has no INT8 tcgen05 MMA, so QK^T runs as
 // kind::f16 on operands that hold the int8 codes as exact fp16 integers;
 // each product is < 2^14 and a 128-term row sum < 2^21, so the fp32
 // accumulator holds the exact INT32 result.  PV runs as kind::f8f6f4 (e4m3 x
-// e4m3 -> fp32) with P~ read straight from tensor memory.  One CTA owns one
-// (segment, query head, 128-row tile):
-//   warp 4      TMA producer: Q once, then a 3-stage K/V ring
-//   warp 5      tcgen05 issuer (one thread) and TMEM owner
-//   warps 0-3   softmax, one row per thread (TMEM lane = row); they also
-//               rescale O in TMEM and run the epilogue
-// TMEM (512 columns): S0 | S1 (double-buffered S) | O (Dp) | P~0 | P~1.
+// e4m3 -> fp32) with P~ read straight from tensor memory.
+//
+// One CTA owns one (segment, query head) and TWO 128-row query tiles that
+// share every K/V tile ("ping-pong"): while the tensor core works on one
+// tile, the softmax warps of the other run.  16 warps:
+//   warps 0-3   softmax of query tile 0 (one row per thread, TMEM lane = row)
+//   warps 4-7   softmax of query tile 1
+//   warps 8-11  correction: rescale O in TMEM when the row max grows (while
+//               the softmax is still exponentiating), then the epilogue
+//   warp 12     TMA producer: both Q tiles, then a 3-stage K/V ring
+//   warp 13     tcgen05 issuer (one thread) and TMEM owner
+// TMEM (512 columns): S0 | S1 | O0 | O1; P~t (e4m3) overwrites the first 32
+// columns of St once the softmax has read St, and the next QK^T of tile t is
+// issued after the PV that reads it.
+// Per tile t and key tile j the hand-offs are:
+//   MMA --s_full--> softmax --alpha_ready--> correction --o_ready--> MMA
+//                   softmax --p_full------------------------------> MMA
+//   MMA (PV done) --o_done--> correction
 // Every wait is bounded: a wait that runs out raises the workspace status
 // word and an abort flag, all roles drain their in-flight copies and MMAs,
 // and the CTA frees its TMEM and exits.
@@ -32,30 +44,34 @@ namespace sage {
 namespace {
 
 constexpr int kStages = 3;
-constexpr int kThreads = 192;
+constexpr int kThreads = 512;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;
-__host__ __device__ constexpr uint32_t col_s(int b) { return b ? 128u : 0u; }
-__host__ __device__ constexpr uint32_t col_p(int b) { return b ? 416u : 384u; }
 constexpr int kAtomBytes = 128 * 128;   // 128 rows x 128 bytes (swizzle atom column)
 constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr float kLog2_448 = 8.80735492205760410750f;
+// register split (launch: 512 threads x 128): 2 x 128 x 192 + 128 x 80 + 128 x 48
+constexpr int kSoftmaxRegs = 192;
+constexpr int kCorrRegs = 80;
+constexpr int kMiscRegs = 48;
 
 template <int DP>
 struct Layout {
-  static constexpr int kQBytes = kBlockM * DP * 2;
+  static constexpr int kQBytes = kBlockM * DP * 2;     // one query tile
   static constexpr int kKBytes = kBlockN * DP * 2;
   static constexpr int kVBytes = DP * kBlockN;
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + kQBytes;
+  static constexpr int kKOff = kQOff + 2 * kQBytes;
   static constexpr int kVOff = kKOff + kStages * kKBytes;
   static constexpr int kBarOff = kVOff + kStages * kVBytes;
-  // q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_done, drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 1 + 1;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kSvOff = kMiscOff + 16;
-  static constexpr int kBytes = kSvOff + DP * 4;
-  // at least ~116 KB so that one CTA (and its 512 TMEM columns) owns an SM
-  static constexpr int kAlloc = (kBytes + 1024) > 118784 ? (kBytes + 1024) : 118784;
+  // q_full, kv_full[S], kv_empty[S], then per tile: s_full, alpha_ready,
+  // p_full, o_ready, o_done, l_ready; then drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 2 * 6 + 1;
+  static constexpr int kAlphaOff = (kBarOff + kNumBars * 8 + 15) / 16 * 16;
+  static constexpr int kLOff = kAlphaOff + 2 * kBlockM * 4;
+  static constexpr int kSvOff = kLOff + 2 * kBlockM * 4;
+  static constexpr int kMiscOff = kSvOff + DP * 4;
+  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kAlloc = kBytes + 1024;
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -88,6 +104,13 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem,
               (accumulate || kk > 0) ? 1u : 0u);
 }
 
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity,
+                                         volatile int* abort_flag, uint32_t* status,
+                                         uint64_t timeout_ns) {
+  bool ok = mbar_wait(bar, parity, abort_flag, status, timeout_ns);
+  return __all_sync(kFull, ok);
+}
+
 template <int DP>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -99,9 +122,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
   const SegGeo& g = p.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- which tile (heaviest causal tiles first)
+  // ---- which pair of query tiles (heaviest causal pairs first)
   const int64_t s = blockIdx.z, h = blockIdx.y;
-  const int64_t qt = p.causal ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;
+  const int64_t pair = p.causal ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;
   int64_t qstart = 0, len_q = g.Lq, kstart = 0, len_k = g.Lk;
   if (g.varlen) {
     const bool okq = seg_range(g.cu_q, s, g.total_q, g.max_q, &qstart, &len_q);
@@ -111,12 +134,20 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
       return;
     }
   }
-  if (qt * kBlockM >= len_q) return;
+  const int64_t qt0 = 2 * pair;
+  if (qt0 * kBlockM >= len_q) return;
   const int64_t hk = h / (g.Hq / g.Hkv);
-  int n_kv = static_cast<int>((len_k + kBlockN - 1) / kBlockN);
-  if (p.causal && n_kv > qt + 1) n_kv = static_cast<int>(qt + 1);
+  const int nk_all = static_cast<int>((len_k + kBlockN - 1) / kBlockN);
+  int n_t[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int64_t qt = qt0 + t;
+    if (qt * kBlockM >= len_q) n_t[t] = 0;
+    else n_t[t] = (p.causal && nk_all > qt + 1) ? static_cast<int>(qt + 1) : nk_all;
+  }
+  const int n_max = n_t[0] > n_t[1] ? n_t[0] : n_t[1];
   const int64_t q_row0 = ws_seg_base(g.varlen, s, qstart, g.Hq, g.q_head_rows) +
-                         h * g.q_head_rows + qt * kBlockM;
+                         h * g.q_head_rows + qt0 * kBlockM;
   const int64_t k_row0 = ws_seg_base(g.varlen, s, kstart, g.Hkv, g.k_head_rows) +
                          hk * g.k_head_rows;
   const int64_t v_row0 = (g.varlen ? 0 : s * g.Hkv * DP) + hk * DP;
@@ -126,13 +157,18 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
   uint64_t* kv_empty = kv_full + kStages;
-  uint64_t* s_full = kv_empty + kStages;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 2;
-  uint64_t* drain = o_done + 1;
+  uint64_t* s_full = kv_empty + kStages;      // [2]
+  uint64_t* alpha_ready = s_full + 2;         // [2]
+  uint64_t* p_full = alpha_ready + 2;         // [2]
+  uint64_t* o_ready = p_full + 2;             // [2]
+  uint64_t* o_done = o_ready + 2;             // [2]
+  uint64_t* l_ready = o_done + 2;             // [2]
+  uint64_t* drain = l_ready + 2;
+  float* alpha_s = reinterpret_cast<float*>(smem + L::kAlphaOff);   // [2][128]
+  float* l_s = reinterpret_cast<float*>(smem + L::kLOff);           // [2][128]
+  float* sv_cache = reinterpret_cast<float*>(smem + L::kSvOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
-  float* sv_cache = reinterpret_cast<float*>(smem + L::kSvOff);
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -141,17 +177,21 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_init(&kv_full[i], 1);
       mbar_init(&kv_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], kBlockM);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&alpha_ready[t], kBlockM);
+      mbar_init(&p_full[t], kBlockM);
+      mbar_init(&o_ready[t], kBlockM);
+      mbar_init(&o_done[t], 1);
+      mbar_init(&l_ready[t], kBlockM);
     }
-    mbar_init(o_done, 1);
     mbar_init(drain, 1);
     mbar_fence_init();
   }
-  if (warp == 5) tmem_alloc(tmem_slot, kTmemCols);
-  if (threadIdx.x < DP) sv_cache[threadIdx.x] = p.s_v[(s * g.Hkv + hk) * DP + threadIdx.x];
-  if (warp == 4 && lane == 0) {
+  if (warp == 13) tmem_alloc(tmem_slot, kTmemCols);
+  if (threadIdx.x >= 256 && threadIdx.x < 256 + DP)
+    sv_cache[threadIdx.x - 256] = p.s_v[(s * g.Hkv + hk) * DP + (threadIdx.x - 256)];
+  if (warp == 12 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -160,20 +200,25 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  const int wg = warp >> 2;
 
-  if (warp == 4) {
-    // ================================================= TMA producer
-    if (lane == 0) {
-      mbar_expect_tx(q_full, L::kQBytes);
-      for (int a = 0; a < DP / 64; ++a)
-        tma_load_2d(smem + L::kQOff + a * kAtomBytes, &tm_q, a * 64,
-                    static_cast<int32_t>(q_row0), q_full);
+  if (wg == 3) {
+    regs_decrease<kMiscRegs>();
+    if (warp == 12 && lane == 0) {
+      // ============================================== TMA producer
+      mbar_expect_tx(q_full, (n_t[1] > 0 ? 2 : 1) * L::kQBytes);
+      for (int t = 0; t < 2; ++t) {
+        if (n_t[t] == 0) continue;
+        for (int a = 0; a < DP / 64; ++a)
+          tma_load_2d(smem + L::kQOff + t * L::kQBytes + a * kAtomBytes, &tm_q, a * 64,
+                      static_cast<int32_t>(q_row0 + t * kBlockM), q_full);
+      }
       int last = -1;
-      for (int j = 0; j < n_kv; ++j) {
+      for (int j = 0; j < n_max; ++j) {
         const int st = j % kStages;
         if (j >= kStages &&
-            !mbar_wait(&kv_empty[st], ((j / kStages) - 1) & 1, abort_flag,
-                       p.status, p.timeout_ns))
+            !mbar_wait(&kv_empty[st], ((j / kStages) - 1) & 1, abort_flag, p.status,
+                       p.timeout_ns))
           break;
         if (j == p.skip_kv_tile) continue;   // failure injection (tests only)
         mbar_expect_tx(&kv_full[st], L::kKBytes + L::kVBytes);
@@ -192,42 +237,46 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (j != p.skip_kv_tile)
           mbar_wait(&kv_full[j % kStages], (j / kStages) & 1, nullptr, p.status,
                     p.timeout_ns);
-    }
-  } else if (warp == 5) {
-    // ================================================= tcgen05 issuer
-    if (lane == 0) {
+    } else if (warp == 13 && lane == 0) {
+      // ============================================== tcgen05 issuer
       const uint32_t qa = smem_u32(smem + L::kQOff);
       const uint32_t ka0 = smem_u32(smem + L::kKOff);
       const uint32_t va0 = smem_u32(smem + L::kVOff);
       bool ok = mbar_wait(q_full, 0, abort_flag, p.status, p.timeout_ns);
       bool issued = false;
-      if (ok && n_kv > 0) {
+      if (ok && n_max > 0) {
         ok = mbar_wait(&kv_full[0], 0, abort_flag, p.status, p.timeout_ns);
         if (ok) {
           tc_fence_after();
-          issue_qk<DP>(tbase + col_s(0), qa, ka0);
-          tc_commit(&s_full[0]);
+          for (int t = 0; t < 2; ++t) {
+            if (n_t[t] == 0) continue;
+            issue_qk<DP>(tbase + t * 128, qa + t * L::kQBytes, ka0);
+            tc_commit(&s_full[t]);
+          }
           issued = true;
         }
-        for (int j = 0; ok && j < n_kv; ++j) {
-          if (j + 1 < n_kv) {
-            const int st1 = (j + 1) % kStages;
-            ok = mbar_wait(&kv_full[st1], ((j + 1) / kStages) & 1, abort_flag,
-                           p.status, p.timeout_ns);
+        for (int j = 0; ok && j < n_max; ++j) {
+          const int st = j % kStages;
+          for (int t = 0; t < 2; ++t) {
+            if (j >= n_t[t]) continue;
+            ok = mbar_wait(&p_full[t], j & 1, abort_flag, p.status, p.timeout_ns) &&
+                 mbar_wait(&o_ready[t], j & 1, abort_flag, p.status, p.timeout_ns);
             if (!ok) break;
             tc_fence_after();
-            issue_qk<DP>(tbase + col_s((j + 1) & 1), qa, ka0 + st1 * L::kKBytes);
-            tc_commit(&s_full[(j + 1) & 1]);
+            issue_pv<DP>(tbase + 256 + t * DP, tbase + t * 128, va0 + st * L::kVBytes, j > 0);
+            tc_commit(&o_done[t]);
+            if (j + 1 < n_t[t]) {
+              const int st1 = (j + 1) % kStages;
+              ok = mbar_wait(&kv_full[st1], ((j + 1) / kStages) & 1, abort_flag, p.status,
+                             p.timeout_ns);
+              if (!ok) break;
+              tc_fence_after();
+              issue_qk<DP>(tbase + t * 128, qa + t * L::kQBytes, ka0 + st1 * L::kKBytes);
+              tc_commit(&s_full[t]);
+            }
           }
-          ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag, p.status,
-                         p.timeout_ns);
           if (!ok) break;
-          tc_fence_after();
-          const int st = j % kStages;
-          issue_pv<DP>(tbase + kColO, tbase + col_p(j & 1), va0 + st * L::kVBytes,
-                       j > 0);
           tc_commit(&kv_empty[st]);
-          tc_commit(o_done);
         }
       }
       if (issued) {   // every MMA must finish before TMEM is released
@@ -235,23 +284,109 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
         mbar_wait(drain, 0, nullptr, p.status, p.timeout_ns);
       }
     }
-  } else {
-    // ================================================= softmax warps 0-3
-    const int r = threadIdx.x;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const int64_t qi = qt * kBlockM + r;          // query index in segment
-    const float sq = p.s_q[q_row0 + r];
-    const float* skp = p.s_k + k_row0 / kBlockN;
-    float m = -INFINITY, l = 0.0f;
+  } else if (wg == 2) {
+    // ================================================ correction + epilogue
+    regs_decrease<kCorrRegs>();
+    const int r = threadIdx.x - 256;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const int b = j & 1;
-      ok = mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag, p.status, p.timeout_ns);
-      ok = __all_sync(kFull, ok);
+    for (int j = 0; ok && j < n_max; ++j) {
+      for (int t = 0; t < 2; ++t) {
+        if (j >= n_t[t]) continue;
+        ok = wait_all(&alpha_ready[t], j & 1, abort_flag, p.status, p.timeout_ns);
+        if (!ok) break;
+        if (j > 0) {
+          // O_t holds PV of key tiles < j once PV(j-1) is done
+          ok = wait_all(&o_done[t], (j - 1) & 1, abort_flag, p.status, p.timeout_ns);
+          if (!ok) break;
+          tc_fence_after();
+          const float alpha = alpha_s[t * kBlockM + r];
+          if (__any_sync(kFull, alpha < 1.0f)) {
+            const uint32_t to = tbase + lane_off + 256 + t * DP;
+#pragma unroll 1
+            for (int cc = 0; cc < DP / 32; ++cc) {
+              uint32_t o[32];
+              tmem_ld32(to + 32 * cc, o);
+              tmem_ld_wait();
+              reg_fence(o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(to + 32 * cc, o);
+            }
+            tmem_st_wait();
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&o_ready[t]);
+      }
+    }
+    // epilogue: out = O * s_v / (448 l), the caller's D channels only
+    const int D = static_cast<int>(g.D);
+    const int64_t seg_off = g.varlen ? qstart * p.out_tok_stride : s * p.out_seg_stride;
+    for (int t = 0; ok && t < 2; ++t) {
+      if (n_t[t] == 0) continue;
+      ok = wait_all(&o_done[t], (n_t[t] - 1) & 1, abort_flag, p.status, p.timeout_ns) &&
+           wait_all(&l_ready[t], 0, abort_flag, p.status, p.timeout_ns);
+      if (!ok) break;
+      tc_fence_after();
+      const float l448 = l_s[t * kBlockM + r];
+      const float inv = l448 > 0.0f ? __fdiv_rn(1.0f, l448) : 0.0f;
+      const int64_t qi = (qt0 + t) * kBlockM + r;
+      const bool valid = qi < len_q;
+      float* orow = p.out + seg_off + h * p.out_head_stride + qi * p.out_tok_stride;
+      const bool vec = (D % 4 == 0) && ((reinterpret_cast<uintptr_t>(orow) & 15) == 0);
+#pragma unroll 1
+      for (int cc = 0; cc < DP / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tbase + lane_off + 256 + t * DP + 32 * cc, o);
+        tmem_ld_wait();
+        reg_fence(o);
+        if (!valid) continue;
+        if (vec) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const int c = 32 * cc + i;
+            if (c < D) {
+              float4 v4;
+              v4.x = __uint_as_float(o[i]) * sv_cache[c] * inv;
+              v4.y = __uint_as_float(o[i + 1]) * sv_cache[c + 1] * inv;
+              v4.z = __uint_as_float(o[i + 2]) * sv_cache[c + 2] * inv;
+              v4.w = __uint_as_float(o[i + 3]) * sv_cache[c + 3] * inv;
+              *reinterpret_cast<float4*>(orow + c) = v4;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int c = 32 * cc + i;
+            if (c < D) orow[c] = __uint_as_float(o[i]) * sv_cache[c] * inv;
+          }
+        }
+      }
+    }
+  } else {
+    // ================================================ softmax of tile wg
+    regs_increase<kSoftmaxRegs>();
+    const int t = wg;
+    const int r = threadIdx.x - t * kBlockM;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t ts = tbase + lane_off + t * 128;
+    const int64_t qi = (qt0 + t) * kBlockM + r;          // query index in segment
+    const int n = n_t[t];
+    const float* skp = p.s_k + k_row0 / kBlockN;
+    const float sq = n > 0 ? p.s_q[q_row0 + t * kBlockM + r] : 0.0f;
+    const int64_t kend = p.causal ? (len_k < qi + 1 ? len_k : qi + 1) : len_k;
+    float m = -INFINITY, l448 = 0.0f;
+    float sk_next = n > 0 ? skp[0] : 0.0f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const float sk = sk_next;
+      if (j + 1 < n) sk_next = skp[j + 1];
+      ok = wait_all(&s_full[t], j & 1, abort_flag, p.status, p.timeout_ns);
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[4][32];
-      const uint32_t ts = tbase + lane_off + col_s(b);
       tmem_ld32(ts, sr[0]);
       tmem_ld32(ts + 32, sr[1]);
       tmem_ld32(ts + 64, sr[2]);
@@ -262,120 +397,69 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
       reg_fence(sr[2]);
       reg_fence(sr[3]);
 
-      const float c = (sq * skp[j]) * p.scale_log2;
+      // c > 0 keeps -inf * c = -inf for masked keys even when a scale is 0
+      const float c = fmaxf((sq * sk) * p.scale_log2, 1e-30f);
       const int64_t key0 = static_cast<int64_t>(j) * kBlockN;
-      const bool need_mask = (key0 + kBlockN > len_k) ||
-                             (p.causal && key0 + kBlockN - 1 > qt * kBlockM);
-      float mx = -INFINITY;
+      if (key0 + kBlockN > kend) {
+        const int64_t lim64 = kend - key0;
+        const int lim = lim64 < 0 ? 0 : static_cast<int>(lim64);
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        float xv = __uint_as_float(sr[i >> 5][i & 31]) * c;
-        if (need_mask) {
-          const int64_t key = key0 + i;
-          if (key >= len_k || (p.causal && key > qi)) xv = -INFINITY;
-        }
-        sr[i >> 5][i & 31] = __float_as_uint(xv);
-        mx = fmaxf(mx, xv);
+        for (int i = 0; i < 128; ++i)
+          if (i >= lim) sr[i >> 5][i & 31] = 0xFF800000u;   // -inf
       }
-      const float m_new = fmaxf(m, mx);
-      const float alpha = fast_exp2(m - m_new);
-      float psum = 0.0f;
-      uint32_t pw[32];
+      // row max of the exact integer scores, four independent chains
+      float mx0 = __uint_as_float(sr[0][0]), mx1 = __uint_as_float(sr[1][0]);
+      float mx2 = __uint_as_float(sr[2][0]), mx3 = __uint_as_float(sr[3][0]);
 #pragma unroll
-      for (int w4 = 0; w4 < 32; ++w4) {
-        float pv[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = 4 * w4 + e;
-          pv[e] = fast_exp2(__uint_as_float(sr[i >> 5][i & 31]) - m_new);
-          psum += pv[e];
-        }
-        pw[w4] = pack_e4m3x2(448.0f * pv[0], 448.0f * pv[1]) |
-                 (pack_e4m3x2(448.0f * pv[2], 448.0f * pv[3]) << 16);
+      for (int i = 1; i < 32; ++i) {
+        mx0 = fmaxf(mx0, __uint_as_float(sr[0][i]));
+        mx1 = fmaxf(mx1, __uint_as_float(sr[1][i]));
+        mx2 = fmaxf(mx2, __uint_as_float(sr[2][i]));
+        mx3 = fmaxf(mx3, __uint_as_float(sr[3][i]));
       }
-      tmem_st32(tbase + lane_off + col_p(b), pw);
+      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      const float m_new = fmaxf(m, m_tile);
+      const float alpha = fast_exp2(m - m_new);          // 0 on the first tile
+      alpha_s[t * kBlockM + r] = alpha;
+      mbar_arrive(&alpha_ready[t]);                      // correction may rescale O now
+
+      // 448 P = 2^(S c - m' + log2 448), quantised to e4m3 into TMEM (over St)
+      const float bias = kLog2_448 - m_new;
+      float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t w[8];
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const int i = 4 * q4;
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[cc][i]), c, bias));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[cc][i + 1]), c, bias));
+          const float p2 = fast_exp2(fmaf(__uint_as_float(sr[cc][i + 2]), c, bias));
+          const float p3 = fast_exp2(fmaf(__uint_as_float(sr[cc][i + 3]), c, bias));
+          a0 += p0;
+          a1 += p1;
+          a2 += p2;
+          a3 += p3;
+          w[q4] = pack_e4m3x2(p0, p1) | (pack_e4m3x2(p2, p3) << 16);
+        }
+        tmem_st8(ts + 8 * cc, w);
+      }
       tmem_st_wait();
-      l = l * alpha + psum;
-      if (j > 0) {
-        // O holds PV of tiles < j once that PV is done; rescale it in place
-        ok = mbar_wait(o_done, (j - 1) & 1, abort_flag, p.status, p.timeout_ns);
-        ok = __all_sync(kFull, ok);
-        if (!ok) break;
-        tc_fence_after();
-        if (__any_sync(kFull, alpha < 1.0f)) {
-#pragma unroll 1
-          for (int cc = 0; cc < DP / 32; ++cc) {
-            uint32_t o[32];
-            const uint32_t to = tbase + lane_off + kColO + 32 * cc;
-            tmem_ld32(to, o);
-            tmem_ld_wait();
-            reg_fence(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(to, o);
-          }
-          tmem_st_wait();
-        }
-      }
+      l448 = l448 * alpha + ((a0 + a1) + (a2 + a3));
       m = m_new;
       tc_fence_before();
-      mbar_arrive(&p_full[b]);
+      mbar_arrive(&p_full[t]);
     }
-
-    if (ok && n_kv > 0) {
-      ok = mbar_wait(o_done, (n_kv - 1) & 1, abort_flag, p.status, p.timeout_ns);
-      ok = __all_sync(kFull, ok);
-    }
-    if (ok) {
-      tc_fence_after();
-      const float inv = l > 0.0f ? __fdiv_rn(1.0f, 448.0f * l) : 0.0f;
-      const bool valid = qi < len_q;
-      const int D = static_cast<int>(g.D);
-      const int64_t seg_off = g.varlen ? qstart * p.out_tok_stride : s * p.out_seg_stride;
-      float* orow = p.out + seg_off + h * p.out_head_stride + qi * p.out_tok_stride;
-      const bool vec = (D % 4 == 0) && ((reinterpret_cast<uintptr_t>(orow) & 15) == 0);
-#pragma unroll 1
-      for (int cc = 0; cc < DP / 32; ++cc) {
-        uint32_t o[32];
-        if (n_kv > 0) {
-          tmem_ld32(tbase + lane_off + kColO + 32 * cc, o);
-          tmem_ld_wait();
-          reg_fence(o);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0u;
-        }
-        if (valid) {
-          if (vec) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              const int c = 32 * cc + i;
-              if (c < D) {
-                float4 v4;
-                v4.x = __uint_as_float(o[i]) * sv_cache[c] * inv;
-                v4.y = __uint_as_float(o[i + 1]) * sv_cache[c + 1] * inv;
-                v4.z = __uint_as_float(o[i + 2]) * sv_cache[c + 2] * inv;
-                v4.w = __uint_as_float(o[i + 3]) * sv_cache[c + 3] * inv;
-                *reinterpret_cast<float4*>(orow + c) = v4;
-              }
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int c = 32 * cc + i;
-              if (c < D) orow[c] = __uint_as_float(o[i]) * sv_cache[c] * inv;
-            }
-          }
-        }
-      }
+    if (ok && n > 0) {
+      l_s[t * kBlockM + r] = l448;
+      mbar_arrive(&l_ready[t]);
     }
   }
 
   // ---- teardown: all roles have drained; release tensor memory
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 13) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
@@ -469,8 +553,9 @@ cudaError_t launch_attention_t(const AttnMaps& maps, const AttnParams& p,
     configured = true;
   }
   const int64_t maxq = p.g.varlen ? p.g.max_q : p.g.Lq;
-  dim3 grid(static_cast<unsigned>((maxq + kBlockM - 1) / kBlockM),
-            static_cast<unsigned>(p.g.Hq), static_cast<unsigned>(p.g.nseg));
+  const int64_t nqt = (maxq + kBlockM - 1) / kBlockM;      // query tiles, two per CTA
+  dim3 grid(static_cast<unsigned>((nqt + 1) / 2), static_cast<unsigned>(p.g.Hq),
+            static_cast<unsigned>(p.g.nseg));
   attn_kernel<DP><<<grid, kThreads, Layout<DP>::kAlloc, st>>>(maps.q, maps.k, maps.v, p);
   return cudaGetLastError();
 }
