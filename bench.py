@@ -112,6 +112,17 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- GPU arm
+def count_launches(torch, fn) -> int:
+    """Kernels of this library launched by one call of fn (CUPTI trace)."""
+    from torch.profiler import ProfilerActivity, profile
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        fn()
+        torch.cuda.synchronize()
+    ours = ("attn_kernel", "kv_stats_kernel", "kv_quant_kernel", "kv_finalize_kernel",
+            "q_quant_kernel")
+    return sum(1 for e in prof.events() if any(o in e.name for o in ours))
+
+
 def to_device(torch, bits, dtype):
     t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
     return t.view(torch.float16 if dtype == wl.F16 else torch.bfloat16)
@@ -165,6 +176,7 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int):
         flush.zero_()
     torch.cuda.synchronize()
     assert sage.device_status(ws) == sage.OK, sage.last_error()
+    launches_per_step = count_launches(torch, fwd)
 
     # ---- timed region: whole step (prologue + attention), device events
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -229,6 +241,7 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int):
     ops = workload_ops(w)
     Dp = 64 if w.D <= 64 else 128
     return dict(total_ms=total_ms, step_ms=step_ms, pro_ms=pro_ms, att_ms=att_ms,
+                launches_per_step=launches_per_step,
                 e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, ops=ops, ops_padded=workload_ops(w, Dp),
                 clocks=clock_info)
 
@@ -353,7 +366,7 @@ def main():
         "prologue_hbm_frac": pro_gbs / peaks["hbm_gbs"],
         "e2e": {"value": r["ops"] / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TOPS",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": r["launches_per_step"] * args.steps,
         "clocks": r["clocks"],
         "cpu_baseline": {"value": cpu_ops / cpu_s / 1e12, "unit": "TOPS", "cores": cores,
                          "kind": "oracle",

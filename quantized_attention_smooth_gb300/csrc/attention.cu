@@ -14,27 +14,31 @@
 // kind::f16 on operands that hold the int8 codes as exact fp16 integers;
 // each product is < 2^14 and a 128-term row sum < 2^21, so the fp32
 // accumulator holds the exact INT32 result.  PV runs as kind::f8f6f4 (e4m3 x
-// e4m3 -> fp32) with P~ read straight from tensor memory.
+// e4m3 -> fp32) with both operands in shared memory.
 //
 // One CTA owns one (segment, query head) and TWO 128-row query tiles that
-// share every K/V tile ("ping-pong"): while the tensor core works on one
-// tile, the softmax warps of the other run.  16 warps:
+// share every K/V tile.  16 warps:
 //   warps 0-3   softmax of query tile 0 (one row per thread, TMEM lane = row)
 //   warps 4-7   softmax of query tile 1
 //   warps 8-11  correction: rescale O in TMEM when the row max grows (while
 //               the softmax is still exponentiating), then the epilogue
-//   warp 12     TMA producer: both Q tiles, then a 3-stage K/V ring
-//   warp 13     tcgen05 issuer (one thread) and TMEM owner
-// TMEM (512 columns): S0 | S1 | O0 | O1; P~t (e4m3) overwrites the first 32
-// columns of St once the softmax has read St, and the next QK^T of tile t is
-// issued after the PV that reads it.
-// Per tile t and key tile j the hand-offs are:
-//   MMA --s_full--> softmax --alpha_ready--> correction --o_ready--> MMA
-//                   softmax --p_full------------------------------> MMA
-//   MMA (PV done) --o_done--> correction
-// Every wait is bounded: a wait that runs out raises the workspace status
-// word and an abort flag, all roles drain their in-flight copies and MMAs,
-// and the CTA frees its TMEM and exits.
+//   warp 12     TMA producer of both Q tiles and the K ring
+//   warp 13     tcgen05 issuer of query tile 0 (one thread) and TMEM owner
+//   warp 14     TMA producer of the V ring
+//   warp 15     tcgen05 issuer of query tile 1 (one thread)
+// TMEM (512 columns): S0 | S1 | O0 | O1.  P~ (e4m3) goes to shared memory in
+// the 128-byte swizzled K-major layout, so S_t is free as soon as the softmax
+// has loaded it into registers: QK^T of the next key tile then runs on the
+// tensor core while the softmax is still exponentiating the current one.
+// Per query tile t and key tile j the hand-offs are:
+//   MMA --s_full--> softmax --s_free--> MMA (next QK^T into S_t)
+//                   softmax --alpha_ready[j&1]--> correction --pv_ready--> MMA
+//                   softmax (P~ in smem) -------------------pv_ready--> MMA
+//   MMA (PV done) --o_done--> correction (rescale), softmax (P~ buffer free)
+// K and V stages are released by one arrival per active query tile.  Every
+// wait is bounded: a wait that runs out raises the workspace status word and
+// an abort flag, all roles drain their in-flight copies and MMAs, and the CTA
+// frees its TMEM and exits.
 
 #include "sage_device.cuh"
 #include "sage_geom.h"
@@ -43,7 +47,8 @@
 namespace sage {
 namespace {
 
-constexpr int kStages = 3;
+constexpr int kKStages = 2;   // K ring (released after the second QK^T)
+constexpr int kVStages = 3;   // V ring (released after the second PV)
 constexpr int kThreads = 512;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kAtomBytes = 128 * 128;   // 128 rows x 128 bytes (swizzle atom column)
@@ -59,15 +64,17 @@ struct Layout {
   static constexpr int kQBytes = kBlockM * DP * 2;     // one query tile
   static constexpr int kKBytes = kBlockN * DP * 2;
   static constexpr int kVBytes = DP * kBlockN;
+  static constexpr int kPBytes = kBlockM * kBlockN;    // e4m3 P~ of one query tile
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + 2 * kQBytes;
-  static constexpr int kVOff = kKOff + kStages * kKBytes;
-  static constexpr int kBarOff = kVOff + kStages * kVBytes;
-  // q_full, kv_full[S], kv_empty[S], then per tile: s_full, alpha_ready,
-  // p_full, o_ready, o_done, l_ready; then drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 * 6 + 1;
+  static constexpr int kVOff = kKOff + kKStages * kKBytes;
+  static constexpr int kPOff = kVOff + kVStages * kVBytes;
+  static constexpr int kBarOff = kPOff + 2 * kPBytes;
+  // q_full, k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], then per tile:
+  // s_full, s_free, alpha_ready[2], pv_ready, o_done, l_ready, drain
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 * 8;
   static constexpr int kAlphaOff = (kBarOff + kNumBars * 8 + 15) / 16 * 16;
-  static constexpr int kLOff = kAlphaOff + 2 * kBlockM * 4;
+  static constexpr int kLOff = kAlphaOff + 4 * kBlockM * 4;
   static constexpr int kSvOff = kLOff + 2 * kBlockM * 4;
   static constexpr int kMiscOff = kSvOff + DP * 4;
   static constexpr int kBytes = kMiscOff + 16;
@@ -80,28 +87,27 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 // S (128x128 fp32 in TMEM) = Q tile . K tile^T, K dimension DP in steps of 16.
+// q_lo / k_lo: low descriptor words of the 1024-byte aligned operand tiles.
 template <int DP>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem,
-                                         uint32_t k_smem) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_lo, uint32_t k_lo) {
   constexpr uint32_t idesc = make_idesc(kFmtF16, kFmtF16, kBlockM, kBlockN);
 #pragma unroll
   for (int kk = 0; kk < DP / 16; ++kk) {
-    const uint32_t off = (kk / 4) * kAtomBytes + (kk % 4) * 32;
-    mma_f16_ss(d_tmem, sdesc_sw128(q_smem + off), sdesc_sw128(k_smem + off),
-               idesc, kk > 0 ? 1u : 0u);
+    const uint32_t off = ((kk / 4) * kAtomBytes + (kk % 4) * 32) >> 4;
+    mma_f16_ss_lo(d_tmem, q_lo + off, k_lo + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
-// O (128xDP fp32 in TMEM) (+)= P~ (128x128 e4m3 in TMEM) . V~ tile^T
+// O (128xDP fp32 in TMEM) (+)= P~ (128x128 e4m3, smem) . V~ tile^T
 // (V~ stored DP rows x 128 keys), K dimension 128 keys in steps of 32.
 template <int DP>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem,
-                                         uint32_t v_smem, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_lo, uint32_t v_lo,
+                                         bool accumulate) {
   constexpr uint32_t idesc = make_idesc(kFmtE4M3, kFmtE4M3, kBlockM, DP);
 #pragma unroll
   for (int kk = 0; kk < kBlockN / 32; ++kk)
-    mma_f8_ts(o_tmem, p_tmem + kk * 8, sdesc_sw128(v_smem + kk * 32), idesc,
-              (accumulate || kk > 0) ? 1u : 0u);
+    mma_f8_ss_lo(o_tmem, p_lo + ((kk * 32) >> 4), v_lo + ((kk * 32) >> 4), idesc,
+                 (accumulate || kk > 0) ? 1u : 0u);
 }
 
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity,
@@ -155,16 +161,20 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = kv_full + kStages;
-  uint64_t* s_full = kv_empty + kStages;      // [2]
-  uint64_t* alpha_ready = s_full + 2;         // [2]
-  uint64_t* p_full = alpha_ready + 2;         // [2]
-  uint64_t* o_ready = p_full + 2;             // [2]
-  uint64_t* o_done = o_ready + 2;             // [2]
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + kKStages;
+  uint64_t* v_full = k_empty + kKStages;
+  uint64_t* v_empty = v_full + kVStages;
+  uint64_t* s_full = v_empty + kVStages;      // [2]
+  uint64_t* s_free = s_full + 2;              // [2]
+  // the softmax may run one key tile ahead of the correction (S is released
+  // early), so the row rescale factors and their barrier alternate by j & 1
+  uint64_t* alpha_ready = s_free + 2;         // [2 tiles][2 key-tile parities]
+  uint64_t* pv_ready = alpha_ready + 4;       // [2] softmax (128) + correction (128)
+  uint64_t* o_done = pv_ready + 2;            // [2]
   uint64_t* l_ready = o_done + 2;             // [2]
-  uint64_t* drain = l_ready + 2;
-  float* alpha_s = reinterpret_cast<float*>(smem + L::kAlphaOff);   // [2][128]
+  uint64_t* drain = l_ready + 2;              // [2]
+  float* alpha_s = reinterpret_cast<float*>(smem + L::kAlphaOff);   // [2][2][128]
   float* l_s = reinterpret_cast<float*>(smem + L::kLOff);           // [2][128]
   float* sv_cache = reinterpret_cast<float*>(smem + L::kSvOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
@@ -173,19 +183,25 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(q_full, 1);
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+    const uint32_t active = n_t[1] > 0 ? 2u : 1u;   // query tiles reading K/V
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], active);
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], active);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&alpha_ready[t], kBlockM);
-      mbar_init(&p_full[t], kBlockM);
-      mbar_init(&o_ready[t], kBlockM);
+      mbar_init(&s_free[t], kBlockM);
+      mbar_init(&alpha_ready[2 * t], kBlockM);
+      mbar_init(&alpha_ready[2 * t + 1], kBlockM);
+      mbar_init(&pv_ready[t], 2 * kBlockM);
       mbar_init(&o_done[t], 1);
       mbar_init(&l_ready[t], kBlockM);
+      mbar_init(&drain[t], 1);
     }
-    mbar_init(drain, 1);
     mbar_fence_init();
   }
   if (warp == 13) tmem_alloc(tmem_slot, kTmemCols);
@@ -205,7 +221,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
   if (wg == 3) {
     regs_decrease<kMiscRegs>();
     if (warp == 12 && lane == 0) {
-      // ============================================== TMA producer
+      // ============================================== TMA producer: Q and K
       mbar_expect_tx(q_full, (n_t[1] > 0 ? 2 : 1) * L::kQBytes);
       for (int t = 0; t < 2; ++t) {
         if (n_t[t] == 0) continue;
@@ -215,73 +231,97 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
       int last = -1;
       for (int j = 0; j < n_max; ++j) {
-        const int st = j % kStages;
-        if (j >= kStages &&
-            !mbar_wait(&kv_empty[st], ((j / kStages) - 1) & 1, abort_flag, p.status,
+        const int st = j % kKStages;
+        if (j >= kKStages &&
+            !mbar_wait(&k_empty[st], ((j / kKStages) - 1) & 1, abort_flag, p.status,
                        p.timeout_ns))
           break;
         if (j == p.skip_kv_tile) continue;   // failure injection (tests only)
-        mbar_expect_tx(&kv_full[st], L::kKBytes + L::kVBytes);
+        mbar_expect_tx(&k_full[st], L::kKBytes);
         uint8_t* kdst = smem + L::kKOff + st * L::kKBytes;
         for (int a = 0; a < DP / 64; ++a)
           tma_load_2d(kdst + a * kAtomBytes, &tm_k, a * 64,
-                      static_cast<int32_t>(k_row0 + j * kBlockN), &kv_full[st]);
-        tma_load_2d(smem + L::kVOff + st * L::kVBytes, &tm_v,
-                    static_cast<int32_t>(v_col0 + j * kBlockN),
-                    static_cast<int32_t>(v_row0), &kv_full[st]);
+                      static_cast<int32_t>(k_row0 + j * kBlockN), &k_full[st]);
         last = j;
       }
       // no copy may still be in flight when the CTA exits
       mbar_wait(q_full, 0, nullptr, p.status, p.timeout_ns);
-      for (int j = max(0, last - kStages + 1); j <= last; ++j)
+      for (int j = max(0, last - kKStages + 1); j <= last; ++j)
         if (j != p.skip_kv_tile)
-          mbar_wait(&kv_full[j % kStages], (j / kStages) & 1, nullptr, p.status,
+          mbar_wait(&k_full[j % kKStages], (j / kKStages) & 1, nullptr, p.status,
                     p.timeout_ns);
-    } else if (warp == 13 && lane == 0) {
-      // ============================================== tcgen05 issuer
-      const uint32_t qa = smem_u32(smem + L::kQOff);
-      const uint32_t ka0 = smem_u32(smem + L::kKOff);
-      const uint32_t va0 = smem_u32(smem + L::kVOff);
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.status, p.timeout_ns);
+    } else if (warp == 14 && lane == 0) {
+      // ============================================== TMA producer: V
+      int last = -1;
+      for (int j = 0; j < n_max; ++j) {
+        const int st = j % kVStages;
+        if (j >= kVStages &&
+            !mbar_wait(&v_empty[st], ((j / kVStages) - 1) & 1, abort_flag, p.status,
+                       p.timeout_ns))
+          break;
+        mbar_expect_tx(&v_full[st], L::kVBytes);
+        tma_load_2d(smem + L::kVOff + st * L::kVBytes, &tm_v,
+                    static_cast<int32_t>(v_col0 + j * kBlockN),
+                    static_cast<int32_t>(v_row0), &v_full[st]);
+        last = j;
+      }
+      for (int j = max(0, last - kVStages + 1); j <= last; ++j)
+        mbar_wait(&v_full[j % kVStages], (j / kVStages) & 1, nullptr, p.status, p.timeout_ns);
+    } else if ((warp == 13 || warp == 15) && lane == 0 && n_t[warp == 13 ? 0 : 1] > 0) {
+      // ============================================== tcgen05 issuer of tile t
+      const int t = warp == 13 ? 0 : 1;
+      const int n = n_t[t];
+      const uint32_t qa = sdesc_sw128_lo(smem_u32(smem + L::kQOff + t * L::kQBytes));
+      const uint32_t ka0 = sdesc_sw128_lo(smem_u32(smem + L::kKOff));
+      const uint32_t va0 = sdesc_sw128_lo(smem_u32(smem + L::kVOff));
+      const uint32_t pa = sdesc_sw128_lo(smem_u32(smem + L::kPOff + t * L::kPBytes));
+      const uint32_t ts = tbase + t * 128, to = tbase + 256 + t * DP;
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.status, p.timeout_ns) &&
+                mbar_wait(&k_full[0], 0, abort_flag, p.status, p.timeout_ns);
       bool issued = false;
-      if (ok && n_max > 0) {
-        ok = mbar_wait(&kv_full[0], 0, abort_flag, p.status, p.timeout_ns);
-        if (ok) {
-          tc_fence_after();
-          for (int t = 0; t < 2; ++t) {
-            if (n_t[t] == 0) continue;
-            issue_qk<DP>(tbase + t * 128, qa + t * L::kQBytes, ka0);
-            tc_commit(&s_full[t]);
-          }
-          issued = true;
-        }
-        for (int j = 0; ok && j < n_max; ++j) {
-          const int st = j % kStages;
-          for (int t = 0; t < 2; ++t) {
-            if (j >= n_t[t]) continue;
-            ok = mbar_wait(&p_full[t], j & 1, abort_flag, p.status, p.timeout_ns) &&
-                 mbar_wait(&o_ready[t], j & 1, abort_flag, p.status, p.timeout_ns);
-            if (!ok) break;
-            tc_fence_after();
-            issue_pv<DP>(tbase + 256 + t * DP, tbase + t * 128, va0 + st * L::kVBytes, j > 0);
-            tc_commit(&o_done[t]);
-            if (j + 1 < n_t[t]) {
-              const int st1 = (j + 1) % kStages;
-              ok = mbar_wait(&kv_full[st1], ((j + 1) / kStages) & 1, abort_flag, p.status,
-                             p.timeout_ns);
-              if (!ok) break;
-              tc_fence_after();
-              issue_qk<DP>(tbase + t * 128, qa + t * L::kQBytes, ka0 + st1 * L::kKBytes);
-              tc_commit(&s_full[t]);
-            }
-          }
+      if (ok) {
+        tc_fence_after();
+        issue_qk<DP>(ts, qa, ka0);
+        tc_commit(&s_full[t]);
+        tc_commit(&k_empty[0]);
+        issued = true;
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        if (j + 1 < n) {
+          // next QK^T into S_t as soon as the softmax has read S_t(j)
+          const int sk = (j + 1) % kKStages;
+          ok = mbar_wait(&s_free[t], j & 1, abort_flag, p.status, p.timeout_ns) &&
+               mbar_wait(&k_full[sk], ((j + 1) / kKStages) & 1, abort_flag, p.status,
+                         p.timeout_ns);
           if (!ok) break;
-          tc_commit(&kv_empty[st]);
+          tc_fence_after();
+          issue_qk<DP>(ts, qa, ka0 + sk * (L::kKBytes >> 4));
+          tc_commit(&s_full[t]);
+          tc_commit(&k_empty[sk]);
         }
+        const int sv = j % kVStages;
+        ok = mbar_wait(&v_full[sv], (j / kVStages) & 1, abort_flag, p.status, p.timeout_ns) &&
+             mbar_wait(&pv_ready[t], j & 1, abort_flag, p.status, p.timeout_ns);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv<DP>(to, pa, va0 + sv * (L::kVBytes >> 4), j > 0);
+        tc_commit(&o_done[t]);
+        tc_commit(&v_empty[sv]);
+      }
+      // key tiles the other query tile reads but this one does not (causal
+      // tile 0 skips the last one): release them once they have landed
+      for (int j = n; ok && j < n_max; ++j) {
+        ok = mbar_wait(&k_full[j % kKStages], (j / kKStages) & 1, abort_flag, p.status,
+                       p.timeout_ns) &&
+             mbar_wait(&v_full[j % kVStages], (j / kVStages) & 1, abort_flag, p.status,
+                       p.timeout_ns);
+        if (!ok) break;
+        mbar_arrive(&k_empty[j % kKStages]);
+        mbar_arrive(&v_empty[j % kVStages]);
       }
       if (issued) {   // every MMA must finish before TMEM is released
-        tc_commit(drain);
-        mbar_wait(drain, 0, nullptr, p.status, p.timeout_ns);
+        tc_commit(&drain[t]);
+        mbar_wait(&drain[t], 0, nullptr, p.status, p.timeout_ns);
       }
     }
   } else if (wg == 2) {
@@ -293,14 +333,15 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
     for (int j = 0; ok && j < n_max; ++j) {
       for (int t = 0; t < 2; ++t) {
         if (j >= n_t[t]) continue;
-        ok = wait_all(&alpha_ready[t], j & 1, abort_flag, p.status, p.timeout_ns);
+        ok = wait_all(&alpha_ready[2 * t + (j & 1)], (j >> 1) & 1, abort_flag, p.status,
+                      p.timeout_ns);
         if (!ok) break;
         if (j > 0) {
           // O_t holds PV of key tiles < j once PV(j-1) is done
           ok = wait_all(&o_done[t], (j - 1) & 1, abort_flag, p.status, p.timeout_ns);
           if (!ok) break;
           tc_fence_after();
-          const float alpha = alpha_s[t * kBlockM + r];
+          const float alpha = alpha_s[(2 * t + (j & 1)) * kBlockM + r];
           if (__any_sync(kFull, alpha < 1.0f)) {
             const uint32_t to = tbase + lane_off + 256 + t * DP;
 #pragma unroll 1
@@ -318,7 +359,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
           }
         }
         tc_fence_before();
-        mbar_arrive(&o_ready[t]);
+        mbar_arrive(&pv_ready[t]);
       }
     }
     // epilogue: out = O * s_v / (448 l), the caller's D channels only
@@ -372,6 +413,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int r = threadIdx.x - t * kBlockM;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t ts = tbase + lane_off + t * 128;
+    // this row of the P~ tile: 128 bytes, 16-byte chunks swizzled by row % 8
+    uint8_t* prow = smem + L::kPOff + t * L::kPBytes + r * 128;
+    const int rsw = r & 7;
     const int64_t qi = (qt0 + t) * kBlockM + r;          // query index in segment
     const int n = n_t[t];
     const float* skp = p.s_k + k_row0 / kBlockN;
@@ -396,6 +440,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
       reg_fence(sr[1]);
       reg_fence(sr[2]);
       reg_fence(sr[3]);
+      tc_fence_before();
+      mbar_arrive(&s_free[t]);                           // S_t may be overwritten
 
       // c > 0 keeps -inf * c = -inf for masked keys even when a scale is 0
       const float c = fmaxf((sq * sk) * p.scale_log2, 1e-30f);
@@ -420,35 +466,39 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
       const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
       const float m_new = fmaxf(m, m_tile);
       const float alpha = fast_exp2(m - m_new);          // 0 on the first tile
-      alpha_s[t * kBlockM + r] = alpha;
-      mbar_arrive(&alpha_ready[t]);                      // correction may rescale O now
+      alpha_s[(2 * t + (j & 1)) * kBlockM + r] = alpha;
+      mbar_arrive(&alpha_ready[2 * t + (j & 1)]);        // correction may rescale O now
 
-      // 448 P = 2^(S c - m' + log2 448), quantised to e4m3 into TMEM (over St)
+      // 448 P = 2^(S c - m' + log2 448), quantised to e4m3
       const float bias = kLog2_448 - m_new;
       float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+      uint32_t w[32];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t w[8];
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const int i = 4 * q4;
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[cc][i]), c, bias));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[cc][i + 1]), c, bias));
-          const float p2 = fast_exp2(fmaf(__uint_as_float(sr[cc][i + 2]), c, bias));
-          const float p3 = fast_exp2(fmaf(__uint_as_float(sr[cc][i + 3]), c, bias));
-          a0 += p0;
-          a1 += p1;
-          a2 += p2;
-          a3 += p3;
-          w[q4] = pack_e4m3x2(p0, p1) | (pack_e4m3x2(p2, p3) << 16);
-        }
-        tmem_st8(ts + 8 * cc, w);
+      for (int q4 = 0; q4 < 32; ++q4) {
+        const int i = 4 * q4;
+        const float p0 = fast_exp2(fmaf(__uint_as_float(sr[i >> 5][i & 31]), c, bias));
+        const float p1 = fast_exp2(fmaf(__uint_as_float(sr[i >> 5][(i & 31) + 1]), c, bias));
+        const float p2 = fast_exp2(fmaf(__uint_as_float(sr[i >> 5][(i & 31) + 2]), c, bias));
+        const float p3 = fast_exp2(fmaf(__uint_as_float(sr[i >> 5][(i & 31) + 3]), c, bias));
+        a0 += p0;
+        a1 += p1;
+        a2 += p2;
+        a3 += p3;
+        w[q4] = pack_e4m3x2(p0, p1) | (pack_e4m3x2(p2, p3) << 16);
       }
-      tmem_st_wait();
+      // the P~ buffer is free once PV(j-1) has read it
+      if (j > 0) {
+        ok = wait_all(&o_done[t], (j - 1) & 1, abort_flag, p.status, p.timeout_ns);
+        if (!ok) break;
+      }
+#pragma unroll
+      for (int c16 = 0; c16 < 8; ++c16)
+        *reinterpret_cast<uint4*>(prow + ((c16 ^ rsw) << 4)) =
+            make_uint4(w[4 * c16], w[4 * c16 + 1], w[4 * c16 + 2], w[4 * c16 + 3]);
+      fence_proxy_async_smem();
       l448 = l448 * alpha + ((a0 + a1) + (a2 + a3));
       m = m_new;
-      tc_fence_before();
-      mbar_arrive(&p_full[t]);
+      mbar_arrive(&pv_ready[t]);
     }
     if (ok && n > 0) {
       l_s[t * kBlockM + r] = l448;
@@ -503,7 +553,8 @@ debug_qk_kernel(const __grid_constant__ CUtensorMap tm_q,
     ok = mbar_wait(ld_full, 0, nullptr, status, timeout_ns);
     if (ok) {
       tc_fence_after();
-      issue_qk<DP>(tbase, smem_u32(smem + L::kQOff), smem_u32(smem + L::kKOff));
+      issue_qk<DP>(tbase, sdesc_sw128_lo(smem_u32(smem + L::kQOff)),
+                   sdesc_sw128_lo(smem_u32(smem + L::kKOff)));
       tc_commit(mma_done);
       ok = mbar_wait(mma_done, 0, nullptr, status, timeout_ns);
     }

@@ -207,6 +207,62 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
+// The same descriptor split in two 32-bit words: the low word carries the
+// start address (and the unused LBO), the high word is constant, so an MMA
+// loop only adds (offset >> 4) to the low word.
+__device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr) {
+  return ((saddr & 0x3FFFFu) >> 4) | (1u << 16);
+}
+constexpr uint32_t kSdescSw128Hi = (1024u >> 4) | (1u << 14) | (2u << 29);
+
+// D[tmem] (+)= A[smem] * B[smem]^T from low descriptor words, fp16 operands.
+__device__ __forceinline__ void mma_f16_ss_lo(uint32_t d_tmem, uint32_t a_lo,
+                                              uint32_t b_lo, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .b64 ad, bd;\n\t.reg .pred p;\n\t"
+      "mov.b64 ad, {%1, %5};\n\tmov.b64 bd, {%2, %5};\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, p;\n}"
+      :: "r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate),
+         "r"(kSdescSw128Hi)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T from a low descriptor word, e4m3 operands.
+__device__ __forceinline__ void mma_f8_ts_lo(uint32_t d_tmem, uint32_t a_tmem,
+                                             uint32_t b_lo, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .b64 bd;\n\t.reg .pred p;\n\t"
+      "mov.b64 bd, {%2, %5};\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], bd, %3, p;\n}"
+      :: "r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate),
+         "r"(kSdescSw128Hi)
+      : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T from low descriptor words, e4m3 operands.
+__device__ __forceinline__ void mma_f8_ss_lo(uint32_t d_tmem, uint32_t a_lo,
+                                             uint32_t b_lo, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .b64 ad, bd;\n\t.reg .pred p;\n\t"
+      "mov.b64 ad, {%1, %5};\n\tmov.b64 bd, {%2, %5};\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %3, p;\n}"
+      :: "r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate),
+         "r"(kSdescSw128Hi)
+      : "memory");
+}
+
+// Makes this thread's generic-proxy shared-memory writes visible to the
+// async proxy (tensor core, TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Instruction descriptor: fp32 accumulator, A/B format codes, K-major A and
 // B, N >> 3 at bit 17, M >> 4 at bit 24.
 __host__ __device__ constexpr uint32_t make_idesc(uint32_t a_fmt,
