@@ -50,7 +50,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Byte offsets of every workspace buffer.
 struct WsLayout {
-  size_t status, ksum, vmax, zero_end, k_mean, s_v, v_inv, s_q, s_k, q16, k16,
+  size_t status, ksum, vmax, done, zero_end, k_mean, s_v, v_inv, s_q, s_k, q16, k16,
       v8, total;
 };
 
@@ -64,10 +64,12 @@ WsLayout ws_layout(const SegGeo& g) {
   w.status = o; o += 256;
   w.ksum = o; o = align256(o + nstat * 8);
   w.vmax = o; o = align256(o + nstat * 4);
-  w.zero_end = o;
+  w.done = o; o = align256(o + g.nseg * g.Hkv * 4);
+  // means and scales start at zero: a segment without keys keeps them so
   w.k_mean = o; o = align256(o + nstat * 4);
   w.s_v = o; o = align256(o + nstat * 4);
   w.v_inv = o; o = align256(o + nstat * 4);
+  w.zero_end = o;
   w.s_q = o; o = align256(o + q_rows * 4);
   w.s_k = o; o = align256(o + (k_rows / 128) * 4);
   w.q16 = o; o = align256(o + q_rows * g.Dp * 2);
@@ -254,6 +256,7 @@ sage_status run_prologue(const SegGeo& g, const void* q, const void* k, const vo
   b.v_inv = reinterpret_cast<float*>(wsb + w.v_inv);
   b.ksum = wsb + w.ksum;
   b.vmax = reinterpret_cast<uint32_t*>(wsb + w.vmax);
+  b.done = reinterpret_cast<uint32_t*>(wsb + w.done);
   b.status = reinterpret_cast<uint32_t*>(wsb + w.status);
   const bool vec = (g.D % 8 == 0) && aligned(q, 16) && aligned(k, 16) && aligned(v, 16);
   e = launch_prologue(g, b, vec, st);

@@ -222,7 +222,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
     regs_decrease<kMiscRegs>();
     if (warp == 12 && lane == 0) {
       // ============================================== TMA producer: Q and K
-      mbar_expect_tx(q_full, (n_t[1] > 0 ? 2 : 1) * L::kQBytes);
+      if (n_max > 0) mbar_expect_tx(q_full, (n_t[1] > 0 ? 2 : 1) * L::kQBytes);
       for (int t = 0; t < 2; ++t) {
         if (n_t[t] == 0) continue;
         for (int a = 0; a < DP / 64; ++a)
@@ -245,7 +245,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
         last = j;
       }
       // no copy may still be in flight when the CTA exits
-      mbar_wait(q_full, 0, nullptr, p.status, p.timeout_ns);
+      if (n_max > 0) mbar_wait(q_full, 0, nullptr, p.status, p.timeout_ns);
       for (int j = max(0, last - kKStages + 1); j <= last; ++j)
         if (j != p.skip_kv_tile)
           mbar_wait(&k_full[j % kKStages], (j / kKStages) & 1, nullptr, p.status,
@@ -366,16 +366,21 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int D = static_cast<int>(g.D);
     const int64_t seg_off = g.varlen ? qstart * p.out_tok_stride : s * p.out_seg_stride;
     for (int t = 0; ok && t < 2; ++t) {
-      if (n_t[t] == 0) continue;
+      if ((qt0 + t) * kBlockM >= len_q) continue;
+      const int64_t qi = (qt0 + t) * kBlockM + r;
+      float* orow = p.out + seg_off + h * p.out_head_stride + qi * p.out_tok_stride;
+      if (n_t[t] == 0) {          // no visible key (empty key sequence): zeros
+        if (qi < len_q)
+          for (int c = 0; c < D; ++c) orow[c] = 0.0f;
+        continue;
+      }
       ok = wait_all(&o_done[t], (n_t[t] - 1) & 1, abort_flag, p.status, p.timeout_ns) &&
            wait_all(&l_ready[t], 0, abort_flag, p.status, p.timeout_ns);
       if (!ok) break;
       tc_fence_after();
       const float l448 = l_s[t * kBlockM + r];
       const float inv = l448 > 0.0f ? __fdiv_rn(1.0f, l448) : 0.0f;
-      const int64_t qi = (qt0 + t) * kBlockM + r;
       const bool valid = qi < len_q;
-      float* orow = p.out + seg_off + h * p.out_head_stride + qi * p.out_tok_stride;
       const bool vec = (D % 4 == 0) && ((reinterpret_cast<uintptr_t>(orow) & 15) == 0);
 #pragma unroll 1
       for (int cc = 0; cc < DP / 32; ++cc) {

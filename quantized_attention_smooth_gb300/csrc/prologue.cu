@@ -53,44 +53,22 @@ __device__ __forceinline__ float to_f32(uint16_t bits, bool bf16) {
 // L2 cache policies: keep the first pass over K/V resident for the second.
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
 
+// Read-only 16-byte load with an L2 policy.  Not volatile: the compiler may
+// schedule it early (the inputs are never written by the prologue).
 __device__ __forceinline__ uint4 ld16(const void* p, uint64_t pol) {
   uint4 u;
-  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w) : "l"(p), "l"(pol));
+  asm("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+      : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w) : "l"(p), "l"(pol));
   return u;
-}
-
-// Loads channels c0..c0+7 of one token row (zeros for channels >= D).
-template <bool kVec>
-__device__ __forceinline__ void load8(const uint16_t* row, int c0, int D,
-                                      bool bf16, float (&x)[8], uint64_t pol) {
-  if (kVec) {
-    if (c0 < D) {
-      const uint4 u = ld16(row + c0, pol);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        x[2 * i] = to_f32(static_cast<uint16_t>(w[i] & 0xFFFFu), bf16);
-        x[2 * i + 1] = to_f32(static_cast<uint16_t>(w[i] >> 16), bf16);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = 0.0f;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      x[i] = (c0 + i < D) ? to_f32(row[c0 + i], bf16) : 0.0f;
-  }
 }
 
 // Two int8 codes clamp(rint(x * inv), -127, 127) as a pair of exact fp16
@@ -101,6 +79,24 @@ __device__ __forceinline__ uint32_t code_f16x2(float x0, float x1, float inv) {
   const float r1 = fminf(fmaxf((__fmul_rn(x1, inv) + 12582912.0f) - 12582912.0f, -127.0f), 127.0f);
   const __half2 hv = __floats2half2_rn(r0, r1);
   return *reinterpret_cast<const uint32_t*>(&hv);
+}
+
+// Channels c0..c0+7 of one token row as four packed 16-bit pairs (zeros for
+// channels >= D).
+template <bool kVec>
+__device__ __forceinline__ uint4 load8_raw(const uint16_t* row, int c0, int D, uint64_t pol) {
+  if constexpr (kVec) {
+    return c0 < D ? ld16(row + c0, pol) : make_uint4(0u, 0u, 0u, 0u);
+  } else {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = (c0 + 2 * i < D) ? row[c0 + 2 * i] : 0u;
+      const uint32_t hi = (c0 + 2 * i + 1 < D) ? row[c0 + 2 * i + 1] : 0u;
+      w[i] = lo | (hi << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -114,7 +110,8 @@ template <bool kVec, bool kBf16>
 __global__ void __launch_bounds__(kThreads)
 kv_stats_kernel(SegGeo g, const uint16_t* __restrict__ k,
                 const uint16_t* __restrict__ v, void* ksum,
-                uint32_t* __restrict__ vmax, uint32_t* status, int h_base) {
+                uint32_t* __restrict__ vmax, uint32_t* status, int h_base,
+                uint32_t* done, float* k_mean, float* s_v, float* v_inv) {
   const int64_t s = blockIdx.z, h = h_base + blockIdx.y;
   int64_t start = 0, len = g.Lk;
   if (g.varlen && !seg_range(g.cu_k, s, g.total_k, g.max_k, &start, &len)) {
@@ -141,57 +138,108 @@ kv_stats_kernel(SegGeo g, const uint16_t* __restrict__ k,
   for (int i = 0; i < 8; ++i) { hs[i] = 0; ls[i] = 0; dsum[i] = 0.0; am[i] = 0.0f; }
   const uint64_t keep = policy_evict_last();
 
-#pragma unroll 4
-  for (int64_t t = t0 + r; t < t1; t += R) {
-    float kx[8], vx[8];
-    load8<kVec>(k + base + t * g.k_tok_stride, c0, static_cast<int>(g.D), kBf16, kx, keep);
-    load8<kVec>(v + base + t * g.k_tok_stride, c0, static_cast<int>(g.D), kBf16, vx, keep);
+  const int D = static_cast<int>(g.D);
+  for (int64_t tb = t0 + r; tb < t1; tb += 8 * R) {
+    uint4 kr[8], vr[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (kBf16) {
-        dsum[i] += static_cast<double>(kx[i]);
-      } else {
-        const float tr = fmaf(kx[i], 16.0f, 12582912.0f);     // 1.5*2^23 + rint(16 k)
-        const float hi_f = tr - 12582912.0f;
-        const float lo_f = fmaf(kx[i], 16777216.0f, hi_f * -1048576.0f);
-        hs[i] += __float_as_int(tr) - 0x4B400000;
-        ls[i] += __float_as_int(lo_f + 12582912.0f) - 0x4B400000;
+    for (int u = 0; u < 8; ++u) {                // 16 loads in flight per thread
+      const int64_t t = tb + u * R;
+      const bool in = t < t1;
+      kr[u] = in ? load8_raw<kVec>(k + base + t * g.k_tok_stride, c0, D, keep)
+                 : make_uint4(0u, 0u, 0u, 0u);
+      vr[u] = in ? load8_raw<kVec>(v + base + t * g.k_tok_stride, c0, D, keep)
+                 : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint32_t kw[4] = {kr[u].x, kr[u].y, kr[u].z, kr[u].w};
+      const uint32_t vw[4] = {vr[u].x, vr[u].y, vr[u].z, vr[u].w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float kx = to_f32(static_cast<uint16_t>(kw[i >> 1] >> (16 * (i & 1))), kBf16);
+        const float vx = to_f32(static_cast<uint16_t>(vw[i >> 1] >> (16 * (i & 1))), kBf16);
+        if (kBf16) {
+          dsum[i] += static_cast<double>(kx);
+        } else {
+          const float tr = fmaf(kx, 16.0f, 12582912.0f);      // 1.5*2^23 + rint(16 k)
+          const float hi_f = tr - 12582912.0f;
+          const float lo_f = fmaf(kx, 16777216.0f, hi_f * -1048576.0f);
+          hs[i] += __float_as_int(tr) - 0x4B400000;
+          ls[i] += __float_as_int(lo_f + 12582912.0f) - 0x4B400000;
+        }
+        am[i] = fmaxf(am[i], fabsf(vx));
       }
-      am[i] = fmaxf(am[i], fabsf(vx[i]));
     }
   }
 
-  __shared__ long long red_i[kThreads][8];
-  __shared__ float red_a[kThreads][8];
+  // reduce the rows: lanes holding the same channels first (warp shuffles),
+  // then the eight warps through shared memory, one channel per thread
+  long long part[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    red_i[threadIdx.x][i] = kBf16 ? __double_as_longlong(dsum[i])
-                                  : static_cast<long long>(hs[i]) * 1048576ll + ls[i];
-    red_a[threadIdx.x][i] = am[i];
-  }
-  __syncthreads();
-  if (r == 0) {
-    long long isum[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) isum[i] = red_i[threadIdx.x][i];
-    for (int rr = 1; rr < R; ++rr) {
-      const int src = rr * G + lc;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (kBf16) dsum[i] += __longlong_as_double(red_i[src][i]);
-        else isum[i] += red_i[src][i];
-        am[i] = fmaxf(am[i], red_a[src][i]);
-      }
-    }
-    const int64_t o = (s * g.Hkv + h) * g.Dp + c0;
+  for (int i = 0; i < 8; ++i)
+    part[i] = kBf16 ? __double_as_longlong(dsum[i])
+                    : static_cast<long long>(hs[i]) * 1048576ll + ls[i];
+  for (int o = G; o < 32; o <<= 1) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      if (c0 + i >= g.D) break;
-      if (kBf16) atomicAdd(reinterpret_cast<double*>(ksum) + o + i, dsum[i]);
-      else atomicAdd(reinterpret_cast<unsigned long long*>(ksum) + o + i,
-                     static_cast<unsigned long long>(isum[i]));
-      atomicMax(vmax + o + i, __float_as_uint(am[i]));   // am >= +0
+      const long long other = __shfl_xor_sync(0xFFFFFFFFu, part[i], o);
+      if (kBf16) part[i] = __double_as_longlong(__longlong_as_double(part[i]) +
+                                                __longlong_as_double(other));
+      else part[i] += other;
+      am[i] = fmaxf(am[i], __shfl_xor_sync(0xFFFFFFFFu, am[i], o));
     }
+  }
+  __shared__ long long red_i[kThreads / 32][128];
+  __shared__ float red_a[kThreads / 32][128];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if (lane < G) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      red_i[wid][c0 + i] = part[i];
+      red_a[wid][c0 + i] = am[i];
+    }
+  }
+  __syncthreads();
+  const int64_t obase = (s * g.Hkv + h) * g.Dp;
+  if (threadIdx.x < g.D) {
+    const int c = threadIdx.x;
+    long long si = 0;
+    double sd = 0.0;
+    float a = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+      if (kBf16) sd += __longlong_as_double(red_i[w][c]);
+      else si += red_i[w][c];
+      a = fmaxf(a, red_a[w][c]);
+    }
+    if (kBf16) atomicAdd(reinterpret_cast<double*>(ksum) + obase + c, sd);
+    else atomicAdd(reinterpret_cast<unsigned long long*>(ksum) + obase + c,
+                   static_cast<unsigned long long>(si));
+    atomicMax(vmax + obase + c, __float_as_uint(a));   // a >= +0
+    if (done != nullptr) __threadfence();
+  }
+  if (done == nullptr) return;
+  // The last CTA of this (segment, kv head) turns the sums into the K mean
+  // and the V scales (the finalize step) while the sums are hot in L2.
+  __shared__ int last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t chunks = static_cast<uint32_t>((len + kStatsChunk - 1) / kStatsChunk);
+    last = atomicAdd(done + s * g.Hkv + h, 1u) == chunks - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  for (int c = threadIdx.x; c < g.Dp; c += kThreads) {
+    const int64_t i = (s * g.Hkv + h) * g.Dp + c;
+    double S;
+    if (kBf16) S = __longlong_as_double(__ldcg(reinterpret_cast<const long long*>(ksum) + i));
+    else S = __ll2double_rn(__ldcg(reinterpret_cast<const long long*>(ksum) + i)) *
+             5.9604644775390625e-08;   // 2^-24, exact
+    k_mean[i] = __double2float_rn(__ddiv_rn(S, static_cast<double>(len)));
+    const float a = __uint_as_float(__ldcg(vmax + i));
+    s_v[i] = __fdiv_rn(a, 448.0f);
+    v_inv[i] = a > 0.0f ? __fdiv_rn(448.0f, a) : 0.0f;
   }
 }
 
@@ -220,6 +268,60 @@ __global__ void kv_finalize_kernel(SegGeo g, const void* ksum,
   v_inv[i] = a > 0.0f ? __fdiv_rn(448.0f, a) : 0.0f;
 }
 
+// ------------------------------------------------------------- Q quant
+// One 128-token tile of Q of query head h in segment s.
+template <bool kVec, bool kBf16>
+__device__ __forceinline__ void quant_q_tile(const SegGeo& g, const uint16_t* __restrict__ q,
+                                             uint16_t* __restrict__ q16,
+                                             float* __restrict__ s_q, uint32_t* status,
+                                             int64_t s, int64_t h, int64_t qt) {
+  int64_t start = 0, len = g.Lq;
+  if (g.varlen && !seg_range(g.cu_q, s, g.total_q, g.max_q, &start, &len)) {
+    if (threadIdx.x == 0 && qt == 0 && h == 0) atomicOr(status, kStatusBadSeqlens);
+    return;
+  }
+  const int64_t t0 = qt * kBlockM;
+  if (t0 >= len) return;
+  const int G = static_cast<int>(g.Dp / 8);
+  const int lc = threadIdx.x % G, r = threadIdx.x / G, R = kThreads / G;
+  const int c0 = lc * 8;
+  const int D = static_cast<int>(g.D);
+  const int64_t in_base = (g.varlen ? start * g.q_tok_stride : s * g.q_seg_stride) +
+                          h * g.q_head_stride;
+  const int64_t row0 = ws_seg_base(g.varlen, s, start, g.Hq, g.q_head_rows) +
+                       h * g.q_head_rows + t0;
+  const uint64_t once = policy_evict_first();
+  const int P = kBlockM / R;                   // rows per thread: 8 (Dp 128) or 4 (Dp 64)
+  uint4 raw[8];
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {                // all loads first: one round trip
+    if (p >= P) break;
+    const int64_t t = t0 + r + p * R;
+    raw[p] = t < len ? load8_raw<kVec>(q + in_base + t * g.q_tok_stride, c0, D, once)
+                     : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    if (p >= P) break;
+    const int64_t rr = r + p * R;
+    const uint32_t w[4] = {raw[p].x, raw[p].y, raw[p].z, raw[p].w};
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      x[i] = to_f32(static_cast<uint16_t>(w[i >> 1] >> (16 * (i & 1))), kBf16);
+    float am = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(x[i]));
+    for (int o = G / 2; o > 0; o >>= 1)
+      am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
+    const float inv = am > 0.0f ? __fdiv_rn(127.0f, am) : 0.0f;
+    *reinterpret_cast<uint4*>(q16 + (row0 + rr) * g.Dp + c0) =
+        make_uint4(code_f16x2(x[0], x[1], inv), code_f16x2(x[2], x[3], inv),
+                   code_f16x2(x[4], x[5], inv), code_f16x2(x[6], x[7], inv));
+    if (lc == 0) s_q[row0 + rr] = __fdiv_rn(am, 127.0f);
+  }
+}
+
 // ---------------------------------------------------------- K/V quant
 // One CTA quantises one 128-token block of K (role 0) or of V (role 1) of one
 // (segment, kv head); blocks are numbered ((s * h_count + hh) * nkb + kb) * 2
@@ -231,7 +333,20 @@ kv_quant_kernel(SegGeo g, const uint16_t* __restrict__ k,
                 const float* __restrict__ k_mean,
                 const float* __restrict__ v_inv, uint16_t* __restrict__ k16,
                 float* __restrict__ s_k, uint8_t* __restrict__ v8,
-                int h_base, int h_count, int nkb) {
+                int h_base, int h_count, int nkb,
+                const uint16_t* __restrict__ q, uint16_t* __restrict__ q16,
+                float* __restrict__ s_q, uint32_t* status, int nqt) {
+  const int64_t nkv = static_cast<int64_t>(g.nseg) * h_count * nkb * 2;
+  if (static_cast<int64_t>(blockIdx.x) >= nkv) {
+    // Q tiles of the query heads that read this group's kv heads
+    const int64_t grp = g.Hq / g.Hkv;
+    const int64_t qb = blockIdx.x - nkv;
+    const int64_t qt = qb % nqt;
+    const int64_t hq = h_base * grp + (qb / nqt) % (h_count * grp);
+    const int64_t sq = qb / (static_cast<int64_t>(nqt) * h_count * grp);
+    quant_q_tile<kVec, kBf16>(g, q, q16, s_q, status, sq, hq, qt);
+    return;
+  }
   const int role = blockIdx.x & 1;
   const int64_t blk = blockIdx.x >> 1;
   const int64_t kb = blk % nkb;
@@ -253,28 +368,35 @@ kv_quant_kernel(SegGeo g, const uint16_t* __restrict__ k,
   const uint64_t last_use = policy_evict_first();
 
   if (role == 0) {
-    // ---- K: smoothing and one int8 scale per 128-token block
+    // ---- K: smoothing and one int8 scale per 128-token block.  The raw
+    // values stay packed (16-bit) in registers; k - mean is recomputed (the
+    // same IEEE subtraction) in the amax and in the quantisation pass.
     __shared__ float red[kThreads / 32];
     const int64_t row0 = ws_seg_base(g.varlen, s, start, g.Hkv, g.k_head_rows) +
                          h * g.k_head_rows + t0;
-    float mean[8], kh[8][8];
+    float mean[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) mean[i] = (c0 + i < D) ? k_mean[stat + i] : 0.0f;
-    float am = 0.0f;
+    uint4 raw[8];
+    bool valid[8];
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
       if (p >= P) break;
       const int64_t t = t0 + r + p * R;
-      float x[8];
-      if (t < len) load8<kVec>(k + in_base + t * g.k_tok_stride, c0, D, kBf16, x, last_use);
-      else {
+      valid[p] = t < len;
+      raw[p] = valid[p] ? load8_raw<kVec>(k + in_base + t * g.k_tok_stride, c0, D, last_use)
+                        : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float am = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = 0.0f;
-      }
+    for (int p = 0; p < 8; ++p) {
+      if (p >= P) break;
+      const uint32_t w[4] = {raw[p].x, raw[p].y, raw[p].z, raw[p].w};
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        kh[p][i] = (t < len && c0 + i < D) ? __fsub_rn(x[i], mean[i]) : 0.0f;
-        am = fmaxf(am, fabsf(kh[p][i]));
+        const float x = to_f32(static_cast<uint16_t>(w[i >> 1] >> (16 * (i & 1))), kBf16);
+        const float kh = (valid[p] && c0 + i < D) ? __fsub_rn(x, mean[i]) : 0.0f;
+        am = fmaxf(am, fabsf(kh));
       }
     }
     am = warp_max(am);
@@ -288,41 +410,56 @@ kv_quant_kernel(SegGeo g, const uint16_t* __restrict__ k,
     for (int p = 0; p < 8; ++p) {
       if (p >= P) break;
       const int64_t rr = r + p * R;
-      uint32_t w[4];
+      const uint32_t w[4] = {raw[p].x, raw[p].y, raw[p].z, raw[p].w};
+      float kh[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        w[i] = code_f16x2(kh[p][2 * i], kh[p][2 * i + 1], kinv);
+      for (int i = 0; i < 8; ++i) {
+        const float x = to_f32(static_cast<uint16_t>(w[i >> 1] >> (16 * (i & 1))), kBf16);
+        kh[i] = (valid[p] && c0 + i < D) ? __fsub_rn(x, mean[i]) : 0.0f;
+      }
       *reinterpret_cast<uint4*>(k16 + (row0 + rr) * g.Dp + c0) =
-          make_uint4(w[0], w[1], w[2], w[3]);
+          make_uint4(code_f16x2(kh[0], kh[1], kinv), code_f16x2(kh[2], kh[3], kinv),
+                     code_f16x2(kh[4], kh[5], kinv), code_f16x2(kh[6], kh[7], kinv));
     }
     if (threadIdx.x == 0) s_k[row0 / kBlockN] = __fdiv_rn(am, 127.0f);
   } else {
     // ---- V: e4m3 per channel, transposed to [channel][token].  A thread
     // quantises 8 channels of 4 consecutive tokens and packs, per channel, the
     // 4 token bytes into one word; word (c, w) of the shared tile sits at
-    // c * 32 + (w ^ (c / 8 % 32)) so that writes and row reads spread banks.
-    __shared__ uint32_t vt[128 * 32];
+    // c * 32 + (w ^ 4 * (c / 8 % 8)), which spreads the writes over banks and
+    // keeps every group of four words (16 bytes of a row) contiguous.
+    __shared__ __align__(16) uint32_t vt[128 * 32];
     float vinv[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) vinv[i] = (c0 + i < D) ? v_inv[stat + i] : 0.0f;
     const int RG = kThreads / G;                 // 4-token groups per pass
-    for (int tw = r; tw < kBlockN / 4; tw += RG) {
+    const int NTW = (kBlockN / 4) / RG;          // groups per thread: 2 (Dp 128) or 1
+    uint4 raw[2][4];
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {                // all loads first: one round trip
+      if (a >= NTW) break;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int64_t t = t0 + 4 * (r + a * RG) + e;
+        raw[a][e] = t < len ? load8_raw<kVec>(v + in_base + t * g.k_tok_stride, c0, D, last_use)
+                            : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+      if (a >= NTW) break;
+      const int tw = r + a * RG;
       uint32_t word[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) word[i] = 0u;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int64_t t = t0 + 4 * tw + e;
-        float x[8];
-        if (t < len) load8<kVec>(v + in_base + t * g.k_tok_stride, c0, D, kBf16, x, last_use);
-        else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) x[i] = 0.0f;
-        }
+        const uint32_t w[4] = {raw[a][e].x, raw[a][e].y, raw[a][e].z, raw[a][e].w};
 #pragma unroll
         for (int i = 0; i < 8; i += 2) {
-          const uint32_t two = pack_e4m3x2(__fmul_rn(x[i], vinv[i]),
-                                           __fmul_rn(x[i + 1], vinv[i + 1]));
+          const float x0 = to_f32(static_cast<uint16_t>(w[i >> 1] & 0xFFFFu), kBf16);
+          const float x1 = to_f32(static_cast<uint16_t>(w[i >> 1] >> 16), kBf16);
+          const uint32_t two = pack_e4m3x2(__fmul_rn(x0, vinv[i]), __fmul_rn(x1, vinv[i + 1]));
           word[i] |= (two & 0xFFu) << (8 * e);
           word[i + 1] |= (two >> 8) << (8 * e);
         }
@@ -330,65 +467,18 @@ kv_quant_kernel(SegGeo g, const uint16_t* __restrict__ k,
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int c = c0 + i;
-        vt[c * 32 + (tw ^ ((c >> 3) & 31))] = word[i];
+        vt[c * 32 + (tw ^ (((c >> 3) & 7) << 2))] = word[i];
       }
     }
     __syncthreads();
     const int64_t vrow0 = (g.varlen ? 0 : s * g.Hkv * g.Dp) + h * g.Dp;
     const int64_t vcol0 = (g.varlen ? ws_seg_base(1, s, start, 0, 0) : 0) + t0;
-    const int words = static_cast<int>(g.Dp) * (kBlockN / 4);
-    for (int wi = threadIdx.x; wi < words; wi += kThreads) {
-      const int c = wi / (kBlockN / 4), tw = wi % (kBlockN / 4);
-      const uint32_t val = vt[c * 32 + (tw ^ ((c >> 3) & 31))];
-      *reinterpret_cast<uint32_t*>(v8 + (vrow0 + c) * g.v_cols + vcol0 + 4 * tw) = val;
+    const int quads = static_cast<int>(g.Dp) * (kBlockN / 16);   // 16-byte pieces
+    for (int qi = threadIdx.x; qi < quads; qi += kThreads) {
+      const int c = qi / (kBlockN / 16), tw = 4 * (qi % (kBlockN / 16));
+      const uint4 val = *reinterpret_cast<const uint4*>(&vt[c * 32 + (tw ^ (((c >> 3) & 7) << 2))]);
+      *reinterpret_cast<uint4*>(v8 + (vrow0 + c) * g.v_cols + vcol0 + 4 * tw) = val;
     }
-  }
-}
-
-// ------------------------------------------------------------- Q quant
-template <bool kVec, bool kBf16>
-__global__ void __launch_bounds__(kThreads)
-q_quant_kernel(SegGeo g, const uint16_t* __restrict__ q,
-               uint16_t* __restrict__ q16, float* __restrict__ s_q,
-               uint32_t* status) {
-  const int64_t s = blockIdx.z, h = blockIdx.y;
-  int64_t start = 0, len = g.Lq;
-  if (g.varlen && !seg_range(g.cu_q, s, g.total_q, g.max_q, &start, &len)) {
-    if (threadIdx.x == 0 && blockIdx.x == 0 && h == 0) atomicOr(status, kStatusBadSeqlens);
-    return;
-  }
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kBlockM;
-  if (t0 >= len) return;
-  const int G = static_cast<int>(g.Dp / 8);
-  const int lc = threadIdx.x % G, r = threadIdx.x / G, R = kThreads / G;
-  const int c0 = lc * 8;
-  const int D = static_cast<int>(g.D);
-  const int64_t in_base = (g.varlen ? start * g.q_tok_stride : s * g.q_seg_stride) +
-                          h * g.q_head_stride;
-  const int64_t row0 = ws_seg_base(g.varlen, s, start, g.Hq, g.q_head_rows) +
-                       h * g.q_head_rows + t0;
-  const uint64_t once = policy_evict_first();
-  for (int rr = r; rr < kBlockM; rr += R) {
-    const int64_t t = t0 + rr;
-    float x[8];
-    if (t < len) load8<kVec>(q + in_base + t * g.q_tok_stride, c0, D, kBf16, x, once);
-    else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = 0.0f;
-    }
-    float am = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(x[i]));
-    for (int o = G / 2; o > 0; o >>= 1)
-      am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
-    const float inv = am > 0.0f ? __fdiv_rn(127.0f, am) : 0.0f;
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      w[i] = code_f16x2(x[2 * i], x[2 * i + 1], inv);
-    *reinterpret_cast<uint4*>(q16 + (row0 + rr) * g.Dp + c0) =
-        make_uint4(w[0], w[1], w[2], w[3]);
-    if (lc == 0) s_q[row0 + rr] = __fdiv_rn(am, 127.0f);
   }
 }
 
@@ -402,31 +492,30 @@ cudaError_t launch_prologue_t(const SegGeo& g, const PrologueBuffers& b,
   const dim3 blk(kThreads);
   const int64_t maxk = g.varlen ? g.max_k : g.Lk;
   const int64_t maxq = g.varlen ? g.max_q : g.Lq;
-  if (maxk > 0) {
-    const int64_t tokens = g.varlen ? g.total_k : g.nseg * g.Lk;
-    const int64_t head_bytes = tokens * g.D * 2 * 2;          // K and V, one kv head
-    int64_t group = head_bytes > 0 ? kL2GroupBytes / head_bytes : g.Hkv;
-    if (group < 1) group = 1;
-    if (group > g.Hkv) group = g.Hkv;
-    const int nkb = static_cast<int>((maxk + kBlockN - 1) / kBlockN);
-    for (int64_t h0 = 0; h0 < g.Hkv; h0 += group) {
-      const int hc = static_cast<int>(g.Hkv - h0 < group ? g.Hkv - h0 : group);
+  const int nqt = static_cast<int>((maxq + kBlockM - 1) / kBlockM);
+  const int64_t grp = g.Hq / g.Hkv;
+  const int64_t tokens = g.varlen ? g.total_k : g.nseg * g.Lk;
+  const int64_t head_bytes = tokens * g.D * 2 * 2;            // K and V, one kv head
+  int64_t group = head_bytes > 0 ? kL2GroupBytes / head_bytes : g.Hkv;
+  if (group < 1) group = 1;
+  if (group > g.Hkv) group = g.Hkv;
+  const int nkb = maxk > 0 ? static_cast<int>((maxk + kBlockN - 1) / kBlockN) : 0;
+  for (int64_t h0 = 0; h0 < g.Hkv; h0 += group) {
+    const int hc = static_cast<int>(g.Hkv - h0 < group ? g.Hkv - h0 : group);
+    if (maxk > 0) {
       dim3 gs(static_cast<unsigned>((maxk + kStatsChunk - 1) / kStatsChunk),
               static_cast<unsigned>(hc), static_cast<unsigned>(g.nseg));
-      kv_stats_kernel<kVec, kBf16><<<gs, blk, 0, st>>>(g, b.k, b.v, b.ksum, b.vmax,
-                                                        b.status, static_cast<int>(h0));
-      const int64_t nstat = g.nseg * hc * g.Dp;
-      kv_finalize_kernel<<<static_cast<unsigned>((nstat + 255) / 256), 256, 0, st>>>(
-          g, b.ksum, b.vmax, b.k_mean, b.s_v, b.v_inv, static_cast<int>(h0), hc);
-      const int64_t nblk = g.nseg * hc * static_cast<int64_t>(nkb) * 2;
-      kv_quant_kernel<kVec, kBf16><<<static_cast<unsigned>(nblk), blk, 0, st>>>(
-          g, b.k, b.v, b.k_mean, b.v_inv, b.k16, b.s_k, b.v8, static_cast<int>(h0), hc, nkb);
+      kv_stats_kernel<kVec, kBf16><<<gs, blk, 0, st>>>(g, b.k, b.v, b.ksum, b.vmax, b.status,
+                                                        static_cast<int>(h0), b.done,
+                                                        b.k_mean, b.s_v, b.v_inv);
     }
-  }
-  if (maxq > 0) {
-    dim3 gq(static_cast<unsigned>((maxq + kBlockM - 1) / kBlockM),
-            static_cast<unsigned>(g.Hq), static_cast<unsigned>(g.nseg));
-    q_quant_kernel<kVec, kBf16><<<gq, blk, 0, st>>>(g, b.q, b.q16, b.s_q, b.status);
+    // K/V blocks of this head group, then the Q tiles of its query heads
+    const int64_t nblk = g.nseg * hc * static_cast<int64_t>(nkb) * 2 +
+                         g.nseg * hc * grp * static_cast<int64_t>(nqt);
+    if (nblk > 0)
+      kv_quant_kernel<kVec, kBf16><<<static_cast<unsigned>(nblk), blk, 0, st>>>(
+          g, b.k, b.v, b.k_mean, b.v_inv, b.k16, b.s_k, b.v8, static_cast<int>(h0), hc, nkb,
+          b.q, b.q16, b.s_q, b.status, nqt);
   }
   return cudaGetLastError();
 }
@@ -464,7 +553,8 @@ void launch_stats_only(const SegGeo& g, const uint16_t* k, const uint16_t* v,
   if (g.Lk > 0) {
     dim3 gs(static_cast<unsigned>((g.Lk + kStatsChunk - 1) / kStatsChunk),
             static_cast<unsigned>(g.Hkv), static_cast<unsigned>(g.nseg));
-    kv_stats_kernel<kVec, kBf16><<<gs, kThreads, 0, st>>>(g, k, v, ksum, vmax, status, 0);
+    kv_stats_kernel<kVec, kBf16><<<gs, kThreads, 0, st>>>(g, k, v, ksum, vmax, status, 0,
+                                                           nullptr, nullptr, nullptr, nullptr);
   }
   const int64_t nstat = g.nseg * g.Hkv * g.Dp;
   kv_finalize_kernel<<<static_cast<unsigned>((nstat + 255) / 256), 256, 0, st>>>(

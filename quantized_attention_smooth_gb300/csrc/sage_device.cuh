@@ -46,6 +46,14 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
                :: "r"(smem_u32(bar)) : "memory");
 }
 
+// Arrive once `after` is computed: the input operand keeps the compiler from
+// hoisting the arrive above the register arithmetic that produces it.
+__device__ __forceinline__ void mbar_arrive_after(uint64_t* bar, float after) {
+  asm volatile("{\n\t.reg .f32 dep;\n\tmov.f32 dep, %1;\n\t"
+               "mbarrier.arrive.shared::cta.b64 _, [%0];\n}"
+               :: "r"(smem_u32(bar)), "f"(after) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

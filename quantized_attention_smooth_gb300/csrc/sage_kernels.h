@@ -23,6 +23,7 @@ struct PrologueBuffers {
   float* v_inv;
   void* ksum;        // int64 (fp16 inputs) or double (bf16), [nseg][Hkv][Dp]
   uint32_t* vmax;    // float bits, [nseg][Hkv][Dp]
+  uint32_t* done;    // stats chunks finished per (segment, kv head), zeroed
   uint32_t* status;
 };
 

@@ -58,6 +58,8 @@ SMALL = [
            seqlens_q=(1, 130, 257, 128), seqlens_k=(5, 128, 300, 1)),
     _small("varlen_causal", B=0, Hq=2, Hkv=2, Lq=0, Lk=0, D=40, layout=wl.NHD, seed=19,
            causal=True, seqlens_q=(200, 64, 333), seqlens_k=(200, 64, 333)),
+    _small("varlen_empty_keys", B=0, Hq=4, Hkv=2, Lq=0, Lk=0, D=64, layout=wl.NHD, seed=20,
+           seqlens_q=(130, 7, 256), seqlens_k=(140, 0, 129)),
 ]
 
 
