@@ -113,14 +113,13 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- GPU arm
 def count_launches(torch, fn) -> int:
-    """Kernels of this library launched by one call of fn (CUPTI trace)."""
-    from torch.profiler import ProfilerActivity, profile
-    with profile(activities=[ProfilerActivity.CUDA]) as prof:
-        fn()
-        torch.cuda.synchronize()
-    ours = ("attn_kernel", "kv_stats_kernel", "kv_quant_kernel", "kv_finalize_kernel",
-            "q_quant_kernel")
-    return sum(1 for e in prof.events() if any(o in e.name for o in ours))
+    """Kernels of this library launched by one call of fn (the library's own
+    host-side launch counter)."""
+    from quantized_attention_smooth_gb300 import sage
+    before = sage.launch_count()
+    fn()
+    torch.cuda.synchronize()
+    return sage.launch_count() - before
 
 
 def to_device(torch, bits, dtype):
@@ -171,16 +170,27 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int):
             dist.barrier()
         torch.cuda.synchronize()
 
+    def step():
+        """One step through the two-call API (the same kernels as fwd()), with
+        events around the prologue and around the attention kernel."""
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record(stream)
+        qt = prologue()
+        b.record(stream)
+        sage.attn_quantized(qt, out, w.layout, w.causal, scale)
+        c.record(stream)
+        return a, b, c
+
     for _ in range(args.warmup):
         fwd()
+        flush.zero_()
+        step()
         flush.zero_()
     torch.cuda.synchronize()
     assert sage.device_status(ws) == sage.OK, sage.last_error()
     launches_per_step = count_launches(torch, fwd)
 
-    # ---- timed region: whole step (prologue + attention), device events
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    # ---- timed region: K steps (prologue + attention), device events
     clocks = ClockSampler(dev.index)
     clocks.start()
     t_end = time.perf_counter() + 0.4          # keep the GPU busy while the sampler starts
@@ -189,33 +199,19 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int):
         flush.zero_()
         torch.cuda.synchronize()
     barrier()
+    ev = []
+    launches0 = sage.launch_count()
     for i in range(args.steps):
-        flush.zero_()
-        ev[i][0].record(stream)
-        fwd()
-        ev[i][1].record(stream)
+        flush.zero_()                          # L2 flush between timed steps
+        ev.append(step())
     barrier()
+    launches = sage.launch_count() - launches0
     clock_info = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
+    step_ms = [a.elapsed_time(c) for a, b, c in ev]
     total_ms = sum(step_ms)
+    pro_ms = statistics.mean(a.elapsed_time(b) for a, b, c in ev)
+    att_ms = statistics.mean(b.elapsed_time(c) for a, b, c in ev)
     assert sage.device_status(ws) == sage.OK, sage.last_error()
-
-    # ---- per-kernel split: prologue alone and attention kernel alone
-    qt = prologue()
-    pro_ev, att_ev = [], []
-    for i in range(max(10, args.steps)):
-        flush.zero_()
-        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-        a.record(stream)
-        qt = prologue()
-        b.record(stream)
-        sage.attn_quantized(qt, out, w.layout, w.causal, scale)
-        c.record(stream)
-        pro_ev.append((a, b))
-        att_ev.append((b, c))
-    torch.cuda.synchronize()
-    pro_ms = statistics.mean(a.elapsed_time(b) for a, b in pro_ev)
-    att_ms = statistics.mean(a.elapsed_time(b) for a, b in att_ev)
 
     # ---- end to end: host buffers, copies inside the timed region
     e2e_ev = []
@@ -241,7 +237,7 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int):
     ops = workload_ops(w)
     Dp = 64 if w.D <= 64 else 128
     return dict(total_ms=total_ms, step_ms=step_ms, pro_ms=pro_ms, att_ms=att_ms,
-                launches_per_step=launches_per_step,
+                launches_per_step=launches_per_step, launches=launches,
                 e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, ops=ops, ops_padded=workload_ops(w, Dp),
                 clocks=clock_info)
 
@@ -366,7 +362,8 @@ def main():
         "prologue_hbm_frac": pro_gbs / peaks["hbm_gbs"],
         "e2e": {"value": r["ops"] / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TOPS",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-        "gpu_launches": r["launches_per_step"] * args.steps,
+        "gpu_launches": r["launches"],
+        "launches_per_step": r["launches_per_step"],
         "clocks": r["clocks"],
         "cpu_baseline": {"value": cpu_ops / cpu_s / 1e12, "unit": "TOPS", "cores": cores,
                          "kind": "oracle",

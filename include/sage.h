@@ -210,6 +210,12 @@ SAGE_API sage_status sage_kv_stats_noalloc(const void* k, const void* v, int dty
 /* Reason of the last failure on this thread ("" if none). */
 SAGE_API const char* sage_last_error(void);
 
+/* Instrumentation (no counterpart in the pages): the number of kernels this
+ * library has launched in this process, all devices and threads, counted on
+ * the host as each launch is issued.  The difference across a region gives
+ * the kernels issued inside it.  Never fails. */
+SAGE_API uint64_t sage_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -20,11 +20,24 @@
 using namespace sage;
 
 namespace {
+std::atomic<uint64_t> g_launches{0};
+}  // namespace
+
+void sage::note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+uint64_t sage::launch_count() { return g_launches.load(std::memory_order_relaxed); }
+
+namespace {
 
 thread_local std::string g_last_error;
 std::atomic<int> g_skip_kv_tile{-1};
 std::atomic<unsigned long long> g_timeout_ns{0};
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;   // 1 s
+
+// Bound of every device-side wait of the next launches.
+uint64_t wait_timeout_ns() {
+  const unsigned long long t = g_timeout_ns.load();
+  return t ? t : kDefaultTimeoutNs;
+}
 
 sage_status fail(sage_status st, const char* fmt, ...) {
   char buf[512];
@@ -50,7 +63,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Byte offsets of every workspace buffer.
 struct WsLayout {
-  size_t status, ksum, vmax, done, zero_end, k_mean, s_v, v_inv, s_q, s_k, q16, k16,
+  size_t status, ksum, vmax, done, ready, zero_end, k_mean, s_v, v_inv, s_q, s_k, q16, k16,
       v8, total;
 };
 
@@ -65,6 +78,7 @@ WsLayout ws_layout(const SegGeo& g) {
   w.ksum = o; o = align256(o + nstat * 8);
   w.vmax = o; o = align256(o + nstat * 4);
   w.done = o; o = align256(o + g.nseg * g.Hkv * 4);
+  w.ready = o; o = align256(o + g.nseg * g.Hkv * 4);
   // means and scales start at zero: a segment without keys keeps them so
   w.k_mean = o; o = align256(o + nstat * 4);
   w.s_v = o; o = align256(o + nstat * 4);
@@ -257,6 +271,9 @@ sage_status run_prologue(const SegGeo& g, const void* q, const void* k, const vo
   b.ksum = wsb + w.ksum;
   b.vmax = reinterpret_cast<uint32_t*>(wsb + w.vmax);
   b.done = reinterpret_cast<uint32_t*>(wsb + w.done);
+  b.ready = reinterpret_cast<uint32_t*>(wsb + w.ready);
+  b.next = reinterpret_cast<unsigned long long*>(wsb + w.status + 8);
+  b.timeout_ns = wait_timeout_ns();
   b.status = reinterpret_cast<uint32_t*>(wsb + w.status);
   const bool vec = (g.D % 8 == 0) && aligned(q, 16) && aligned(k, 16) && aligned(v, 16);
   e = launch_prologue(g, b, vec, st);
@@ -299,8 +316,7 @@ sage_status launch_attn(const sage_quantized* qt, float* out, int layout, int is
   p.scale_log2 = resolve_scale(sm_scale, qt->D) * 1.44269504088896340736f;
   p.causal = is_causal ? 1 : 0;
   p.skip_kv_tile = g_skip_kv_tile.load();
-  const unsigned long long t = g_timeout_ns.load();
-  p.timeout_ns = t ? t : kDefaultTimeoutNs;
+  p.timeout_ns = wait_timeout_ns();
   p.status = qt->status;
   cudaError_t e = launch_attention(maps, p, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
@@ -528,11 +544,14 @@ sage_status sage_kv_stats_noalloc(const void* k, const void* v, int dtype, int l
   const bool vec = (D % 8 == 0) && aligned(k, 16) && aligned(v, 16);
   cudaError_t e = launch_kv_stats_static(g, static_cast<const uint16_t*>(k),
                                          static_cast<const uint16_t*>(v), k_mean, s_v, vec,
+                                         wait_timeout_ns(),
                                          reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "static-scratch statistics");
   return ok();
 }
 
 const char* sage_last_error(void) { return g_last_error.c_str(); }
+
+uint64_t sage_launch_count(void) { return launch_count(); }
 
 }  // extern "C"

@@ -613,6 +613,7 @@ cudaError_t launch_attention_t(const AttnMaps& maps, const AttnParams& p,
   dim3 grid(static_cast<unsigned>((nqt + 1) / 2), static_cast<unsigned>(p.g.Hq),
             static_cast<unsigned>(p.g.nseg));
   attn_kernel<DP><<<grid, kThreads, Layout<DP>::kAlloc, st>>>(maps.q, maps.k, maps.v, p);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -629,6 +630,7 @@ cudaError_t launch_debug_qk_t(const AttnMaps& maps, const AttnParams& p,
   }
   debug_qk_kernel<DP><<<1, 128, Layout<DP>::kAlloc, st>>>(maps.q, maps.k, q_row0, k_row0,
                                                           out, p.status, p.timeout_ns);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -652,6 +654,7 @@ cudaError_t launch_debug_e4m3(const float* in, uint8_t* out, int64_t n,
   if (n <= 0) return cudaSuccess;
   const int64_t blocks = (n + 255) / 256 < 152 * 16 ? (n + 255) / 256 : 152 * 16;
   debug_e4m3_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(in, out, n);
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -9,6 +9,10 @@
 
 namespace sage {
 
+// Counts one kernel launch of this library (process-wide, all devices).
+void note_launch();
+uint64_t launch_count();
+
 struct PrologueBuffers {
   const uint16_t* q;
   const uint16_t* k;
@@ -23,8 +27,11 @@ struct PrologueBuffers {
   float* v_inv;
   void* ksum;        // int64 (fp16 inputs) or double (bf16), [nseg][Hkv][Dp]
   uint32_t* vmax;    // float bits, [nseg][Hkv][Dp]
-  uint32_t* done;    // stats chunks finished per (segment, kv head), zeroed
+  uint32_t* done;    // stats items finished per (segment, kv head), zeroed
+  uint32_t* ready;   // per (segment, kv head): statistics final, zeroed
+  unsigned long long* next;   // work-item counter, zeroed
   uint32_t* status;
+  uint64_t timeout_ns;        // bound of every wait
 };
 
 cudaError_t launch_prologue(const SegGeo& g, const PrologueBuffers& b,
@@ -37,7 +44,7 @@ constexpr int64_t kStaticStatEntries = 16384;
 // accumulators in a static device array instead of a caller workspace.
 cudaError_t launch_kv_stats_static(const SegGeo& g, const uint16_t* k,
                                    const uint16_t* v, float* k_mean, float* s_v,
-                                   bool vec, cudaStream_t st);
+                                   bool vec, uint64_t timeout_ns, cudaStream_t st);
 
 struct AttnParams {
   SegGeo g;

@@ -23,7 +23,7 @@ EXPORTS = (
     "sage_quant_prologue_varlen", "sage_attn_quantized", "sage_attn_fwd",
     "sage_attn_fwd_varlen", "sage_debug_qk_int32", "sage_debug_e4m3",
     "sage_debug_set_fault", "sage_device_status", "sage_last_error",
-    "sage_kv_stats_noalloc",
+    "sage_kv_stats_noalloc", "sage_launch_count",
 )
 
 
@@ -77,6 +77,7 @@ def _load():
         "sage_device_status": ([P, P], I),
         "sage_last_error": ([], ctypes.c_char_p),
         "sage_kv_stats_noalloc": ([P, P, I, I, I64, I64, I64, I64, P, P, P], I),
+        "sage_launch_count": ([], ctypes.c_uint64),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -91,6 +92,11 @@ lib = _lib
 
 def last_error() -> str:
     return _lib.sage_last_error().decode()
+
+
+def launch_count() -> int:
+    """Kernels this library has launched in this process (host-side count)."""
+    return int(_lib.sage_launch_count())
 
 
 def _check(rc: int, where: str):
