@@ -169,6 +169,30 @@ using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, voi
                               const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                               CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+EncodeFn encode_fn();
+
+}  // namespace
+
+bool sage::encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, uint32_t rank, void* base,
+                        const uint64_t* dims, const uint64_t* strides_bytes,
+                        const uint32_t* box, CUtensorMapSwizzle swizzle) {
+  EncodeFn fn = encode_fn();
+  if (fn == nullptr || rank < 1 || rank > 5) return false;
+  cuuint64_t d[5], s[4];
+  cuuint32_t b[5], e[5];
+  for (uint32_t i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+    if (i + 1 < rank) s[i] = strides_bytes[i];
+  }
+  return fn(map, dt, rank, base, d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+namespace {
+
 EncodeFn encode_fn() {
   static EncodeFn fn = nullptr;
   if (fn == nullptr) {
@@ -185,15 +209,10 @@ EncodeFn encode_fn() {
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, void* base,
                uint64_t inner, uint64_t outer, uint64_t row_bytes,
                uint32_t box_inner, uint32_t box_outer) {
-  EncodeFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t dims[2] = {inner, outer};
+  const uint64_t strides[1] = {row_bytes};
+  const uint32_t box[2] = {box_inner, box_outer};
+  return encode_tiled(map, dt, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 sage_status make_maps(const sage_quantized* qt, AttnMaps* maps) {
@@ -272,7 +291,7 @@ sage_status run_prologue(const SegGeo& g, const void* q, const void* k, const vo
   b.vmax = reinterpret_cast<uint32_t*>(wsb + w.vmax);
   b.done = reinterpret_cast<uint32_t*>(wsb + w.done);
   b.ready = reinterpret_cast<uint32_t*>(wsb + w.ready);
-  b.next = reinterpret_cast<unsigned long long*>(wsb + w.status + 8);
+  b.next = reinterpret_cast<unsigned int*>(wsb + w.status + 8);
   b.timeout_ns = wait_timeout_ns();
   b.status = reinterpret_cast<uint32_t*>(wsb + w.status);
   const bool vec = (g.D % 8 == 0) && aligned(q, 16) && aligned(k, 16) && aligned(v, 16);

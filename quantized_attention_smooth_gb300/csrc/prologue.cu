@@ -6,34 +6,42 @@
 // overview's Core features (INT8 Q/K, smoothing) and the SageAttention-RDNA4
 // v0.4.0 notes (key mean summed in fp64, 64-bit offsets).
 //
-// One persistent kernel.  Its CTAs take work items, in order, from a counter
-// in the workspace.  A unit is one (segment, kv head); its items are
-//   stats  256 tokens of K and V: exact per-channel sums of K (int64 fixed
-//          point at 2^-24 for fp16, fp64 for bf16) and per-channel max |V|,
-//          added to the unit's accumulators with atomics.  The unit's last
-//          stats item turns them into the K mean, the V scale and its
-//          reciprocal multiplier and raises the unit's ready flag.
-//   Q      128 tokens of one query head that reads this kv head: int8 codes
-//          (stored as exact fp16 integers, the tensor-core operand), one
-//          scale per token.
-//   K      128 tokens: smoothed K (k - mean, fp32) -> int8 codes, one scale
-//          per block.  Waits for the ready flag.
-//   V      128 tokens: e4m3 per channel, transposed to channel-major through
-//          shared memory.  Waits for the ready flag.
-// The list puts a unit's K and V items `lag` units after its stats and Q
-// items, far enough that its statistics are normally done before a CTA takes
-// them and near enough that the unit's K and V are still in L2 (the stats
-// pass marks them evict-last).  Items are taken in list order by running
-// CTAs only, so every item waited on is already held by a running CTA and
-// the waits always end; they are bounded all the same (timeout -> status
-// bit).  Every 128-token tile of the workspace is written in full (zeros
-// past the sequence end and past D), so the attention kernel never reads
-// stale bytes.
+// One persistent kernel, two CTAs per SM.  A CTA has eight consumer warps, a
+// producer warp and a helper warp around a ring of three 32 KB shared-memory
+// stages.  The producer takes work items, in order, from a counter in the
+// workspace and copies each item's 128-token input tile into a free stage
+// with a tensor copy (TMA), zero-padded to Dp channels; the consumers
+// quantise the tile in the stage and release it.  A unit is one (segment,
+// kv head); its items are
+//   stats K   128 keys: exact per-channel sums (int64 fixed point at 2^-24
+//             for fp16, fp64 for bf16), added to the unit's accumulators;
+//   stats V   128 values: per-channel max |v|, likewise;
+//   Q         128 tokens of one query head that reads this kv head: int8
+//             codes (stored as exact fp16 integers, the tensor-core operand),
+//             one scale per token;
+//   K         128 keys: smoothed K (k - mean, fp32) -> int8 codes, one scale
+//             per block;
+//   V         128 values: e4m3 per channel, transposed to channel-major.
+// Consumers hand every finished stats tile to the helper warp, which counts
+// it for its unit; the count that completes a unit makes the helper turn
+// the sums into the K mean, the V scale and its reciprocal multiplier and
+// raise the unit's ready flag.  A K or V tile's stage also expects the
+// unit's means (or multipliers): the helper copies them next to the tile
+// once the unit is final, so the producer never waits on a unit and the
+// consumers read nothing but their stage.  The list puts a unit's K and V
+// items `lag` units after its stats and Q items: far enough that the unit
+// is normally final by then, near enough that its K and V are still in L2
+// (the stats copies mark them evict-last).  Items are taken in list order by
+// running CTAs and issued in that order, and a stats tile never waits, so
+// the wait of the lowest waiting item always ends; every wait is bounded all
+// the same (timeout -> status bit).  Every 128-token tile of the workspace
+// is written in full (zeros past the sequence end and past D), so the
+// attention kernel never reads stale bytes.
 //
-// Loads are 128-bit (8 elements) when D % 8 == 0 and the tensors are 16-byte
-// aligned, otherwise element-wise.  Rounding is explicit (__fmul2_rn,
-// __fdiv_rn, round-to-nearest-even additions) so the codes match a plain
-// IEEE restatement.
+// Without 16-byte aligned rows (D % 8 != 0 or unaligned tensors) the same
+// kernel runs with element-wise global loads instead of tensor copies.
+// Rounding is explicit (packed .rn multiplies, __fdiv_rn, round-to-nearest-
+// even additions) so the codes match a plain IEEE restatement.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -48,26 +56,36 @@ namespace sage {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kChunk = 256;                 // tokens per stats item
+constexpr int kConsumers = 256;              // eight consumer warps
+constexpr int kProducerWarp = 8;
+constexpr int kHelperWarp = 9;
+constexpr int kThreads = kConsumers + 64;
+constexpr int kStages = 3;
+constexpr int kQueue = 8;                    // finished stats tiles awaiting the helper
+constexpr int kRequests = 4;                 // K/V tiles awaiting their statistics
+constexpr int kTileBytes = 128 * 128 * 2;    // 128 rows of up to 128 16-bit values
+constexpr uint32_t kSleepNs = 20000;         // suspend hint of barrier waits
 // fp32 2^23 + 2^22 + 0x6600: adding it rounds to an integer n (ties to even)
 // and leaves 0x6600 + n, the fp16 bits of 1536 + n, in the low 16 bits.
 constexpr float kCodeMagic = 12609024.0f;
-constexpr float kRintMagic = 12582912.0f;   // 1.5 * 2^23
+constexpr float kRintMagic = 12582912.0f;    // 1.5 * 2^23
 
-// Work list of one call (host-computed).
+enum ItemKind { kStatsK = 0, kStatsV = 1, kQ = 2, kK = 3, kV = 4, kEnd = 5 };
+
+// Work list of one call (host-computed; every count fits in 31 bits).
 struct Plan {
-  int64_t units;      // nseg * Hkv
-  int64_t lag;        // units between a unit's stats/Q items and its K/V items
-  int64_t total;      // items
-  int32_t n_stats;    // stats items per unit
+  int32_t units;      // nseg * Hkv
+  int32_t lag;        // units between a unit's stats/Q items and its K/V items
+  int32_t total;      // items
+  int32_t n_stats;    // stats items per unit (K and V tiles alternate)
   int32_t n_q;        // Q items per unit (query heads of the kv head x tiles)
-  int32_t n_kv;       // K and V items per unit (2 per 128-token block)
+  int32_t n_kv;       // K and V items per unit (K and V tiles alternate)
   int32_t nqt;        // 128-token tiles per query head
 };
 
 struct ProParams {
   SegGeo g;
+  CUtensorMap mq, mk, mv;     // 3D maps of q, k, v (tensor-copy path)
   const uint16_t* q;
   const uint16_t* k;
   const uint16_t* v;
@@ -81,67 +99,79 @@ struct ProParams {
   float* v_inv;
   void* ksum;                 // int64 (fp16) or double (bf16) per (unit, channel)
   uint32_t* vmax;             // float bits per (unit, channel)
-  uint32_t* done;             // stats items finished per unit
+  uint32_t* done;             // stats tiles finished per unit
   uint32_t* ready;            // per unit: statistics final
-  unsigned long long* next;   // work counter
+  unsigned int* next;         // work counter
   uint32_t* status;
   uint64_t timeout_ns;
+  int32_t q_hnd, k_hnd;       // 1: tiles are (head, token) planes; 0: token-major
   float one;                  // 1.0, opaque to the compiler (see code2)
   Plan plan;
 };
 
-enum ItemKind { kItemStats = 0, kItemQ = 1, kItemKV = 2 };
-
-struct Item {
-  int kind;
-  int64_t unit;
-  int32_t sub;
+struct Slot {
+  int32_t kind, sub, unit, nvalid;
 };
 
-// Item i of the list.  Slots 0 .. lag-1 hold stats and Q items of units
-// 0 .. lag-1; slot j >= lag holds those of unit j and then the K/V items of
-// unit j - lag; the last lag slots hold K/V items only.
-__device__ __forceinline__ Item decode(const Plan& P, int64_t i) {
-  const int64_t a = P.n_stats + P.n_q;
-  const int64_t per = a + P.n_kv;
-  Item it;
-  int64_t off;
+struct alignas(1024) PSmem {
+  unsigned char tile[kStages][kTileBytes];
+  float aux[kStages][128];    // K items: the unit's K mean; V items: its V multipliers
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t qfull[kQueue];
+  uint64_t qempty[kQueue];
+  uint64_t rfull[kRequests];
+  uint64_t rempty[kRequests];
+  int32_t queue[kQueue];
+  int4 req[kRequests];        // (kind, unit, stage, -) of a K/V tile awaiting its statistics
+  Slot slot[kStages];
+  float red[8];
+  int abort;
+};
+
+// Item i of the list: (kind, unit, sub).  Slots 0 .. lag-1 hold stats and Q
+// items of units 0 .. lag-1; slot j >= lag holds those of unit j and then
+// the K/V items of unit j - lag; the last lag slots hold K/V items only.
+__device__ __forceinline__ void decode(const Plan& P, int i, int* kind, int* unit, int* sub) {
+  const int a = P.n_stats + P.n_q;
+  const int per = a + P.n_kv;
+  int off;
   if (i < P.lag * a) {
-    it.unit = i / a;
-    off = i - it.unit * a;
+    *unit = i / a;
+    off = i - *unit * a;
   } else {
     i -= P.lag * a;
-    const int64_t mid = (P.units - P.lag) * per;
+    const int mid = (P.units - P.lag) * per;
     if (i >= mid) {
       i -= mid;
-      const int64_t j = i / P.n_kv;
-      it.kind = kItemKV;
-      it.unit = P.units - P.lag + j;
-      it.sub = static_cast<int32_t>(i - j * P.n_kv);
-      return it;
+      const int j = i / P.n_kv;
+      *unit = P.units - P.lag + j;
+      off = i - j * P.n_kv;
+      *kind = (off & 1) ? kV : kK;
+      *sub = off >> 1;
+      return;
     }
-    const int64_t j = i / per;
+    const int j = i / per;
     off = i - j * per;
     if (off >= a) {
-      it.kind = kItemKV;
-      it.unit = j;
-      it.sub = static_cast<int32_t>(off - a);
-      return it;
+      *unit = j;
+      off -= a;
+      *kind = (off & 1) ? kV : kK;
+      *sub = off >> 1;
+      return;
     }
-    it.unit = P.lag + j;
+    *unit = P.lag + j;
   }
   if (off < P.n_stats) {
-    it.kind = kItemStats;
-    it.sub = static_cast<int32_t>(off);
+    *kind = (off & 1) ? kStatsV : kStatsK;
+    *sub = off >> 1;
   } else {
-    it.kind = kItemQ;
-    it.sub = static_cast<int32_t>(off - P.n_stats);
+    *kind = kQ;
+    *sub = off - P.n_stats;
   }
-  return it;
 }
 
 // ------------------------------------------------------------ memory ops
-// L2 cache policies: keep the stats pass over K/V resident for the K/V items.
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t pol;
   asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
@@ -153,50 +183,73 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return pol;
 }
 
-// Read-only 16-byte load with an L2 policy.  Not volatile: the compiler may
-// schedule it early (the inputs are never written by the prologue).
-__device__ __forceinline__ uint4 ld16(const void* p, uint64_t pol) {
-  uint4 u;
-  asm("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-      : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w) : "l"(p), "l"(pol));
-  return u;
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, int32_t x,
+                                                 int32_t y, int32_t z, uint64_t* bar,
+                                                 uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;"
+      :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z),
+         "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
 }
 
-// The same load, kept by the compiler where written: a second pass re-reads
-// its rows (from L1) instead of holding them in registers across a barrier.
-__device__ __forceinline__ uint4 ld16_again(const void* p) {
-  uint4 u;
-  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w) : "l"(p));
-  return u;
+// Contiguous global -> shared copy (16-byte aligned ends) completing on bar.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
-// Channels c0..c0+7 of one token row as packed 16-bit values (zeros for
-// channels >= D).
-template <bool kVec, bool kAgain = false>
-__device__ __forceinline__ uint4 load8(const uint16_t* row, int c0, int D, uint64_t pol) {
-  if constexpr (kVec) {
-    if constexpr (kAgain) return c0 < D ? ld16_again(row + c0) : make_uint4(0u, 0u, 0u, 0u);
-    return c0 < D ? ld16(row + c0, pol) : make_uint4(0u, 0u, 0u, 0u);
-  } else {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t lo = (c0 + 2 * i < D) ? row[c0 + 2 * i] : 0u;
-      const uint32_t hi = (c0 + 2 * i + 1 < D) ? row[c0 + 2 * i + 1] : 0u;
-      w[i] = lo | (hi << 16);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
   uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 __device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+// Barrier of the eight consumer warps (the other two warps run on their own).
+__device__ __forceinline__ void csync() {
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+
+// mbarrier wait that lets the warp sleep until the phase completes (or the
+// hint runs out) instead of polling; bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_sleep_wait(uint64_t* bar, uint32_t parity,
+                                                volatile int* abort, uint32_t* status,
+                                                uint64_t timeout_ns) {
+  uint64_t t0 = 0;
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(kSleepNs) : "memory");
+    if (ok) return true;
+    if (abort != nullptr && *abort) return false;
+    const uint64_t now = global_timer_ns();
+    if (t0 == 0) {
+      t0 = now;
+    } else if (now - t0 > timeout_ns) {
+      if (abort != nullptr) *abort = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
 }
 
 // ------------------------------------------------------------- numerics
@@ -223,8 +276,8 @@ __device__ __forceinline__ float mag_f32(uint32_t m) {
   else return __half2float(__ushort_as_half(static_cast<unsigned short>(m)));
 }
 
-// Max magnitude (bits) of the eight 16-bit values of a load.  Magnitudes of
-// finite fp16/bf16 values order like their bit patterns.
+// Max magnitude (bits) of the eight 16-bit values of a row piece.
+// Magnitudes of finite fp16/bf16 values order like their bit patterns.
 __device__ __forceinline__ uint32_t max_mag8(const uint4& u) {
   const uint32_t m = __vmaxu2(__vmaxu2(u.x & 0x7FFF7FFFu, u.y & 0x7FFF7FFFu),
                               __vmaxu2(u.z & 0x7FFF7FFFu, u.w & 0x7FFF7FFFu));
@@ -276,233 +329,202 @@ __device__ __forceinline__ uint32_t row_max_transposed(uint32_t (&a)[P], int lan
   return max(a[0], __shfl_xor_sync(0xFFFFFFFFu, a[0], 1));
 }
 
-// --------------------------------------------------------------- smem
-struct StatsSmem {
-  long long part[kThreads / 32][128];
-  uint32_t vmax[kThreads / 32][128];
-};
-struct Smem {
-  union {
-    StatsSmem st;
-    uint32_t vt[128 * 32];            // V tile, [channel][4-token word]
-    float red[kThreads / 32];
-  } u;
-  long long next[2];
-  int flag;
+// Segment bounds (dense: the whole sequence); false on bad cu_seqlens.
+__device__ __forceinline__ bool key_range(const SegGeo& g, int64_t s, int64_t* start,
+                                          int64_t* len) {
+  *start = 0;
+  *len = g.Lk;
+  return !g.varlen || seg_range(g.cu_k, s, g.total_k, g.max_k, start, len);
+}
+__device__ __forceinline__ bool query_range(const SegGeo& g, int64_t s, int64_t* start,
+                                            int64_t* len) {
+  *start = 0;
+  *len = g.Lq;
+  return !g.varlen || seg_range(g.cu_q, s, g.total_q, g.max_q, start, len);
+}
+
+// Rows of the current 128-token tile for one thread: row r + R * i as
+// channels c0..c0+7.  Tensor-copy path: the stage holds 128 rows of Dp
+// values (zeros past D), read with constant offsets.  Fallback: element-wise
+// global loads of token t0 + r + R * i (zeros past D).
+template <bool kTma, int DP>
+struct TileRows {
+  const unsigned char* at;      // kTma: stage + (r * DP + c0) * 2
+  const uint16_t* row0;         // !kTma: row r of the tile, channel 0
+  int64_t tok_stride;           // !kTma
+  int c0, D;                    // !kTma
+  template <int R>
+  __device__ __forceinline__ uint4 get(int i) const {
+    if constexpr (kTma) {
+      return *reinterpret_cast<const uint4*>(at + i * (R * DP * 2));
+    } else {
+      if (c0 >= D) return make_uint4(0u, 0u, 0u, 0u);
+      const uint16_t* row = row0 + static_cast<int64_t>(i) * R * tok_stride;
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = (c0 + 2 * j < D) ? row[c0 + 2 * j] : 0u;
+        const uint32_t hi = (c0 + 2 * j + 1 < D) ? row[c0 + 2 * j + 1] : 0u;
+        w[j] = lo | (hi << 16);
+      }
+      return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
 };
 
-// Thread 0 waits (bounded) for a unit's ready flag; the CTA learns the
-// outcome through shared memory.  Returns false on timeout.
-__device__ __forceinline__ bool wait_ready(const ProParams& p, int64_t unit, Smem& sm) {
-  if (threadIdx.x == 0) {
-    const uint32_t* f = p.ready + unit;
-    int ok = ld_acquire(f) != 0u;
-    if (!ok) {
-      const uint64_t t0 = global_timer_ns();
-      while (true) {
-        __nanosleep(128);
-        if (ld_acquire(f) != 0u) { ok = 1; break; }
-        if (global_timer_ns() - t0 > p.timeout_ns) {
-          atomicOr(p.status, kStatusTimeout);
-          break;
+// ------------------------------------------------------------- stats K
+template <bool kBf16, int DP, class Rows>
+__device__ __forceinline__ void stats_k(const ProParams& p, int unit, int nvalid,
+                                        const Rows& rows, unsigned char* scratch) {
+  constexpr int G = DP / 8, R = kConsumers / G, P = kBlockN / R;   // P 8 or 4 rows
+  const int lc = threadIdx.x % G, r = threadIdx.x / G, c0 = lc * 8;
+  const bool full = nvalid == kBlockN;
+  // fp16 keys: a thread holds at most 8 rows of a channel, each split exactly
+  // into hi = rint(16 k) and lo = k - hi / 16 (a multiple of 2^-24, |lo| <=
+  // 1/32); up to 16 of either sum exactly in fp32 (|sum hi| < 2^24, |sum lo|
+  // * 2^24 <= 2^23).  The FP64 pipe (slow on GB300) stays out of the loop.
+  // bf16 keys: fp64 sums.
+  long long part[8];
+  if constexpr (kBf16) {
+    double ds[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ds[j] = 0.0;
+#pragma unroll
+    for (int i = 0; i < P; ++i) {
+      if (full || r + R * i < nvalid) {
+        const uint4 u = rows.template get<R>(i);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 x = cvt2<true>(word(u, j));
+          ds[2 * j] += static_cast<double>(x.x);
+          ds[2 * j + 1] += static_cast<double>(x.y);
         }
       }
     }
-    sm.flag = ok;
-  }
-  __syncthreads();
-  return sm.flag != 0;
-}
-
-// ---------------------------------------------------------------- stats
-template <bool kVec, bool kBf16, int DP>
-__device__ __forceinline__ void stats_item(const ProParams& p, int64_t unit, int chunk,
-                                           Smem& sm) {
-  constexpr int G = DP / 8, R = kThreads / G, TPT = kChunk / R;   // TPT 16 or 8
-  const SegGeo& g = p.g;
-  const int64_t s = unit / g.Hkv, h = unit % g.Hkv;
-  int64_t start = 0, len = g.Lk;
-  if (g.varlen && !seg_range(g.cu_k, s, g.total_k, g.max_k, &start, &len)) {
-    if (threadIdx.x == 0 && chunk == 0) atomicOr(p.status, kStatusBadSeqlens);
-    len = 0;
-  }
-  const int64_t chunks = len > 0 ? (len + kChunk - 1) / kChunk : 1;
-  if (chunk >= chunks) return;
-  const int lc = threadIdx.x % G, r = threadIdx.x / G, c0 = lc * 8;
-  const int D = static_cast<int>(g.D);
-  const int64_t base = (g.varlen ? start * g.k_tok_stride : s * g.k_seg_stride) +
-                       h * g.k_head_stride;
-  const uint16_t* kb = p.k + base;
-  const uint16_t* vb = p.v + base;
-  const int64_t t0 = static_cast<int64_t>(chunk) * kChunk;
-  const int64_t t1 = min(len, t0 + kChunk);
-  const uint64_t keep = policy_evict_last();
-
-  // fp16 keys: per thread at most 16 tokens, each split exactly into
-  // hi = rint(16 k) and lo = k - hi / 16 (a multiple of 2^-24, |lo| <= 1/32);
-  // 16 of either sum exactly in fp32 (|sum hi| < 2^24, |sum lo| * 2^24 <=
-  // 2^23).  The FP64 pipe (slow on GB300) stays out of the loop.  bf16 keys:
-  // fp64 sums.
-  float2 hs[4], ls[4];
-  double ds[8];
-  uint32_t vm[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    hs[i] = make_float2(0.0f, 0.0f);
-    ls[i] = make_float2(0.0f, 0.0f);
-    vm[i] = 0u;
-  }
+    for (int j = 0; j < 8; ++j) part[j] = __double_as_longlong(ds[j]);
+  } else {
+    float2 hs[4], ls[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) ds[i] = 0.0;
-
-#pragma unroll
-  for (int j0 = 0; j0 < TPT; j0 += 4) {
-    uint4 kr[4], vr[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {             // 8 loads in flight per thread
-      const int64_t t = t0 + r + static_cast<int64_t>(R) * (j0 + u);
-      const bool in = t < t1;
-      kr[u] = in ? load8<kVec>(kb + t * g.k_tok_stride, c0, D, keep) : make_uint4(0u, 0u, 0u, 0u);
-      vr[u] = in ? load8<kVec>(vb + t * g.k_tok_stride, c0, D, keep) : make_uint4(0u, 0u, 0u, 0u);
+    for (int j = 0; j < 4; ++j) {
+      hs[j] = make_float2(0.0f, 0.0f);
+      ls[j] = make_float2(0.0f, 0.0f);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int i = 0; i < P; ++i) {
+      if (full || r + R * i < nvalid) {
+        const uint4 u = rows.template get<R>(i);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        vm[i] = __vmaxu2(vm[i], word(vr[u], i) & 0x7FFF7FFFu);
-        const float2 x = cvt2<kBf16>(word(kr[u], i));
-        if constexpr (kBf16) {
-          ds[2 * i] += static_cast<double>(x.x);
-          ds[2 * i + 1] += static_cast<double>(x.y);
-        } else {
+        for (int j = 0; j < 4; ++j) {
+          const float2 x = cvt2<false>(word(u, j));
           const float2 tr = __ffma2_rn(x, make_float2(16.0f, 16.0f),
                                        make_float2(kRintMagic, kRintMagic));
           const float2 hi = __fadd2_rn(tr, make_float2(-kRintMagic, -kRintMagic));
           const float2 lo = __ffma2_rn(hi, make_float2(-0.0625f, -0.0625f), x);
-          hs[i] = __fadd2_rn(hs[i], hi);
-          ls[i] = __fadd2_rn(ls[i], lo);
+          hs[j] = __fadd2_rn(hs[j], hi);
+          ls[j] = __fadd2_rn(ls[j], lo);
         }
       }
     }
-  }
-
-  // combine the rows: lanes holding the same channels (warp shuffles), then
-  // the eight warps through shared memory, one channel per thread
-  long long part[8];
-  uint32_t am[8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if constexpr (kBf16) {
-      part[2 * i] = __double_as_longlong(ds[2 * i]);
-      part[2 * i + 1] = __double_as_longlong(ds[2 * i + 1]);
-    } else {
-      part[2 * i] = static_cast<long long>(__float2int_rn(hs[i].x)) * 1048576ll +
-                    __float2int_rn(ls[i].x * 16777216.0f);
-      part[2 * i + 1] = static_cast<long long>(__float2int_rn(hs[i].y)) * 1048576ll +
-                        __float2int_rn(ls[i].y * 16777216.0f);
+    for (int j = 0; j < 4; ++j) {
+      part[2 * j] = static_cast<long long>(__float2int_rn(hs[j].x)) * 1048576ll +
+                    __float2int_rn(ls[j].x * 16777216.0f);
+      part[2 * j + 1] = static_cast<long long>(__float2int_rn(hs[j].y)) * 1048576ll +
+                        __float2int_rn(ls[j].y * 16777216.0f);
     }
-    am[2 * i] = vm[i] & 0xFFFFu;
-    am[2 * i + 1] = vm[i] >> 16;
+  }
+  // lanes holding the same channels (warp shuffles), then the eight warps
+  // through shared memory (the stage, once every row has been read)
+#pragma unroll
+  for (int o = G; o < 32; o <<= 1) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const long long other = __shfl_xor_sync(0xFFFFFFFFu, part[j], o);
+      if constexpr (kBf16)
+        part[j] = __double_as_longlong(__longlong_as_double(part[j]) +
+                                       __longlong_as_double(other));
+      else
+        part[j] += other;
+    }
+  }
+  long long (*tab)[DP] = reinterpret_cast<long long (*)[DP]>(scratch);
+  csync();
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if (lane < G) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) tab[wid][c0 + j] = part[j];
+  }
+  csync();
+  if (threadIdx.x < p.g.D) {
+    const int c = threadIdx.x;
+    if constexpr (kBf16) {
+      double sd = 0.0;
+#pragma unroll
+      for (int w = 0; w < kConsumers / 32; ++w) sd += __longlong_as_double(tab[w][c]);
+      atomicAdd(static_cast<double*>(p.ksum) + static_cast<int64_t>(unit) * DP + c, sd);
+    } else {
+      long long si = 0;
+#pragma unroll
+      for (int w = 0; w < kConsumers / 32; ++w) si += tab[w][c];
+      atomicAdd(static_cast<unsigned long long*>(p.ksum) + static_cast<int64_t>(unit) * DP + c,
+                static_cast<unsigned long long>(si));
+    }
+  }
+}
+
+// ------------------------------------------------------------- stats V
+template <bool kBf16, int DP, class Rows>
+__device__ __forceinline__ void stats_v(const ProParams& p, int unit, int nvalid,
+                                        const Rows& rows, unsigned char* scratch) {
+  constexpr int G = DP / 8, R = kConsumers / G, P = kBlockN / R;
+  const int lc = threadIdx.x % G, r = threadIdx.x / G, c0 = lc * 8;
+  const bool full = nvalid == kBlockN;
+  uint32_t vm[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int i = 0; i < P; ++i) {
+    if (full || r + R * i < nvalid) {
+      const uint4 u = rows.template get<R>(i);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) vm[j] = __vmaxu2(vm[j], word(u, j) & 0x7FFF7FFFu);
+    }
   }
 #pragma unroll
   for (int o = G; o < 32; o <<= 1) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const long long other = __shfl_xor_sync(0xFFFFFFFFu, part[i], o);
-      if constexpr (kBf16)
-        part[i] = __double_as_longlong(__longlong_as_double(part[i]) +
-                                       __longlong_as_double(other));
-      else
-        part[i] += other;
-      am[i] = max(am[i], __shfl_xor_sync(0xFFFFFFFFu, am[i], o));
-    }
+    for (int j = 0; j < 4; ++j) vm[j] = __vmaxu2(vm[j], __shfl_xor_sync(0xFFFFFFFFu, vm[j], o));
   }
+  uint32_t (*tab)[DP / 2] = reinterpret_cast<uint32_t (*)[DP / 2]>(scratch);
+  csync();
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   if (lane < G) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      sm.u.st.part[wid][c0 + i] = part[i];
-      sm.u.st.vmax[wid][c0 + i] = am[i];
-    }
+    for (int j = 0; j < 4; ++j) tab[wid][c0 / 2 + j] = vm[j];
   }
-  __syncthreads();
-  const int64_t obase = unit * DP;
-  if (threadIdx.x < D) {
+  csync();
+  if (threadIdx.x < p.g.D) {
     const int c = threadIdx.x;
-    long long si = 0;
-    double sd = 0.0;
-    uint32_t a = 0u;
+    uint32_t m = 0u;
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) {
-      if constexpr (kBf16) sd += __longlong_as_double(sm.u.st.part[w][c]);
-      else si += sm.u.st.part[w][c];
-      a = max(a, sm.u.st.vmax[w][c]);
-    }
-    if constexpr (kBf16) atomicAdd(static_cast<double*>(p.ksum) + obase + c, sd);
-    else atomicAdd(static_cast<unsigned long long*>(p.ksum) + obase + c,
-                   static_cast<unsigned long long>(si));
-    atomicMax(p.vmax + obase + c, __float_as_uint(mag_f32<kBf16>(a)));
-    __threadfence();
+    for (int w = 0; w < kConsumers / 32; ++w) m = __vmaxu2(m, tab[w][c >> 1]);
+    m = (c & 1) ? (m >> 16) : (m & 0xFFFFu);
+    atomicMax(p.vmax + static_cast<int64_t>(unit) * DP + c, __float_as_uint(mag_f32<kBf16>(m)));
   }
-  // The unit's last stats item turns the sums into the K mean and the V
-  // scales while they are hot in L2, then raises the ready flag.
-  __syncthreads();
-  if (threadIdx.x == 0)
-    sm.flag = atomicAdd(p.done + unit, 1u) == static_cast<uint32_t>(chunks - 1);
-  __syncthreads();
-  const bool last = sm.flag != 0;
-  __syncthreads();                             // sm.flag is reused by the next item
-  if (!last) return;
-  __threadfence();
-  for (int c = threadIdx.x; c < DP; c += kThreads) {
-    const int64_t i = obase + c;
-    double S;
-    if constexpr (kBf16)
-      S = __longlong_as_double(__ldcg(static_cast<const long long*>(p.ksum) + i));
-    else
-      S = __ll2double_rn(__ldcg(static_cast<const long long*>(p.ksum) + i)) *
-          5.9604644775390625e-08;   // 2^-24, exact
-    p.k_mean[i] = len > 0 ? __double2float_rn(__ddiv_rn(S, static_cast<double>(len))) : 0.0f;
-    const float a = __uint_as_float(__ldcg(p.vmax + i));
-    p.s_v[i] = __fdiv_rn(a, 448.0f);
-    p.v_inv[i] = a > 0.0f ? __fdiv_rn(448.0f, a) : 0.0f;
-  }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) st_release(p.ready + unit, 1u);
 }
 
 // ------------------------------------------------------------------- Q
-template <bool kVec, bool kBf16, int DP>
-__device__ __forceinline__ void q_item(const ProParams& p, int64_t unit, int sub) {
-  constexpr int G = DP / 8, R = kThreads / G, P = kBlockM / R;   // P 8 or 4
-  const SegGeo& g = p.g;
-  const int64_t grp = g.Hq / g.Hkv;
-  const int64_t s = unit / g.Hkv;
-  const int64_t hq = (unit % g.Hkv) * grp + sub / p.plan.nqt;
-  const int64_t qt = sub % p.plan.nqt;
-  int64_t start = 0, len = g.Lq;
-  if (g.varlen && !seg_range(g.cu_q, s, g.total_q, g.max_q, &start, &len)) {
-    if (threadIdx.x == 0 && sub == 0) atomicOr(p.status, kStatusBadSeqlens);
-    return;
-  }
-  const int64_t t0 = qt * kBlockM;
-  if (t0 >= len) return;
+// out: q16 row of this thread's first row (r), channel c0.
+template <bool kBf16, int DP, class Rows>
+__device__ __forceinline__ void q_tile(const ProParams& p, int nvalid, const Rows& rows,
+                                       uint16_t* out, float* sq) {
+  constexpr int G = DP / 8, R = kConsumers / G, P = kBlockM / R;   // P 8 or 4
   const int lane = threadIdx.x & 31;
-  const int lc = threadIdx.x % G, r = threadIdx.x / G, c0 = lc * 8;
-  const int D = static_cast<int>(g.D);
-  const uint16_t* qb = p.q + (g.varlen ? start * g.q_tok_stride : s * g.q_seg_stride) +
-                       hq * g.q_head_stride;
-  const int64_t row0 = ws_seg_base(g.varlen, s, start, g.Hq, g.q_head_rows) +
-                       hq * g.q_head_rows + t0;
-  const uint64_t once = policy_evict_first();
+  const int lc = threadIdx.x % G, r = threadIdx.x / G;
+  const bool full = nvalid == kBlockM;
   uint4 raw[P];
 #pragma unroll
-  for (int i = 0; i < P; ++i) {                // all loads first: one round trip
-    const int64_t t = t0 + r + R * i;
-    raw[i] = t < len ? load8<kVec>(qb + t * g.q_tok_stride, c0, D, once)
-                     : make_uint4(0u, 0u, 0u, 0u);
-  }
+  for (int i = 0; i < P; ++i)
+    raw[i] = (full || r + R * i < nvalid) ? rows.template get<R>(i) : make_uint4(0u, 0u, 0u, 0u);
   uint32_t am[P];
 #pragma unroll
   for (int i = 0; i < P; ++i) am[i] = max_mag8(raw[i]);
@@ -512,7 +534,7 @@ __device__ __forceinline__ void q_item(const ProParams& p, int64_t unit, int sub
   const bool odd = (lc & 1) != 0;
   const float quo = __fdiv_rn(odd ? amax : 127.0f, odd ? 127.0f : amax);
   const float mine = amax > 0.0f ? quo : 0.0f;
-  if (odd) p.s_q[row0 + r + R * (lc >> 1)] = mine;
+  if (odd) sq[r + R * (lc >> 1)] = mine;
 #pragma unroll
   for (int i = 0; i < P; ++i) {
     const float inv = __shfl_sync(0xFFFFFFFFu, mine, (lane & ~(G - 1)) | (2 * i));
@@ -521,116 +543,94 @@ __device__ __forceinline__ void q_item(const ProParams& p, int64_t unit, int sub
     o.y = code2(cvt2<kBf16>(raw[i].y), inv, p.one);
     o.z = code2(cvt2<kBf16>(raw[i].z), inv, p.one);
     o.w = code2(cvt2<kBf16>(raw[i].w), inv, p.one);
-    *reinterpret_cast<uint4*>(p.q16 + (row0 + r + R * i) * DP + c0) = o;
+    *reinterpret_cast<uint4*>(out + i * (R * DP)) = o;
   }
 }
 
 // ------------------------------------------------------------------- K
-template <bool kVec, bool kBf16, int DP>
-__device__ __forceinline__ void k_item(const ProParams& p, int64_t unit, int kb_idx,
-                                       Smem& sm) {
-  constexpr int G = DP / 8, R = kThreads / G, P = kBlockN / R;
-  const SegGeo& g = p.g;
-  const int64_t s = unit / g.Hkv, h = unit % g.Hkv;
-  int64_t start = 0, len = g.Lk;
-  if (g.varlen && !seg_range(g.cu_k, s, g.total_k, g.max_k, &start, &len)) return;
-  const int64_t t0 = static_cast<int64_t>(kb_idx) * kBlockN;
-  if (t0 >= len) return;
-  if (!wait_ready(p, unit, sm)) return;
+// out: k16 row of this thread's first row (r), channel c0; mean: the unit's
+// K mean (shared memory).
+template <bool kBf16, int DP, class Rows>
+__device__ __forceinline__ void k_tile(const ProParams& p, int nvalid, const Rows& rows,
+                                       const float* mean, uint16_t* out, float* sk,
+                                       float* red) {
+  constexpr int G = DP / 8, R = kConsumers / G, P = kBlockN / R;
   const int lc = threadIdx.x % G, r = threadIdx.x / G, c0 = lc * 8;
-  const int D = static_cast<int>(g.D);
-  const uint16_t* kb = p.k + (g.varlen ? start * g.k_tok_stride : s * g.k_seg_stride) +
-                       h * g.k_head_stride;
-  const int64_t row0 = ws_seg_base(g.varlen, s, start, g.Hkv, g.k_head_rows) +
-                       h * g.k_head_rows + t0;
+  const bool full = nvalid == kBlockN;
   float2 nmean[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    nmean[i] = make_float2(-__ldcg(p.k_mean + unit * DP + c0 + 2 * i),
-                           -__ldcg(p.k_mean + unit * DP + c0 + 2 * i + 1));
-  const uint64_t last_use = policy_evict_first();
-  // smoothing k - mean (fp32) is recomputed in both passes; the second pass
-  // re-reads its rows; rows past the sequence end count as zero
+  for (int j = 0; j < 4; ++j) nmean[j] = make_float2(-mean[c0 + 2 * j], -mean[c0 + 2 * j + 1]);
+  // smoothing k - mean (fp32) is recomputed in the second pass from the
+  // tile; rows past the sequence end count as zero
   float am = 0.0f;
-  {
-    uint4 raw[P];
 #pragma unroll
-    for (int i = 0; i < P; ++i) {
-      const int64_t t = t0 + r + R * i;
-      raw[i] = t < len ? load8<kVec>(kb + t * g.k_tok_stride, c0, D, last_use)
-                       : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int i = 0; i < P; ++i) {
-      float ar = 0.0f;
+  for (int i = 0; i < P; ++i) {
+    if (full || r + R * i < nvalid) {
+      const uint4 u = rows.template get<R>(i);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float2 kh = __fadd2_rn(cvt2<kBf16>(word(raw[i], j)), nmean[j]);
-        ar = fmaxf(ar, fmaxf(fabsf(kh.x), fabsf(kh.y)));
+        const float2 kh = __fadd2_rn(cvt2<kBf16>(word(u, j)), nmean[j]);
+        am = fmaxf(am, fmaxf(fabsf(kh.x), fabsf(kh.y)));
       }
-      if (t0 + r + R * i < len) am = fmaxf(am, ar);
     }
   }
   am = warp_max(am);
-  if ((threadIdx.x & 31) == 0) sm.u.red[threadIdx.x >> 5] = am;
-  __syncthreads();
-  am = sm.u.red[0];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = am;
+  csync();
+  am = red[0];
 #pragma unroll
-  for (int w = 1; w < kThreads / 32; ++w) am = fmaxf(am, sm.u.red[w]);
+  for (int w = 1; w < kConsumers / 32; ++w) am = fmaxf(am, red[w]);
   const float kinv = am > 0.0f ? __fdiv_rn(127.0f, am) : 0.0f;
 #pragma unroll
   for (int i = 0; i < P; ++i) {
-    const int64_t t = t0 + r + R * i;
     uint4 o = make_uint4(0u, 0u, 0u, 0u);
-    if (t < len) {
-      const uint4 x = load8<kVec, true>(kb + t * g.k_tok_stride, c0, D, last_use);
-      o.x = code2(__fadd2_rn(cvt2<kBf16>(x.x), nmean[0]), kinv, p.one);
-      o.y = code2(__fadd2_rn(cvt2<kBf16>(x.y), nmean[1]), kinv, p.one);
-      o.z = code2(__fadd2_rn(cvt2<kBf16>(x.z), nmean[2]), kinv, p.one);
-      o.w = code2(__fadd2_rn(cvt2<kBf16>(x.w), nmean[3]), kinv, p.one);
+    if (full || r + R * i < nvalid) {
+      const uint4 u = rows.template get<R>(i);
+      o.x = code2(__fadd2_rn(cvt2<kBf16>(u.x), nmean[0]), kinv, p.one);
+      o.y = code2(__fadd2_rn(cvt2<kBf16>(u.y), nmean[1]), kinv, p.one);
+      o.z = code2(__fadd2_rn(cvt2<kBf16>(u.z), nmean[2]), kinv, p.one);
+      o.w = code2(__fadd2_rn(cvt2<kBf16>(u.w), nmean[3]), kinv, p.one);
     }
-    *reinterpret_cast<uint4*>(p.k16 + (row0 + r + R * i) * DP + c0) = o;
+    *reinterpret_cast<uint4*>(out + i * (R * DP)) = o;
   }
-  if (threadIdx.x == 0) p.s_k[row0 / kBlockN] = __fdiv_rn(am, 127.0f);
+  if (threadIdx.x == 0) *sk = __fdiv_rn(am, 127.0f);
 }
 
 // ------------------------------------------------------------------- V
 // A thread quantises 8 channels of 4 consecutive tokens and packs, per
-// channel, the 4 token bytes into one word; word (c, w) of the shared tile
-// sits at c * 32 + (w ^ 4 * (c / 8 % 8)), which spreads the writes over banks
-// and keeps every group of four words (16 bytes of a row) contiguous.
-template <bool kVec, bool kBf16, int DP>
-__device__ __forceinline__ void v_item(const ProParams& p, int64_t unit, int kb_idx,
-                                       Smem& sm) {
-  constexpr int G = DP / 8, RG = kThreads / G, NTW = (kBlockN / 4) / RG;   // NTW 2 or 1
-  const SegGeo& g = p.g;
-  const int64_t s = unit / g.Hkv, h = unit % g.Hkv;
-  int64_t start = 0, len = g.Lk;
-  if (g.varlen && !seg_range(g.cu_k, s, g.total_k, g.max_k, &start, &len)) return;
-  const int64_t t0 = static_cast<int64_t>(kb_idx) * kBlockN;
-  if (t0 >= len) return;
-  if (!wait_ready(p, unit, sm)) return;
+// channel, the 4 token bytes into one word; word (c, w) of the transposed
+// tile sits at c * 32 + (w ^ 4 * (c / 8 % 8)), which spreads the writes over
+// banks and keeps every group of four words (16 bytes of a row) contiguous.
+// The transposed tile overwrites the stage once every row has been read.
+// out: v8 at (channel 0 of the unit, first token of the tile).
+template <bool kTma, bool kBf16, int DP>
+__device__ __forceinline__ void v_tile(const ProParams& p, int nvalid, const TileRows<kTma, DP>& rows,
+                                       const float* vinv_s, uint8_t* out, uint32_t* vt) {
+  constexpr int G = DP / 8, RG = kConsumers / G, NTW = (kBlockN / 4) / RG;   // NTW 2 or 1
   const int lc = threadIdx.x % G, r = threadIdx.x / G, c0 = lc * 8;
-  const int D = static_cast<int>(g.D);
-  const uint16_t* vb = p.v + (g.varlen ? start * g.k_tok_stride : s * g.k_seg_stride) +
-                       h * g.k_head_stride;
+  const bool full = nvalid == kBlockN;
   float vinv[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) vinv[i] = __ldcg(p.v_inv + unit * DP + c0 + i);
-  const uint64_t last_use = policy_evict_first();
+  for (int j = 0; j < 8; ++j) vinv[j] = vinv_s[c0 + j];
+  // thread (lc, r) reads tokens 4 (r + a RG) + e: rows 4r + e + 4 RG a
+  TileRows<kTma, DP> rv = rows;
+  if constexpr (kTma) rv.at = rows.at + 3 * r * DP * 2;          // row r -> row 4r
+  else rv.row0 = rows.row0 + static_cast<int64_t>(3 * r) * rows.tok_stride;
   uint4 raw[NTW][4];
 #pragma unroll
-  for (int a = 0; a < NTW; ++a) {               // all loads first: one round trip
+  for (int a = 0; a < NTW; ++a) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int64_t t = t0 + 4 * (r + a * RG) + e;
-      raw[a][e] = t < len ? load8<kVec>(vb + t * g.k_tok_stride, c0, D, last_use)
-                          : make_uint4(0u, 0u, 0u, 0u);
+      const int t = 4 * (r + a * RG) + e;
+      raw[a][e] = (full || t < nvalid) ? rv.template get<1>(e + 4 * RG * a)
+                                       : make_uint4(0u, 0u, 0u, 0u);
     }
   }
+  csync();                                      // every row read: the stage is free
+  const int swz = ((c0 >> 3) & 7) << 2;         // the same for the 8 channels of c0
 #pragma unroll
   for (int a = 0; a < NTW; ++a) {
-    const int tw = r + a * RG;
+    uint32_t* w0 = vt + c0 * 32 + ((r + a * RG) ^ swz);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {               // channels c0 + 2j, c0 + 2j + 1
       const float2 x0 = cvt2<kBf16>(word(raw[a][0], j));
@@ -643,86 +643,492 @@ __device__ __forceinline__ void v_item(const ProParams& p, int64_t unit, int kb_
       const float2 a23 = __fmul2_rn(make_float2(x2.x, x3.x), i0);
       const float2 b01 = __fmul2_rn(make_float2(x0.y, x1.y), i1);
       const float2 b23 = __fmul2_rn(make_float2(x2.y, x3.y), i1);
-      const uint32_t wa = __byte_perm(pack_e4m3x2(a01.x, a01.y), pack_e4m3x2(a23.x, a23.y), 0x5410);
-      const uint32_t wb = __byte_perm(pack_e4m3x2(b01.x, b01.y), pack_e4m3x2(b23.x, b23.y), 0x5410);
-      const int ca = c0 + 2 * j, cb = ca + 1;
-      sm.u.vt[ca * 32 + (tw ^ (((ca >> 3) & 7) << 2))] = wa;
-      sm.u.vt[cb * 32 + (tw ^ (((cb >> 3) & 7) << 2))] = wb;
+      w0[(2 * j) * 32] = __byte_perm(pack_e4m3x2(a01.x, a01.y), pack_e4m3x2(a23.x, a23.y), 0x5410);
+      w0[(2 * j + 1) * 32] = __byte_perm(pack_e4m3x2(b01.x, b01.y), pack_e4m3x2(b23.x, b23.y), 0x5410);
     }
   }
-  __syncthreads();
-  const int64_t vrow0 = (g.varlen ? 0 : s * g.Hkv * DP) + h * DP;
-  const int64_t vcol0 = (g.varlen ? ws_seg_base(1, s, start, 0, 0) : 0) + t0;
+  csync();
   constexpr int kQuads = DP * (kBlockN / 16);   // 16-byte pieces
+  const int64_t vcols = p.g.v_cols;
 #pragma unroll
-  for (int qi = threadIdx.x; qi < kQuads; qi += kThreads) {
+  for (int qi = threadIdx.x; qi < kQuads; qi += kConsumers) {
     const int c = qi / (kBlockN / 16), tw = 4 * (qi % (kBlockN / 16));
-    const uint4 val = *reinterpret_cast<const uint4*>(&sm.u.vt[c * 32 + (tw ^ (((c >> 3) & 7) << 2))]);
-    *reinterpret_cast<uint4*>(p.v8 + (vrow0 + c) * g.v_cols + vcol0 + 4 * tw) = val;
+    const uint4 val = *reinterpret_cast<const uint4*>(&vt[c * 32 + (tw ^ (((c >> 3) & 7) << 2))]);
+    *reinterpret_cast<uint4*>(out + c * vcols + 4 * tw) = val;
+  }
+}
+
+// ------------------------------------------------------------- consumers
+template <bool kTma, bool kBf16, int DP>
+__device__ __forceinline__ void consume(const ProParams& p, const Slot& it, int stage,
+                                        PSmem& sm) {
+  constexpr int G = DP / 8;
+  const SegGeo& g = p.g;
+  const int64_t s = it.unit / g.Hkv, h = it.unit % g.Hkv;
+  const int lc = threadIdx.x % G, r = threadIdx.x / G, c0 = lc * 8;
+  TileRows<kTma, DP> rows;
+  rows.at = sm.tile[stage] + (r * DP + c0) * 2;
+  rows.c0 = c0;
+  rows.D = static_cast<int>(g.D);
+  int64_t start = 0, len = 0;
+  if (it.kind == kQ) {
+    const int64_t hq = h * (g.Hq / g.Hkv) + it.sub / p.plan.nqt;
+    const int64_t t0 = static_cast<int64_t>(it.sub % p.plan.nqt) * kBlockM;
+    query_range(g, s, &start, &len);
+    if constexpr (!kTma) {
+      rows.row0 = p.q + (g.varlen ? start * g.q_tok_stride : s * g.q_seg_stride) +
+                  hq * g.q_head_stride + (t0 + r) * g.q_tok_stride;
+      rows.tok_stride = g.q_tok_stride;
+    }
+    const int64_t row0 = ws_seg_base(g.varlen, s, start, g.Hq, g.q_head_rows) +
+                         hq * g.q_head_rows + t0;
+    q_tile<kBf16, DP>(p, it.nvalid, rows, p.q16 + (row0 + r) * DP + c0, p.s_q + row0);
+    return;
+  }
+  key_range(g, s, &start, &len);
+  const int64_t t0 = static_cast<int64_t>(it.sub) * kBlockN;
+  if constexpr (!kTma) {
+    const uint16_t* src = (it.kind == kStatsK || it.kind == kK) ? p.k : p.v;
+    rows.row0 = src + (g.varlen ? start * g.k_tok_stride : s * g.k_seg_stride) +
+                h * g.k_head_stride + (t0 + r) * g.k_tok_stride;
+    rows.tok_stride = g.k_tok_stride;
+  }
+  if (it.kind == kStatsK) {
+    stats_k<kBf16, DP>(p, it.unit, it.nvalid, rows, sm.tile[stage]);
+  } else if (it.kind == kStatsV) {
+    stats_v<kBf16, DP>(p, it.unit, it.nvalid, rows, sm.tile[stage]);
+  } else if (it.kind == kK) {
+    const int64_t row0 = ws_seg_base(g.varlen, s, start, g.Hkv, g.k_head_rows) +
+                         h * g.k_head_rows + t0;
+    k_tile<kBf16, DP>(p, it.nvalid, rows, sm.aux[stage], p.k16 + (row0 + r) * DP + c0,
+                      p.s_k + row0 / kBlockN, sm.red);
+  } else {
+    const int64_t vrow0 = (g.varlen ? 0 : s * g.Hkv * DP) + h * DP;
+    const int64_t vcol0 = (g.varlen ? ws_seg_base(1, s, start, 0, 0) : 0) + t0;
+    v_tile<kTma, kBf16, DP>(p, it.nvalid, rows, sm.aux[stage], p.v8 + vrow0 * g.v_cols + vcol0,
+                            reinterpret_cast<uint32_t*>(sm.tile[stage]));
+  }
+}
+
+// ---------------------------------------------------------- statistics
+// Turns a unit's sums into its K mean and V scales (one warp), then raises
+// the unit's ready flag.  The caller has acquired the unit's counter (or the
+// unit has no keys), so every accumulator update is visible; the lanes' writes
+// are ordered before the flag by the warp barrier and the release store.
+template <bool kBf16, int DP>
+__device__ __forceinline__ void finalize_unit(const ProParams& p, int unit, int64_t len) {
+  constexpr int C = DP / 32;                   // channels per lane
+  const int lane = threadIdx.x & 31;
+  const int64_t base = static_cast<int64_t>(unit) * DP + lane;
+  long long sum[C];
+  uint32_t vm[C];
+#pragma unroll
+  for (int j = 0; j < C; ++j) {                // every load in flight at once
+    sum[j] = __ldcg(static_cast<const long long*>(p.ksum) + base + 32 * j);
+    vm[j] = __ldcg(p.vmax + base + 32 * j);
+  }
+#pragma unroll
+  for (int j = 0; j < C; ++j) {
+    double S;
+    if constexpr (kBf16) S = __longlong_as_double(sum[j]);
+    else S = __ll2double_rn(sum[j]) * 5.9604644775390625e-08;   // 2^-24, exact
+    p.k_mean[base + 32 * j] =
+        len > 0 ? __double2float_rn(__ddiv_rn(S, static_cast<double>(len))) : 0.0f;
+    const float a = __uint_as_float(vm[j]);
+    p.s_v[base + 32 * j] = __fdiv_rn(a, 448.0f);
+    p.v_inv[base + 32 * j] = a > 0.0f ? __fdiv_rn(448.0f, a) : 0.0f;
+  }
+  __syncwarp();
+  if (lane == 0) st_release(p.ready + unit, 1u);
+}
+
+// Target of a unit's done counter: its K and V stats tiles.
+__device__ __forceinline__ uint32_t stats_target(const SegGeo& g, int unit, int64_t* len) {
+  int64_t start;
+  if (!key_range(g, unit / g.Hkv, &start, len)) *len = 0;
+  return static_cast<uint32_t>(2 * ((*len + kBlockN - 1) / kBlockN));
+}
+
+// Counts a finished stats tile (handed over by the consumers, whose
+// accumulator updates precede the hand-over) for its unit; the add that
+// completes the count finalizes the unit, whose other tiles' updates its
+// acquire side makes visible.  Called by a whole warp.
+template <bool kBf16, int DP>
+__device__ __forceinline__ void count_tile(const ProParams& p, int unit) {
+  const int lane = threadIdx.x & 31;
+  int64_t len;
+  const uint32_t target = stats_target(p.g, unit, &len);
+  uint32_t last = 0;
+  if (lane == 0) {
+    uint32_t prev;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(prev) : "l"(p.done + unit) : "memory");
+    last = prev + 1 == target;
+  }
+  last = __shfl_sync(0xFFFFFFFFu, last, 0);
+  if (last) {
+    __syncwarp();
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");   // acquire for lanes 1..31
+    finalize_unit<kBf16, DP>(p, unit, len);
+  }
+}
+
+// Takes one finished stats tile off the consumers' queue, if there is one,
+// and counts it (helper warp).  Returns 1 if it counted a tile, -1 on the end marker, 0 if
+// the queue was empty.
+template <bool kBf16, int DP>
+__device__ __forceinline__ int count_queued(const ProParams& p, PSmem& sm, int* q,
+                                            uint32_t* ph) {
+  if (!mbar_test(&sm.qfull[*q], *ph)) return 0;
+  const int unit = sm.queue[*q];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&sm.qempty[*q]);
+  if (++*q == kQueue) {
+    *q = 0;
+    *ph ^= 1u;
+  }
+  if (unit < 0) return -1;
+  count_tile<kBf16, DP>(p, unit);
+  return 1;
+}
+
+// The helper warp has two queues, polled without blocking either:
+//  * finished stats tiles handed over by the consumers, each counted for its
+//    unit (count_tile);
+//  * K/V tiles posted by the producer, whose stage copy expects the unit's
+//    K mean or V multipliers as well: once the unit is final the helper
+//    copies them next to the tile, which completes the stage.
+// Waiting for a unit thus never holds up the producer, which keeps filling
+// the ring, nor the counting of stats tiles.
+template <bool kBf16, int DP>
+__device__ __forceinline__ void helper(const ProParams& p, PSmem& sm) {
+  const int lane = threadIdx.x & 31;
+  int q = 0, rq = 0;
+  uint32_t qph = 0, rph = 0;
+  bool q_end = false, r_end = false, pending = false;
+  int pu = 0, pkind = 0, pstage = 0;
+  uint32_t poll = 0;
+  uint64_t pt0 = 0;
+  volatile int* abort = &sm.abort;
+  while (!(q_end && r_end && !pending) && !*abort) {
+    bool busy = false;
+    if (!q_end) {
+      const int c = count_queued<kBf16, DP>(p, sm, &q, &qph);
+      if (c < 0) q_end = true;
+      if (c != 0) busy = true;
+    }
+    if (!pending && !r_end && mbar_test(&sm.rfull[rq], rph)) {
+      const int4 r = sm.req[rq];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.rempty[rq]);
+      if (++rq == kRequests) {
+        rq = 0;
+        rph ^= 1u;
+      }
+      if (r.x == kEnd) {
+        r_end = true;
+      } else {
+        pending = true;
+        pkind = r.x;
+        pu = r.y;
+        pstage = r.z;
+        pt0 = global_timer_ns();
+        if (lane == 0) poll = ld_relaxed(p.ready + pu);
+      }
+      busy = true;
+    }
+    if (pending) {
+      // the flag was read (relaxed) on the previous turn; its value is
+      // normally back by now, so polling does not hold up the counting
+      uint32_t st = __shfl_sync(0xFFFFFFFFu, poll, 0);
+      if (st == 1u) {
+        if (lane == 0) {
+          // order the copy after the finalizer's writes: acquire, then
+          // hand the generic-proxy data to the copy engine (async proxy)
+          asm volatile("fence.acq_rel.gpu;" ::: "memory");
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          const float* src =
+              (pkind == kK ? p.k_mean : p.v_inv) + static_cast<int64_t>(pu) * DP;
+          bulk_load(sm.aux[pstage], src, DP * 4, &sm.full[pstage]);
+        }
+        pending = false;
+        busy = true;
+      } else if (global_timer_ns() - pt0 > p.timeout_ns) {
+        if (lane == 0) {
+          atomicOr(p.status, kStatusTimeout);
+          // give up: complete the stage with whatever is there
+          bulk_load(sm.aux[pstage], (pkind == kK ? p.k_mean : p.v_inv) +
+                                        static_cast<int64_t>(pu) * DP, DP * 4, &sm.full[pstage]);
+        }
+        pending = false;
+        busy = true;
+      } else if (lane == 0) {
+        poll = ld_relaxed(p.ready + pu);
+      }
+    }
+    if (!busy) __nanosleep(64);
+  }
+}
+
+// Consumer thread 0 hands a finished stats tile (unit >= 0) or the end
+// marker (unit < 0) to the helper warp, which counts it.
+__device__ __forceinline__ bool hand_over(const ProParams& p, PSmem& sm, int unit, int* q,
+                                          uint32_t* ph) {
+  if (!mbar_sleep_wait(&sm.qempty[*q], *ph ^ 1u, &sm.abort, p.status, p.timeout_ns))
+    return false;
+  sm.queue[*q] = unit;
+  mbar_arrive(&sm.qfull[*q]);
+  if (++*q == kQueue) {
+    *q = 0;
+    *ph ^= 1u;
+  }
+  return true;
+}
+
+// The producer warp posts a K/V tile (or the end marker) to the helper.
+__device__ __forceinline__ void post_request(const ProParams& p, PSmem& sm, int kind, int unit,
+                                             int stage, int* rq, uint32_t* rph) {
+  if ((threadIdx.x & 31) == 0) {
+    if (mbar_sleep_wait(&sm.rempty[*rq], *rph ^ 1u, &sm.abort, p.status, p.timeout_ns)) {
+      sm.req[*rq] = make_int4(kind, unit, stage, 0);
+      mbar_arrive(&sm.rfull[*rq]);
+    }
+  }
+  __syncwarp();
+  if (++*rq == kRequests) {
+    *rq = 0;
+    *rph ^= 1u;
+  }
+}
+
+// -------------------------------------------------------------- producer
+template <bool kTma, bool kBf16, int DP>
+__device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
+  const SegGeo& g = p.g;
+  const Plan& P = p.plan;
+  const int lane = threadIdx.x & 31;
+  const uint64_t keep = policy_evict_last(), once = policy_evict_first();
+  int stage = 0;
+  uint32_t upar = 0;       // bit s: parity of the uses of stage s so far
+  uint32_t tma = 0;        // bit s: stage s was last filled by a tensor copy
+  bool ok = true;
+  int rq = 0;
+  uint32_t rph = 0;
+  int idx = 0;
+  if (lane == 0) idx = static_cast<int>(atomicAdd(p.next, 1u));
+  while (true) {
+    idx = __shfl_sync(0xFFFFFFFFu, idx, 0);
+    const int cur = idx;
+    // take the next item now; its index is needed only on the next turn
+    if (lane == 0 && cur < P.total) idx = static_cast<int>(atomicAdd(p.next, 1u));
+    Slot it{kEnd, 0, 0, 0};
+    int64_t s = 0, h = 0, start = 0, len = 0, t0 = 0;
+    if (cur < P.total) {
+      int kind, unit, sub;
+      decode(P, cur, &kind, &unit, &sub);
+      it.kind = kind;
+      it.unit = unit;
+      it.sub = sub;
+      s = unit / g.Hkv;
+      h = unit % g.Hkv;
+      bool seg_ok;
+      if (kind == kQ) {
+        seg_ok = query_range(g, s, &start, &len);
+        h = h * (g.Hq / g.Hkv) + sub / P.nqt;           // query head
+        t0 = static_cast<int64_t>(sub % P.nqt) * kBlockM;
+      } else {
+        seg_ok = key_range(g, s, &start, &len);
+        t0 = static_cast<int64_t>(sub) * kBlockN;
+      }
+      if (!seg_ok) {
+        if (lane == 0 && sub == 0) atomicOr(p.status, kStatusBadSeqlens);
+        len = 0;
+      }
+      if (t0 >= len) {
+        // nothing to load or quantise; an empty unit's statistics are final
+        // (all zero) at once
+        if (kind == kStatsK && sub == 0) finalize_unit<kBf16, DP>(p, unit, 0);
+        continue;
+      }
+      it.nvalid = static_cast<int32_t>(len - t0 < kBlockN ? len - t0 : kBlockN);
+    }
+    // wait until the consumers have released this stage's previous item
+    if (!mbar_sleep_wait(&sm.empty[stage], ((upar >> stage) & 1u) ^ 1u, &sm.abort, p.status,
+                         p.timeout_ns)) {
+      ok = false;
+      break;
+    }
+    if (lane == 0) sm.slot[stage] = it;
+    __syncwarp();
+    if (it.kind == kEnd) {
+      if (lane == 0) mbar_arrive(&sm.full[stage]);
+      post_request(p, sm, kEnd, 0, 0, &rq, &rph);
+      break;
+    }
+    if (lane == 0) {
+      const bool kv = it.kind == kK || it.kind == kV;
+      const uint32_t aux_bytes = kv ? DP * 4 : 0;
+      if constexpr (kTma) {
+        const CUtensorMap* map = it.kind == kQ ? &p.mq
+                               : (it.kind == kStatsK || it.kind == kK) ? &p.mk : &p.mv;
+        const int hnd = it.kind == kQ ? p.q_hnd : p.k_hnd;
+        const int64_t H = it.kind == kQ ? g.Hq : g.Hkv;
+        const int64_t L = it.kind == kQ ? g.Lq : g.Lk;
+        int32_t y, zc;
+        if (hnd) {
+          y = static_cast<int32_t>(t0);
+          zc = static_cast<int32_t>(s * H + h);
+        } else {
+          y = static_cast<int32_t>(h);
+          zc = static_cast<int32_t>((g.varlen ? start : s * L) + t0);
+        }
+        mbar_expect_tx(&sm.full[stage], static_cast<uint32_t>(kBlockN * DP * 2) + aux_bytes);
+        tma_load_3d_hint(sm.tile[stage], map, 0, y, zc, &sm.full[stage],
+                         it.kind <= kStatsV ? keep : once);
+      } else {
+        mbar_expect_tx(&sm.full[stage], aux_bytes);
+      }
+    }
+    // the unit's statistics are copied into the stage by the helper warp
+    if (it.kind == kK || it.kind == kV) post_request(p, sm, it.kind, it.unit, stage, &rq, &rph);
+    if constexpr (kTma) tma |= 1u << stage;
+    upar ^= 1u << stage;
+    stage = stage + 1 == kStages ? 0 : stage + 1;
+  }
+  if (!ok) {
+    // let every copy already issued land before the CTA can exit
+    for (int st = 0; st < kStages; ++st)
+      if (tma & (1u << st))
+        mbar_wait(&sm.full[st], ((upar >> st) & 1u) ^ 1u, nullptr, p.status, p.timeout_ns);
   }
 }
 
 // --------------------------------------------------------------- kernel
-template <bool kVec, bool kBf16, int DP>
-__global__ void __launch_bounds__(kThreads, 3)
+template <bool kTma, bool kBf16, int DP>
+__global__ void __launch_bounds__(kThreads, 2)
 prologue_kernel(const __grid_constant__ ProParams p) {
-  __shared__ __align__(16) Smem sm;
-  if (threadIdx.x == 0) sm.next[0] = static_cast<long long>(atomicAdd(p.next, 1ull));
-  __syncthreads();
-  long long cur = sm.next[0];
-  int buf = 1;
-  while (cur < p.plan.total) {
-    // take the next item now; its index is needed only after this one
-    unsigned long long nxt = 0;
-    if (threadIdx.x == 0) nxt = atomicAdd(p.next, 1ull);
-    const Item it = decode(p.plan, cur);
-    if (it.kind == kItemStats) {
-      stats_item<kVec, kBf16, DP>(p, it.unit, it.sub, sm);
-    } else if (it.kind == kItemQ) {
-      q_item<kVec, kBf16, DP>(p, it.unit, it.sub);
-    } else if ((it.sub & 1) == 0) {
-      k_item<kVec, kBf16, DP>(p, it.unit, it.sub >> 1, sm);
-    } else {
-      v_item<kVec, kBf16, DP>(p, it.unit, it.sub >> 1, sm);
+  extern __shared__ unsigned char smem_raw[];
+  PSmem& sm = *reinterpret_cast<PSmem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
     }
-    if (threadIdx.x == 0) sm.next[buf] = static_cast<long long>(nxt);
-    __syncthreads();
-    cur = sm.next[buf];
-    buf ^= 1;
+    for (int s = 0; s < kQueue; ++s) {
+      mbar_init(&sm.qfull[s], 1);
+      mbar_init(&sm.qempty[s], 1);
+    }
+    for (int s = 0; s < kRequests; ++s) {
+      mbar_init(&sm.rfull[s], 1);
+      mbar_init(&sm.rempty[s], 1);
+    }
+    sm.abort = 0;
+    mbar_fence_init();
   }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5;
+  if (warp == kProducerWarp) {
+    if constexpr (kTma) {
+      if ((threadIdx.x & 31) == 0) {
+        tma_prefetch_desc(&p.mq);
+        tma_prefetch_desc(&p.mk);
+        tma_prefetch_desc(&p.mv);
+      }
+    }
+    produce<kTma, kBf16, DP>(p, sm);
+    return;
+  }
+  if (warp == kHelperWarp) {
+    helper<kBf16, DP>(p, sm);
+    return;
+  }
+  int stage = 0, q = 0;
+  uint32_t phase = 0, qph = 0;
+  while (true) {
+    if (!mbar_sleep_wait(&sm.full[stage], phase, &sm.abort, p.status, p.timeout_ns)) break;
+    const Slot it = sm.slot[stage];
+    if (it.kind == kEnd) break;
+    consume<kTma, kBf16, DP>(p, it, stage, sm);
+    csync();                                    // every consumer is done with the stage
+    if (threadIdx.x == 0) {
+      mbar_arrive(&sm.empty[stage]);
+      if (it.kind <= kStatsV) hand_over(p, sm, it.unit, &q, &qph);
+    }
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+  if (threadIdx.x == 0) hand_over(p, sm, -1, &q, &qph);   // the helper may stop
 }
 
+constexpr size_t kSmemBytes = sizeof(PSmem) + 1024;   // + alignment slack
+
 // Work list of a call: n_q = n_kv = 0 gives statistics only.
-Plan make_plan(const SegGeo& g, bool with_quant, int64_t grid) {
+bool make_plan(const SegGeo& g, bool with_quant, int64_t grid, Plan* out) {
   Plan P{};
   const int64_t maxk = g.varlen ? g.max_k : g.Lk;
   const int64_t maxq = g.varlen ? g.max_q : g.Lq;
-  P.units = g.nseg * g.Hkv;
-  P.n_stats = static_cast<int32_t>(maxk > 0 ? (maxk + kChunk - 1) / kChunk : 1);
-  P.nqt = static_cast<int32_t>((maxq + kBlockM - 1) / kBlockM);
-  if (with_quant) {
-    P.n_q = static_cast<int32_t>(g.Hq / g.Hkv) * P.nqt;
-    P.n_kv = static_cast<int32_t>(2 * ((maxk + kBlockN - 1) / kBlockN));
-  }
-  const int64_t per = P.n_stats + P.n_q + P.n_kv;
-  if (P.n_kv == 0) {
-    P.lag = P.units;                      // no K/V items: everything in the first phase
-  } else {
-    // at least twice the CTAs in flight between a unit's stats and its K/V
-    // items, while the K and V of the units in between stay well inside L2
+  const int64_t nkb = (maxk + kBlockN - 1) / kBlockN;
+  const int64_t units = g.nseg * g.Hkv;
+  const int64_t n_stats = nkb > 0 ? 2 * nkb : 1;
+  const int64_t nqt = (maxq + kBlockM - 1) / kBlockM;
+  const int64_t n_q = with_quant ? (g.Hq / g.Hkv) * nqt : 0;
+  const int64_t n_kv = with_quant ? 2 * nkb : 0;
+  const int64_t per = n_stats + n_q + n_kv;
+  if (units * per >= (int64_t(1) << 31)) return false;
+  int64_t lag = units;                    // no K/V items: everything in the first phase
+  if (n_kv > 0) {
+    // eight items per CTA between a unit's stats and its K/V items (a CTA
+    // holds up to four: its stages and the one being set up), while the K
+    // and V of the units in between stay well inside L2
     const int64_t unit_bytes = 4 * maxk * g.D;
-    int64_t lag = (2 * grid + per - 1) / per;
-    const int64_t l2_budget = 40ll << 20;
+    lag = (8 * grid + per - 1) / per;
+    const int64_t l2_budget = 48ll << 20;
     if (unit_bytes > 0 && lag * unit_bytes > l2_budget) lag = l2_budget / unit_bytes;
     if (lag < 1) lag = 1;
-    if (lag > P.units) lag = P.units;
-    P.lag = lag;
+    if (lag > units) lag = units;
   }
-  P.total = P.units * per;
-  return P;
+  P.units = static_cast<int32_t>(units);
+  P.lag = static_cast<int32_t>(lag);
+  P.total = static_cast<int32_t>(units * per);
+  P.n_stats = static_cast<int32_t>(n_stats);
+  P.n_q = static_cast<int32_t>(n_q);
+  P.n_kv = static_cast<int32_t>(n_kv);
+  P.nqt = static_cast<int32_t>(nqt);
+  *out = P;
+  return true;
 }
 
-template <bool kVec, bool kBf16, int DP>
+// 3D map of a q/k/v input: (channel, token, head plane) for head-major
+// tensors, (channel, head, token) for token-major ones.  Boxes are 128 rows
+// of Dp channels; channels past D are zero-filled by the copy.
+bool input_map(CUtensorMap* map, const uint16_t* base, int64_t D, int64_t Dp, int64_t H,
+               int64_t L, int64_t ntok, bool hnd) {
+  uint64_t dims[3], strides[2];
+  uint32_t box[3];
+  dims[0] = static_cast<uint64_t>(D);
+  strides[0] = static_cast<uint64_t>(D) * 2;
+  box[0] = static_cast<uint32_t>(Dp);
+  if (hnd) {
+    dims[1] = static_cast<uint64_t>(L);
+    dims[2] = static_cast<uint64_t>(ntok / L * H);
+    strides[1] = static_cast<uint64_t>(L * D) * 2;
+    box[1] = 128;
+    box[2] = 1;
+  } else {
+    dims[1] = static_cast<uint64_t>(H);
+    dims[2] = static_cast<uint64_t>(ntok);
+    strides[1] = static_cast<uint64_t>(H * D) * 2;
+    box[1] = 1;
+    box[2] = 128;
+  }
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t*>(base),
+                      dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+template <bool kTma, bool kBf16, int DP>
 cudaError_t launch_t(ProParams& prm, bool with_quant, cudaStream_t st) {
   static int per_sm[64] = {};                  // resident CTAs per SM, per device
   int dev = 0;
@@ -730,9 +1136,13 @@ cudaError_t launch_t(ProParams& prm, bool with_quant, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (per_sm[dev] == 0) {
+    e = cudaFuncSetAttribute(prologue_kernel<kTma, kBf16, DP>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
     int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prologue_kernel<kVec, kBf16, DP>,
-                                                      kThreads, 0);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prologue_kernel<kTma, kBf16, DP>,
+                                                      kThreads, kSmemBytes);
     if (e != cudaSuccess) return e;
     per_sm[dev] = n > 0 ? n : 1;
   }
@@ -740,18 +1150,30 @@ cudaError_t launch_t(ProParams& prm, bool with_quant, cudaStream_t st) {
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   int64_t grid = static_cast<int64_t>(sms) * per_sm[dev];
-  prm.plan = make_plan(prm.g, with_quant, grid);
+  if (!make_plan(prm.g, with_quant, grid, &prm.plan)) return cudaErrorInvalidValue;
   if (grid > prm.plan.total) grid = prm.plan.total;
   if (grid <= 0) return cudaSuccess;
-  prologue_kernel<kVec, kBf16, DP><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(prm);
+  prologue_kernel<kTma, kBf16, DP><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, st>>>(prm);
   note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_any(ProParams& prm, bool vec, bool with_quant, cudaStream_t st) {
-  const bool bf16 = prm.g.dtype == 1;
-  const bool d64 = prm.g.Dp == 64;
+  const SegGeo& g = prm.g;
+  const bool bf16 = g.dtype == 1;
+  const bool d64 = g.Dp == 64;
   if (vec) {
+    // tensor maps of the inputs (a tensor with no tokens is never read)
+    prm.q_hnd = !g.varlen && g.q_tok_stride == g.D;
+    prm.k_hnd = !g.varlen && g.k_tok_stride == g.D;
+    const int64_t ntq = g.varlen ? g.total_q : g.nseg * g.Lq;
+    const int64_t ntk = g.varlen ? g.total_k : g.nseg * g.Lk;
+    if (prm.q != nullptr && ntq > 0 &&
+        !input_map(&prm.mq, prm.q, g.D, g.Dp, g.Hq, g.Lq, ntq, prm.q_hnd))
+      return cudaErrorInvalidValue;
+    if (ntk > 0 && (!input_map(&prm.mk, prm.k, g.D, g.Dp, g.Hkv, g.Lk, ntk, prm.k_hnd) ||
+                    !input_map(&prm.mv, prm.v, g.D, g.Dp, g.Hkv, g.Lk, ntk, prm.k_hnd)))
+      return cudaErrorInvalidValue;
     if (bf16) return d64 ? launch_t<true, true, 64>(prm, with_quant, st)
                          : launch_t<true, true, 128>(prm, with_quant, st);
     return d64 ? launch_t<true, false, 64>(prm, with_quant, st)
@@ -827,7 +1249,7 @@ cudaError_t launch_kv_stats_static(const SegGeo& g, const uint16_t* k,
   prm.k = k; prm.v = v;
   prm.k_mean = k_mean; prm.s_v = s_v;
   prm.status = reinterpret_cast<uint32_t*>(base);
-  prm.next = reinterpret_cast<unsigned long long*>(base + 8);
+  prm.next = reinterpret_cast<unsigned int*>(base + 8);
   prm.done = reinterpret_cast<uint32_t*>(base + 256);
   prm.ready = reinterpret_cast<uint32_t*>(base + 256 + 4 * kMaxStaticUnits);
   prm.ksum = base + kStaticHeader;

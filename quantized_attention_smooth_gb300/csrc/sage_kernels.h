@@ -9,6 +9,12 @@
 
 namespace sage {
 
+// cuTensorMapEncodeTiled (looked up once through the runtime): 16-bit or
+// 8-bit elements, no interleave, 256-byte L2 promotion, zero fill.
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, uint32_t rank, void* base,
+                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                  CUtensorMapSwizzle swizzle);
+
 // Counts one kernel launch of this library (process-wide, all devices).
 void note_launch();
 uint64_t launch_count();
@@ -29,7 +35,7 @@ struct PrologueBuffers {
   uint32_t* vmax;    // float bits, [nseg][Hkv][Dp]
   uint32_t* done;    // stats items finished per (segment, kv head), zeroed
   uint32_t* ready;   // per (segment, kv head): statistics final, zeroed
-  unsigned long long* next;   // work-item counter, zeroed
+  unsigned int* next;         // work-item counter, zeroed
   uint32_t* status;
   uint64_t timeout_ns;        // bound of every wait
 };
