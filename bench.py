@@ -34,9 +34,10 @@ DEFAULT_WORKLOAD = "b2_h24_l4096_d128"
 L2_FLUSH_BYTES = 256 << 20
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes per attention-kernel launch from the ncu capture summarised in
-# profiles/ (None until a capture of the current kernel exists).
-ATTN_NCU_DRAM_BYTES = None
+# DRAM bytes (read + write) per attention-kernel launch on the default
+# workload, from the ncu capture summarised in
+# profiles/attn_kernel_b2_h24_l4096_d128.md (None for other workloads).
+ATTN_NCU_DRAM_BYTES = {"b2_h24_l4096_d128": 126.747136e6 + 58.950656e6}
 
 
 def load_peaks():
@@ -352,7 +353,7 @@ def main():
         "config": config_of(w),
         "roofline": {"bound": "tensor", "achieved": att_tflops, "peak": mix_peak,
                      "unit": "TFLOP/s", "frac": att_tflops / mix_peak,
-                     "traffic": ATTN_NCU_DRAM_BYTES,
+                     "traffic": ATTN_NCU_DRAM_BYTES.get(w.name),
                      "kernel": "attn_kernel (fused QK^T/softmax/PV)",
                      "peak_note": f"4/3 x {src} bf16 burst {bf16} (QK^T at the 16-bit "
                                   "rate, PV at the FP8 rate)",
