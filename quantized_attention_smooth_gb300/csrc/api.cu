@@ -63,7 +63,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Byte offsets of every workspace buffer.
 struct WsLayout {
-  size_t status, ksum, vmax, done, ready, zero_end, k_mean, s_v, v_inv, s_q, s_k, q16, k16,
+  size_t status, ksum, vmax, done, sync, zero_end, k_mean, s_v, v_inv, s_q, s_k, q16, k16,
       v8, total;
 };
 
@@ -78,7 +78,7 @@ WsLayout ws_layout(const SegGeo& g) {
   w.ksum = o; o = align256(o + nstat * 8);
   w.vmax = o; o = align256(o + nstat * 4);
   w.done = o; o = align256(o + g.nseg * g.Hkv * 4);
-  w.ready = o; o = align256(o + g.nseg * g.Hkv * 4);
+  w.sync = o; o = align256(o + 3 * 64 * 4);
   // means and scales start at zero: a segment without keys keeps them so
   w.k_mean = o; o = align256(o + nstat * 4);
   w.s_v = o; o = align256(o + nstat * 4);
@@ -290,8 +290,7 @@ sage_status run_prologue(const SegGeo& g, const void* q, const void* k, const vo
   b.ksum = wsb + w.ksum;
   b.vmax = reinterpret_cast<uint32_t*>(wsb + w.vmax);
   b.done = reinterpret_cast<uint32_t*>(wsb + w.done);
-  b.ready = reinterpret_cast<uint32_t*>(wsb + w.ready);
-  b.next = reinterpret_cast<unsigned int*>(wsb + w.status + 8);
+  b.sync = reinterpret_cast<unsigned int*>(wsb + w.sync);
   b.timeout_ns = wait_timeout_ns();
   b.status = reinterpret_cast<uint32_t*>(wsb + w.status);
   const bool vec = (g.D % 8 == 0) && aligned(q, 16) && aligned(k, 16) && aligned(v, 16);

@@ -6,13 +6,13 @@
 // overview's Core features (INT8 Q/K, smoothing) and the SageAttention-RDNA4
 // v0.4.0 notes (key mean summed in fp64, 64-bit offsets).
 //
-// One persistent kernel, two CTAs per SM.  A CTA has eight consumer warps, a
-// producer warp and a helper warp around a ring of three 32 KB shared-memory
-// stages.  The producer takes work items, in order, from a counter in the
-// workspace and copies each item's 128-token input tile into a free stage
-// with a tensor copy (TMA), zero-padded to Dp channels; the consumers
-// quantise the tile in the stage and release it.  A unit is one (segment,
-// kv head); its items are
+// One persistent kernel, two CTAs per SM, launched cooperatively (every CTA
+// resident).  A CTA has eight consumer warps, a producer warp and a helper
+// warp around a ring of three 32 KB shared-memory stages.  The producer takes
+// work items from a counter in the workspace and copies each item's 128-token
+// input tile into a free stage with a tensor copy (TMA), zero-padded to Dp
+// channels; the consumers quantise the tile in the stage and release it.  A
+// unit is one (segment, kv head); its items are
 //   stats K   128 keys: exact per-channel sums (int64 fixed point at 2^-24
 //             for fp16, fp64 for bf16), added to the unit's accumulators;
 //   stats V   128 values: per-channel max |v|, likewise;
@@ -20,23 +20,23 @@
 //             codes (stored as exact fp16 integers, the tensor-core operand),
 //             one scale per token;
 //   K         128 keys: smoothed K (k - mean, fp32) -> int8 codes, one scale
-//             per block;
-//   V         128 values: e4m3 per channel, transposed to channel-major.
-// Consumers hand every finished stats tile to the helper warp, which counts
-// it for its unit; the count that completes a unit makes the helper turn
-// the sums into the K mean, the V scale and its reciprocal multiplier and
-// raise the unit's ready flag.  A K or V tile's stage also expects the
-// unit's means (or multipliers): the helper copies them next to the tile
-// once the unit is final, so the producer never waits on a unit and the
-// consumers read nothing but their stage.  The list puts a unit's K and V
-// items `lag` units after its stats and Q items: far enough that the unit
-// is normally final by then, near enough that its K and V are still in L2
-// (the stats copies mark them evict-last).  Items are taken in list order by
-// running CTAs and issued in that order, and a stats tile never waits, so
-// the wait of the lowest waiting item always ends; every wait is bounded all
-// the same (timeout -> status bit).  Every 128-token tile of the workspace
-// is written in full (zeros past the sequence end and past D), so the
-// attention kernel never reads stale bytes.
+//             per block (the unit's K mean is copied next to the tile);
+//   V         128 values: e4m3 per channel (multipliers next to the tile),
+//             transposed to channel-major.
+// The units are cut into groups whose K and V fit comfortably in L2, and
+// each group has two lists: A (its stats and Q tiles) and B (its K and V
+// tiles, which need the group's statistics).  A items never wait; a CTA that
+// has taken the last A item of group g arrives at the group's barrier (a
+// counter) once its stats tiles of the group are counted, and B items of the
+// group are taken only after every CTA has arrived, so they find their
+// statistics final and their K and V, read by the A list with an evict-last
+// hint, still in L2.  The A list runs at most one group ahead of the B list.
+// Consumers hand each finished stats tile to the helper warp, which counts it
+// for its unit; the count that completes a unit finalizes it (K mean, V
+// scale and reciprocal multiplier).  Nothing waits inside a list, and every
+// wait is bounded (timeout -> status bit).  Every 128-token tile of the
+// workspace is written in full (zeros past the sequence end and past D), so
+// the attention kernel never reads stale bytes.
 //
 // Without 16-byte aligned rows (D % 8 != 0 or unaligned tensors) the same
 // kernel runs with element-wise global loads instead of tensor copies.
@@ -62,7 +62,7 @@ constexpr int kHelperWarp = 9;
 constexpr int kThreads = kConsumers + 64;
 constexpr int kStages = 3;
 constexpr int kQueue = 8;                    // finished stats tiles awaiting the helper
-constexpr int kRequests = 4;                 // K/V tiles awaiting their statistics
+constexpr int kMaxGroups = 64;               // counters per list in the workspace
 constexpr int kTileBytes = 128 * 128 * 2;    // 128 rows of up to 128 16-bit values
 constexpr uint32_t kSleepNs = 20000;         // suspend hint of barrier waits
 // fp32 2^23 + 2^22 + 0x6600: adding it rounds to an integer n (ties to even)
@@ -70,13 +70,21 @@ constexpr uint32_t kSleepNs = 20000;         // suspend hint of barrier waits
 constexpr float kCodeMagic = 12609024.0f;
 constexpr float kRintMagic = 12582912.0f;    // 1.5 * 2^23
 
-enum ItemKind { kStatsK = 0, kStatsV = 1, kQ = 2, kK = 3, kV = 4, kEnd = 5 };
+enum ItemKind { kStatsK = 0, kStatsV = 1, kQ = 2, kK = 3, kV = 4, kEnd = 5, kGroupEnd = 6 };
 
-// Work list of one call (host-computed; every count fits in 31 bits).
+// Work of one call (host-computed; every count fits in 31 bits).  The units
+// are cut into groups whose K and V fit comfortably in L2.  Each group has
+// two item lists with their own counters: A (stats and Q tiles, no
+// dependencies) and B (K and V tiles, which need the group's statistics).
+// A CTA that has taken its last A item of group g says so at group g's
+// barrier; once every CTA has (and has counted its stats tiles), the
+// group's statistics are final and its B items may be taken.  A items never
+// wait, and may run one group ahead of the B items, which bounds the K and V
+// held in L2 between their two reads.
 struct Plan {
   int32_t units;      // nseg * Hkv
-  int32_t lag;        // units between a unit's stats/Q items and its K/V items
-  int32_t total;      // items
+  int32_t group;      // units per group
+  int32_t groups;
   int32_t n_stats;    // stats items per unit (K and V tiles alternate)
   int32_t n_q;        // Q items per unit (query heads of the kv head x tiles)
   int32_t n_kv;       // K and V items per unit (K and V tiles alternate)
@@ -100,8 +108,9 @@ struct ProParams {
   void* ksum;                 // int64 (fp16) or double (bf16) per (unit, channel)
   uint32_t* vmax;             // float bits per (unit, channel)
   uint32_t* done;             // stats tiles finished per unit
-  uint32_t* ready;            // per unit: statistics final
-  unsigned int* next;         // work counter
+  unsigned int* cnt_a;        // [kMaxGroups] A-list counters
+  unsigned int* cnt_b;        // [kMaxGroups] B-list counters
+  unsigned int* gbar;         // [kMaxGroups] CTAs done with the group's A list
   uint32_t* status;
   uint64_t timeout_ns;
   int32_t q_hnd, k_hnd;       // 1: tiles are (head, token) planes; 0: token-major
@@ -120,48 +129,22 @@ struct alignas(1024) PSmem {
   uint64_t empty[kStages];
   uint64_t qfull[kQueue];
   uint64_t qempty[kQueue];
-  uint64_t rfull[kRequests];
-  uint64_t rempty[kRequests];
   int32_t queue[kQueue];
-  int4 req[kRequests];        // (kind, unit, stage, -) of a K/V tile awaiting its statistics
   Slot slot[kStages];
   float red[8];
   int abort;
 };
 
-// Item i of the list: (kind, unit, sub).  Slots 0 .. lag-1 hold stats and Q
-// items of units 0 .. lag-1; slot j >= lag holds those of unit j and then
-// the K/V items of unit j - lag; the last lag slots hold K/V items only.
-__device__ __forceinline__ void decode(const Plan& P, int i, int* kind, int* unit, int* sub) {
+__device__ __forceinline__ int group_units(const Plan& P, int g) {
+  return min(P.units - g * P.group, P.group);
+}
+
+// Item i of group g's A list (stats tiles of each unit, then its Q tiles).
+__device__ __forceinline__ void decode_a(const Plan& P, int g, int i, int* kind, int* unit,
+                                         int* sub) {
   const int a = P.n_stats + P.n_q;
-  const int per = a + P.n_kv;
-  int off;
-  if (i < P.lag * a) {
-    *unit = i / a;
-    off = i - *unit * a;
-  } else {
-    i -= P.lag * a;
-    const int mid = (P.units - P.lag) * per;
-    if (i >= mid) {
-      i -= mid;
-      const int j = i / P.n_kv;
-      *unit = P.units - P.lag + j;
-      off = i - j * P.n_kv;
-      *kind = (off & 1) ? kV : kK;
-      *sub = off >> 1;
-      return;
-    }
-    const int j = i / per;
-    off = i - j * per;
-    if (off >= a) {
-      *unit = j;
-      off -= a;
-      *kind = (off & 1) ? kV : kK;
-      *sub = off >> 1;
-      return;
-    }
-    *unit = P.lag + j;
-  }
+  const int u = i / a, off = i - u * a;
+  *unit = g * P.group + u;
   if (off < P.n_stats) {
     *kind = (off & 1) ? kStatsV : kStatsK;
     *sub = off >> 1;
@@ -169,6 +152,15 @@ __device__ __forceinline__ void decode(const Plan& P, int i, int* kind, int* uni
     *kind = kQ;
     *sub = off - P.n_stats;
   }
+}
+
+// Item i of group g's B list (K and V tiles alternate).
+__device__ __forceinline__ void decode_b(const Plan& P, int g, int i, int* kind, int* unit,
+                                         int* sub) {
+  const int u = i / P.n_kv, off = i - u * P.n_kv;
+  *unit = g * P.group + u;
+  *kind = (off & 1) ? kV : kK;
+  *sub = off >> 1;
 }
 
 // ------------------------------------------------------------ memory ops
@@ -202,14 +194,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
-__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
-}
 
 // Barrier of the eight consumer warps (the other two warps run on their own).
 __device__ __forceinline__ void csync() {
@@ -242,15 +226,6 @@ __device__ __forceinline__ bool mbar_sleep_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
-  return ok != 0;
-}
 
 // ------------------------------------------------------------- numerics
 __device__ __forceinline__ uint32_t word(const uint4& u, int i) {
@@ -435,7 +410,8 @@ __device__ __forceinline__ void stats_k(const ProParams& p, int unit, int nvalid
     }
   }
   // lanes holding the same channels (warp shuffles), then the eight warps
-  // through shared memory (the stage, once every row has been read)
+  // through shared memory (the stage, once every row has been read), one
+  // atomic per channel (per-warp atomics contend on the same addresses)
 #pragma unroll
   for (int o = G; o < 32; o <<= 1) {
 #pragma unroll
@@ -711,10 +687,9 @@ __device__ __forceinline__ void consume(const ProParams& p, const Slot& it, int 
 }
 
 // ---------------------------------------------------------- statistics
-// Turns a unit's sums into its K mean and V scales (one warp), then raises
-// the unit's ready flag.  The caller has acquired the unit's counter (or the
-// unit has no keys), so every accumulator update is visible; the lanes' writes
-// are ordered before the flag by the warp barrier and the release store.
+// Turns a unit's sums into its K mean and V scales (one warp).  The caller
+// has acquired the unit's counter (or the unit has no keys), so every
+// accumulator update is visible.
 template <bool kBf16, int DP>
 __device__ __forceinline__ void finalize_unit(const ProParams& p, int unit, int64_t len) {
   constexpr int C = DP / 32;                   // channels per lane
@@ -738,8 +713,6 @@ __device__ __forceinline__ void finalize_unit(const ProParams& p, int unit, int6
     p.s_v[base + 32 * j] = __fdiv_rn(a, 448.0f);
     p.v_inv[base + 32 * j] = a > 0.0f ? __fdiv_rn(448.0f, a) : 0.0f;
   }
-  __syncwarp();
-  if (lane == 0) st_release(p.ready + unit, 1u);
 }
 
 // Target of a unit's done counter: its K and V stats tiles.
@@ -773,105 +746,47 @@ __device__ __forceinline__ void count_tile(const ProParams& p, int unit) {
   }
 }
 
-// Takes one finished stats tile off the consumers' queue, if there is one,
-// and counts it (helper warp).  Returns 1 if it counted a tile, -1 on the end marker, 0 if
-// the queue was empty.
-template <bool kBf16, int DP>
-__device__ __forceinline__ int count_queued(const ProParams& p, PSmem& sm, int* q,
-                                            uint32_t* ph) {
-  if (!mbar_test(&sm.qfull[*q], *ph)) return 0;
-  const int unit = sm.queue[*q];
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(&sm.qempty[*q]);
-  if (++*q == kQueue) {
-    *q = 0;
-    *ph ^= 1u;
-  }
-  if (unit < 0) return -1;
-  count_tile<kBf16, DP>(p, unit);
-  return 1;
+// Markers the consumers hand to the helper besides finished stats tiles:
+// the end, and the end of group g's A list (kMarkGroup - g).
+constexpr int kMarkEnd = -1;
+constexpr int kMarkGroup = -2;
+
+// Group g's barrier (helper lane 0): this CTA has taken its last A item of
+// the group and counted every stats tile of it; the release makes the units
+// it finalized visible to whoever acquires the barrier count.
+__device__ __forceinline__ void group_arrive(const ProParams& p, int g) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(p.gbar + g) : "memory");
 }
 
-// The helper warp has two queues, polled without blocking either:
-//  * finished stats tiles handed over by the consumers, each counted for its
-//    unit (count_tile);
-//  * K/V tiles posted by the producer, whose stage copy expects the unit's
-//    K mean or V multipliers as well: once the unit is final the helper
-//    copies them next to the tile, which completes the stage.
-// Waiting for a unit thus never holds up the producer, which keeps filling
-// the ring, nor the counting of stats tiles.
+// The helper warp takes what the consumers hand over, in order: a finished
+// stats tile is counted for its unit (count_tile); a group marker means the
+// CTA is done with the group's A list (every stats tile of it counted), so
+// the helper arrives at the group's barrier.  It never waits for other CTAs.
 template <bool kBf16, int DP>
 __device__ __forceinline__ void helper(const ProParams& p, PSmem& sm) {
   const int lane = threadIdx.x & 31;
-  int q = 0, rq = 0;
-  uint32_t qph = 0, rph = 0;
-  bool q_end = false, r_end = false, pending = false;
-  int pu = 0, pkind = 0, pstage = 0;
-  uint32_t poll = 0;
-  uint64_t pt0 = 0;
-  volatile int* abort = &sm.abort;
-  while (!(q_end && r_end && !pending) && !*abort) {
-    bool busy = false;
-    if (!q_end) {
-      const int c = count_queued<kBf16, DP>(p, sm, &q, &qph);
-      if (c < 0) q_end = true;
-      if (c != 0) busy = true;
+  int q = 0;
+  uint32_t qph = 0;
+  while (true) {
+    if (!mbar_sleep_wait(&sm.qfull[q], qph, &sm.abort, p.status, p.timeout_ns)) return;
+    const int unit = sm.queue[q];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.qempty[q]);
+    if (++q == kQueue) {
+      q = 0;
+      qph ^= 1u;
     }
-    if (!pending && !r_end && mbar_test(&sm.rfull[rq], rph)) {
-      const int4 r = sm.req[rq];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.rempty[rq]);
-      if (++rq == kRequests) {
-        rq = 0;
-        rph ^= 1u;
-      }
-      if (r.x == kEnd) {
-        r_end = true;
-      } else {
-        pending = true;
-        pkind = r.x;
-        pu = r.y;
-        pstage = r.z;
-        pt0 = global_timer_ns();
-        if (lane == 0) poll = ld_relaxed(p.ready + pu);
-      }
-      busy = true;
+    if (unit == kMarkEnd) return;
+    if (unit <= kMarkGroup) {
+      if (lane == 0) group_arrive(p, kMarkGroup - unit);
+      continue;
     }
-    if (pending) {
-      // the flag was read (relaxed) on the previous turn; its value is
-      // normally back by now, so polling does not hold up the counting
-      uint32_t st = __shfl_sync(0xFFFFFFFFu, poll, 0);
-      if (st == 1u) {
-        if (lane == 0) {
-          // order the copy after the finalizer's writes: acquire, then
-          // hand the generic-proxy data to the copy engine (async proxy)
-          asm volatile("fence.acq_rel.gpu;" ::: "memory");
-          asm volatile("fence.proxy.async.global;" ::: "memory");
-          const float* src =
-              (pkind == kK ? p.k_mean : p.v_inv) + static_cast<int64_t>(pu) * DP;
-          bulk_load(sm.aux[pstage], src, DP * 4, &sm.full[pstage]);
-        }
-        pending = false;
-        busy = true;
-      } else if (global_timer_ns() - pt0 > p.timeout_ns) {
-        if (lane == 0) {
-          atomicOr(p.status, kStatusTimeout);
-          // give up: complete the stage with whatever is there
-          bulk_load(sm.aux[pstage], (pkind == kK ? p.k_mean : p.v_inv) +
-                                        static_cast<int64_t>(pu) * DP, DP * 4, &sm.full[pstage]);
-        }
-        pending = false;
-        busy = true;
-      } else if (lane == 0) {
-        poll = ld_relaxed(p.ready + pu);
-      }
-    }
-    if (!busy) __nanosleep(64);
+    count_tile<kBf16, DP>(p, unit);
   }
 }
 
-// Consumer thread 0 hands a finished stats tile (unit >= 0) or the end
-// marker (unit < 0) to the helper warp, which counts it.
+// Consumer thread 0 hands a finished stats tile (unit >= 0) or a marker to
+// the helper warp.
 __device__ __forceinline__ bool hand_over(const ProParams& p, PSmem& sm, int unit, int* q,
                                           uint32_t* ph) {
   if (!mbar_sleep_wait(&sm.qempty[*q], *ph ^ 1u, &sm.abort, p.status, p.timeout_ns))
@@ -885,22 +800,6 @@ __device__ __forceinline__ bool hand_over(const ProParams& p, PSmem& sm, int uni
   return true;
 }
 
-// The producer warp posts a K/V tile (or the end marker) to the helper.
-__device__ __forceinline__ void post_request(const ProParams& p, PSmem& sm, int kind, int unit,
-                                             int stage, int* rq, uint32_t* rph) {
-  if ((threadIdx.x & 31) == 0) {
-    if (mbar_sleep_wait(&sm.rempty[*rq], *rph ^ 1u, &sm.abort, p.status, p.timeout_ns)) {
-      sm.req[*rq] = make_int4(kind, unit, stage, 0);
-      mbar_arrive(&sm.rfull[*rq]);
-    }
-  }
-  __syncwarp();
-  if (++*rq == kRequests) {
-    *rq = 0;
-    *rph ^= 1u;
-  }
-}
-
 // -------------------------------------------------------------- producer
 template <bool kTma, bool kBf16, int DP>
 __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
@@ -912,42 +811,119 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
   uint32_t upar = 0;       // bit s: parity of the uses of stage s so far
   uint32_t tma = 0;        // bit s: stage s was last filled by a tensor copy
   bool ok = true;
-  int rq = 0;
-  uint32_t rph = 0;
-  int idx = 0;
-  if (lane == 0) idx = static_cast<int>(atomicAdd(p.next, 1u));
-  while (true) {
-    idx = __shfl_sync(0xFFFFFFFFu, idx, 0);
-    const int cur = idx;
-    // take the next item now; its index is needed only on the next turn
-    if (lane == 0 && cur < P.total) idx = static_cast<int>(atomicAdd(p.next, 1u));
-    Slot it{kEnd, 0, 0, 0};
+  int ga = 0, gb = 0;      // group of the A list / B list being taken
+  bool b_open = false;     // group gb's statistics are final
+  uint32_t poll = 0;       // group gb's barrier count, read on the previous turn
+  bool polled = false;
+  int a_idx = 0, b_idx = 0;  // claims taken ahead (lane 0), valid when *_pend
+  bool a_pend = false, b_pend = false;
+  const uint32_t grid = gridDim.x;
+  uint64_t idle0 = 0;
+  while (ok) {
+    // ---- choose the next item: a B item if its group is final, else an A
+    // item (at most one group ahead of the B list), else poll and wait
+    Slot it{-1, 0, 0, 0};
+    bool marker = false;
+    while (gb < P.groups) {
+      if (!b_open) {
+        if (polled) {
+          polled = false;
+          if (__shfl_sync(0xFFFFFFFFu, poll, 0) >= grid) {
+            b_open = true;
+            if (lane == 0) {
+              // acquire the group's statistics; the copy engine (async proxy)
+              // reads them below
+              asm volatile("fence.acq_rel.gpu;" ::: "memory");
+              asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
+            __syncwarp();
+          }
+        }
+        if (!b_open) break;
+      }
+      if (!b_pend && lane == 0) b_idx = static_cast<int>(atomicAdd(p.cnt_b + gb, 1u));
+      const int idx = __shfl_sync(0xFFFFFFFFu, b_idx, 0);
+      b_pend = false;
+      if (idx < group_units(P, gb) * P.n_kv) {
+        decode_b(P, gb, idx, &it.kind, &it.unit, &it.sub);
+        // claim the group's next B item now; it is used on the next turn
+        if (lane == 0) b_idx = static_cast<int>(atomicAdd(p.cnt_b + gb, 1u));
+        b_pend = true;
+        break;
+      }
+      ++gb;
+      b_open = false;
+    }
+    if (it.kind < 0 && ga < P.groups && (P.n_kv == 0 || ga <= gb + 1)) {
+      if (!a_pend && lane == 0) a_idx = static_cast<int>(atomicAdd(p.cnt_a + ga, 1u));
+      const int idx = __shfl_sync(0xFFFFFFFFu, a_idx, 0);
+      a_pend = false;
+      if (idx < group_units(P, ga) * (P.n_stats + P.n_q)) {
+        decode_a(P, ga, idx, &it.kind, &it.unit, &it.sub);
+        // claim the group's next A item now (A items never wait, so holding
+        // the claim cannot hold up a barrier)
+        if (lane == 0) a_idx = static_cast<int>(atomicAdd(p.cnt_a + ga, 1u));
+        a_pend = true;
+      } else {
+        it.kind = kGroupEnd;                  // this CTA is done with group ga's A list
+        it.unit = ga;
+        marker = true;
+        ++ga;
+      }
+    }
+    if (it.kind < 0) {
+      if (ga >= P.groups && (P.n_kv == 0 || gb >= P.groups)) {
+        it.kind = kEnd;
+        marker = true;
+      } else {
+        // nothing to take yet: read group gb's barrier count for the next turn
+        if (!polled && gb < P.groups && !b_open) {
+          if (lane == 0)
+            asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];"
+                         : "=r"(poll) : "l"(p.gbar + gb) : "memory");
+          polled = true;
+        }
+        if (idle0 == 0) idle0 = global_timer_ns();
+        else if (global_timer_ns() - idle0 > p.timeout_ns) {
+          if (lane == 0) atomicOr(p.status, kStatusTimeout);
+          sm.abort = 1;
+          ok = false;
+          break;
+        }
+        __nanosleep(64);
+        continue;
+      }
+    }
+    idle0 = 0;
+    if (!polled && gb < P.groups && !b_open) {
+      // keep the barrier read in flight while this item is set up
+      if (lane == 0)
+        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];"
+                     : "=r"(poll) : "l"(p.gbar + gb) : "memory");
+      polled = true;
+    }
+
     int64_t s = 0, h = 0, start = 0, len = 0, t0 = 0;
-    if (cur < P.total) {
-      int kind, unit, sub;
-      decode(P, cur, &kind, &unit, &sub);
-      it.kind = kind;
-      it.unit = unit;
-      it.sub = sub;
-      s = unit / g.Hkv;
-      h = unit % g.Hkv;
+    if (!marker) {
+      s = it.unit / g.Hkv;
+      h = it.unit % g.Hkv;
       bool seg_ok;
-      if (kind == kQ) {
+      if (it.kind == kQ) {
         seg_ok = query_range(g, s, &start, &len);
-        h = h * (g.Hq / g.Hkv) + sub / P.nqt;           // query head
-        t0 = static_cast<int64_t>(sub % P.nqt) * kBlockM;
+        h = h * (g.Hq / g.Hkv) + it.sub / P.nqt;        // query head
+        t0 = static_cast<int64_t>(it.sub % P.nqt) * kBlockM;
       } else {
         seg_ok = key_range(g, s, &start, &len);
-        t0 = static_cast<int64_t>(sub) * kBlockN;
+        t0 = static_cast<int64_t>(it.sub) * kBlockN;
       }
       if (!seg_ok) {
-        if (lane == 0 && sub == 0) atomicOr(p.status, kStatusBadSeqlens);
+        if (lane == 0 && it.sub == 0) atomicOr(p.status, kStatusBadSeqlens);
         len = 0;
       }
       if (t0 >= len) {
         // nothing to load or quantise; an empty unit's statistics are final
         // (all zero) at once
-        if (kind == kStatsK && sub == 0) finalize_unit<kBf16, DP>(p, unit, 0);
+        if (it.kind == kStatsK && it.sub == 0) finalize_unit<kBf16, DP>(p, it.unit, 0);
         continue;
       }
       it.nvalid = static_cast<int32_t>(len - t0 < kBlockN ? len - t0 : kBlockN);
@@ -960,10 +936,13 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
     }
     if (lane == 0) sm.slot[stage] = it;
     __syncwarp();
-    if (it.kind == kEnd) {
+    if (marker) {
       if (lane == 0) mbar_arrive(&sm.full[stage]);
-      post_request(p, sm, kEnd, 0, 0, &rq, &rph);
-      break;
+      tma &= ~(1u << stage);
+      upar ^= 1u << stage;
+      stage = stage + 1 == kStages ? 0 : stage + 1;
+      if (it.kind == kEnd) break;
+      continue;
     }
     if (lane == 0) {
       const bool kv = it.kind == kK || it.kind == kV;
@@ -988,9 +967,13 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
       } else {
         mbar_expect_tx(&sm.full[stage], aux_bytes);
       }
+      if (kv) {
+        // the unit's K mean or V multipliers, final since its group's barrier
+        const float* src =
+            (it.kind == kK ? p.k_mean : p.v_inv) + static_cast<int64_t>(it.unit) * DP;
+        bulk_load(sm.aux[stage], src, aux_bytes, &sm.full[stage]);
+      }
     }
-    // the unit's statistics are copied into the stage by the helper warp
-    if (it.kind == kK || it.kind == kV) post_request(p, sm, it.kind, it.unit, stage, &rq, &rph);
     if constexpr (kTma) tma |= 1u << stage;
     upar ^= 1u << stage;
     stage = stage + 1 == kStages ? 0 : stage + 1;
@@ -1019,10 +1002,6 @@ prologue_kernel(const __grid_constant__ ProParams p) {
       mbar_init(&sm.qfull[s], 1);
       mbar_init(&sm.qempty[s], 1);
     }
-    for (int s = 0; s < kRequests; ++s) {
-      mbar_init(&sm.rfull[s], 1);
-      mbar_init(&sm.rempty[s], 1);
-    }
     sm.abort = 0;
     mbar_fence_init();
   }
@@ -1049,24 +1028,25 @@ prologue_kernel(const __grid_constant__ ProParams p) {
     if (!mbar_sleep_wait(&sm.full[stage], phase, &sm.abort, p.status, p.timeout_ns)) break;
     const Slot it = sm.slot[stage];
     if (it.kind == kEnd) break;
-    consume<kTma, kBf16, DP>(p, it, stage, sm);
+    if (it.kind != kGroupEnd) consume<kTma, kBf16, DP>(p, it, stage, sm);
     csync();                                    // every consumer is done with the stage
     if (threadIdx.x == 0) {
       mbar_arrive(&sm.empty[stage]);
       if (it.kind <= kStatsV) hand_over(p, sm, it.unit, &q, &qph);
+      else if (it.kind == kGroupEnd) hand_over(p, sm, kMarkGroup - it.unit, &q, &qph);
     }
     if (++stage == kStages) {
       stage = 0;
       phase ^= 1u;
     }
   }
-  if (threadIdx.x == 0) hand_over(p, sm, -1, &q, &qph);   // the helper may stop
+  if (threadIdx.x == 0) hand_over(p, sm, kMarkEnd, &q, &qph);   // the helper may stop
 }
 
 constexpr size_t kSmemBytes = sizeof(PSmem) + 1024;   // + alignment slack
 
-// Work list of a call: n_q = n_kv = 0 gives statistics only.
-bool make_plan(const SegGeo& g, bool with_quant, int64_t grid, Plan* out) {
+// Work of a call: n_q = n_kv = 0 gives statistics only.
+bool make_plan(const SegGeo& g, bool with_quant, Plan* out) {
   Plan P{};
   const int64_t maxk = g.varlen ? g.max_k : g.Lk;
   const int64_t maxq = g.varlen ? g.max_q : g.Lq;
@@ -1078,21 +1058,21 @@ bool make_plan(const SegGeo& g, bool with_quant, int64_t grid, Plan* out) {
   const int64_t n_kv = with_quant ? 2 * nkb : 0;
   const int64_t per = n_stats + n_q + n_kv;
   if (units * per >= (int64_t(1) << 31)) return false;
-  int64_t lag = units;                    // no K/V items: everything in the first phase
+  int64_t group = units;
   if (n_kv > 0) {
-    // eight items per CTA between a unit's stats and its K/V items (a CTA
-    // holds up to four: its stages and the one being set up), while the K
-    // and V of the units in between stay well inside L2
+    // a group's K and V are read in one phase and again (from L2) in the
+    // next, while the following group streams in: two groups must fit
     const int64_t unit_bytes = 4 * maxk * g.D;
-    lag = (8 * grid + per - 1) / per;
-    const int64_t l2_budget = 48ll << 20;
-    if (unit_bytes > 0 && lag * unit_bytes > l2_budget) lag = l2_budget / unit_bytes;
-    if (lag < 1) lag = 1;
-    if (lag > units) lag = units;
+    const int64_t l2_budget = 24ll << 20;
+    group = unit_bytes > 0 ? l2_budget / unit_bytes : units;
+    if (group < 1) group = 1;
+    if (group > units) group = units;
+    if ((units + group - 1) / group > kMaxGroups) group = (units + kMaxGroups - 1) / kMaxGroups;
   }
+  const int64_t groups = units > 0 ? (units + group - 1) / group : 0;
   P.units = static_cast<int32_t>(units);
-  P.lag = static_cast<int32_t>(lag);
-  P.total = static_cast<int32_t>(units * per);
+  P.group = static_cast<int32_t>(group);
+  P.groups = static_cast<int32_t>(groups);
   P.n_stats = static_cast<int32_t>(n_stats);
   P.n_q = static_cast<int32_t>(n_q);
   P.n_kv = static_cast<int32_t>(n_kv);
@@ -1149,11 +1129,15 @@ cudaError_t launch_t(ProParams& prm, bool with_quant, cudaStream_t st) {
   int sms = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  int64_t grid = static_cast<int64_t>(sms) * per_sm[dev];
-  if (!make_plan(prm.g, with_quant, grid, &prm.plan)) return cudaErrorInvalidValue;
-  if (grid > prm.plan.total) grid = prm.plan.total;
-  if (grid <= 0) return cudaSuccess;
-  prologue_kernel<kTma, kBf16, DP><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, st>>>(prm);
+  if (!make_plan(prm.g, with_quant, &prm.plan)) return cudaErrorInvalidValue;
+  if (prm.plan.groups <= 0) return cudaSuccess;
+  // every CTA is resident at once (the group barriers count them all): a
+  // cooperative launch of exactly the resident CTAs
+  const unsigned grid = static_cast<unsigned>(sms * per_sm[dev]);
+  void* args[] = {&prm};
+  e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(prologue_kernel<kTma, kBf16, DP>),
+                                  dim3(grid), dim3(kThreads), args, kSmemBytes, st);
+  if (e != cudaSuccess) return e;
   note_launch();
   return cudaGetLastError();
 }
@@ -1195,22 +1179,23 @@ cudaError_t launch_prologue(const SegGeo& g, const PrologueBuffers& b,
   prm.q16 = b.q16; prm.k16 = b.k16; prm.v8 = b.v8;
   prm.s_q = b.s_q; prm.s_k = b.s_k; prm.s_v = b.s_v;
   prm.k_mean = b.k_mean; prm.v_inv = b.v_inv;
-  prm.ksum = b.ksum; prm.vmax = b.vmax; prm.done = b.done; prm.ready = b.ready;
-  prm.next = b.next; prm.status = b.status; prm.timeout_ns = b.timeout_ns;
+  prm.ksum = b.ksum; prm.vmax = b.vmax; prm.done = b.done;
+  prm.cnt_a = b.sync; prm.cnt_b = b.sync + kMaxGroups; prm.gbar = b.sync + 2 * kMaxGroups;
+  prm.status = b.status; prm.timeout_ns = b.timeout_ns;
   prm.one = 1.0f;
   return launch_any(prm, vec, true, st);
 }
 
 // ------------------------------------------- statistics without allocation
 // Scratch of the allocation-free statistics entry point: a header (status
-// word, work counter, per-unit done counters and ready flags), then
+// word, per-unit done counters, list counters and group-barrier counters), then
 // per-channel K sums (8 B), V maxima (4 B) and V multipliers (4 B) for at
 // most kStaticStatEntries (segment, kv head, channel) triples.  It lives in
 // the module image, so every device that loads this library holds it until
 // the process exits; concurrent calls share it.
 namespace {
 constexpr int64_t kMaxStaticUnits = kStaticStatEntries / 64;
-constexpr size_t kStaticHeader = 256 + 2 * 4 * kMaxStaticUnits;
+constexpr size_t kStaticHeader = 256 + 4 * kMaxStaticUnits + 12 * kMaxGroups;
 __device__ __align__(256) unsigned char g_stats_scratch[
     kStaticHeader + kStaticStatEntries * (8 + 4 + 4)];
 
@@ -1249,9 +1234,10 @@ cudaError_t launch_kv_stats_static(const SegGeo& g, const uint16_t* k,
   prm.k = k; prm.v = v;
   prm.k_mean = k_mean; prm.s_v = s_v;
   prm.status = reinterpret_cast<uint32_t*>(base);
-  prm.next = reinterpret_cast<unsigned int*>(base + 8);
   prm.done = reinterpret_cast<uint32_t*>(base + 256);
-  prm.ready = reinterpret_cast<uint32_t*>(base + 256 + 4 * kMaxStaticUnits);
+  prm.cnt_a = reinterpret_cast<unsigned int*>(base + 256 + 4 * kMaxStaticUnits);
+  prm.cnt_b = prm.cnt_a + kMaxGroups;
+  prm.gbar = prm.cnt_a + 2 * kMaxGroups;
   prm.ksum = base + kStaticHeader;
   prm.vmax = reinterpret_cast<uint32_t*>(base + kStaticHeader + kStaticStatEntries * 8);
   prm.v_inv = reinterpret_cast<float*>(base + kStaticHeader + kStaticStatEntries * 12);

@@ -33,9 +33,8 @@ struct PrologueBuffers {
   float* v_inv;
   void* ksum;        // int64 (fp16 inputs) or double (bf16), [nseg][Hkv][Dp]
   uint32_t* vmax;    // float bits, [nseg][Hkv][Dp]
-  uint32_t* done;    // stats items finished per (segment, kv head), zeroed
-  uint32_t* ready;   // per (segment, kv head): statistics final, zeroed
-  unsigned int* next;         // work-item counter, zeroed
+  uint32_t* done;    // stats tiles finished per (segment, kv head), zeroed
+  unsigned int* sync;         // 3 x 64 counters (A lists, B lists, group barriers), zeroed
   uint32_t* status;
   uint64_t timeout_ns;        // bound of every wait
 };
