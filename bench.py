@@ -231,16 +231,54 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int):
     h2d = sum(host[k].numel() * host[k].element_size() for k in ("q", "k", "v"))
     d2h = out_host.numel() * 4
 
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ops = workload_ops(w)
     Dp = 64 if w.D <= 64 else 128
-    return dict(total_ms=total_ms, step_ms=step_ms, pro_ms=pro_ms, att_ms=att_ms,
-                launches_per_step=launches_per_step, launches=launches,
-                e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, ops=ops, ops_padded=workload_ops(w, Dp),
-                clocks=clock_info)
+    r = dict(total_ms=total_ms, step_ms=step_ms, pro_ms=pro_ms, att_ms=att_ms,
+             launches_per_step=launches_per_step, launches=launches,
+             e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, ops=workload_ops(w),
+             ops_padded=workload_ops(w, Dp),
+             ops_effective=w.ops(causal_effective=True),
+             ops_padded_effective=w.ops(dim=Dp, causal_effective=True),
+             clocks=clock_info)
+    return reduce_over_ranks(r, world, dev)
+
+
+# ---------------------------------------------------------- rank aggregation
+TIME_KEYS = ("total_ms", "pro_ms", "att_ms", "e2e_ms")
+
+
+def reduce_over_ranks(r: dict, world: int, device=None) -> dict:
+    """Max over ranks of every time-like figure: the job's step ends when its
+    slowest rank's does.  Rank counts and op totals stay per rank (every rank
+    runs the same workload on its own GPU, replicas with no collective in the
+    data path).  Called by every rank; one all-reduce."""
+    if world <= 1:
+        return r
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(r[k]) for k in TIME_KEYS], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    out = dict(r)
+    out.update(zip(TIME_KEYS, t.tolist()))
+    return out
+
+
+def job_figures(r: dict, world: int, steps: int) -> dict:
+    """Whole-job throughputs in TOPS: the ops all `world` ranks processed
+    divided by the max-over-ranks time.  `value` counts 4*Lq*Lk*D literally;
+    the padded figures use the head dimension the tensor cores see, and the
+    effective ones drop the causally masked half."""
+    def tops(ops, ms):
+        return ops * world / (ms * 1e-3) / 1e12
+    step_ms = r["total_ms"] / steps
+    return {
+        "value": tops(r["ops"], step_ms),
+        "value_padded_d": tops(r["ops_padded"], step_ms),
+        "value_causal_effective": tops(r["ops_effective"], step_ms),
+        "e2e": tops(r["ops"], r["e2e_ms"]),
+        "attention_tflops_padded": r["ops_padded"] / (r["att_ms"] * 1e-3) / 1e12,
+        "attention_tflops_padded_effective":
+            r["ops_padded_effective"] / (r["att_ms"] * 1e-3) / 1e12,
+    }
 
 
 # ---------------------------------------------------------- CPU oracle arm
@@ -260,7 +298,10 @@ def oracle_sample(w: wl.Workload, inp: dict, rows: int, heads: int = 1):
     oracle.attn(pro, w.causal, wl.default_sm_scale(w), rows=(0, rows))
     dt = time.perf_counter() - t0
     if w.causal:
+        # the sample's unmasked work, restated in the metric's literal count
+        # (the workload's literal/effective ratio): a linear extrapolation
         pairs = sum(min(i + 1, lk) for i in range(rows))
+        pairs *= w.ops() / w.ops(causal_effective=True)
     else:
         pairs = rows * lk
     ops = 4.0 * qs.shape[0] * pairs * w.D
@@ -339,8 +380,11 @@ def main():
     bf16 = peaks["bf16_tflops"]
     mix_peak = bf16 * 4.0 / 3.0
     fp8_peak = bf16 * 2.0
-    att_tflops = r["ops_padded"] / (r["att_ms"] * 1e-3) / 1e12
-    tops = r["ops"] * world * args.steps / (r["total_ms"] * 1e-3) / 1e12
+    fig = job_figures(r, world, args.steps)
+    # the kernel's algorithmic work: padded head dimension, masked tiles of a
+    # causal problem not counted (the kernel skips them)
+    att_tflops = fig["attention_tflops_padded_effective"]
+    tops = fig["value"]
     pro_gbs = prologue_bytes(w) / (r["pro_ms"] * 1e-3) / 1e9
     inp = wl.make_inputs(w)
     cpu_ops, cpu_s, cores = oracle_sample(w, inp, args.cpu_rows)
@@ -358,10 +402,16 @@ def main():
                      "peak_note": f"4/3 x {src} bf16 burst {bf16} (QK^T at the 16-bit "
                                   "rate, PV at the FP8 rate)",
                      "fp8_peak": fp8_peak, "frac_of_fp8_peak": att_tflops / fp8_peak},
+        "ops_per_step": {"literal": r["ops"], "padded_d": r["ops_padded"],
+                         "causal_effective": r["ops_effective"],
+                         "padded_d_causal_effective": r["ops_padded_effective"]},
+        "value_padded_d": fig["value_padded_d"],
+        "value_causal_effective": fig["value_causal_effective"],
         "attention_ms": r["att_ms"], "attention_tops": att_tflops,
+        "attention_tops_literal": r["ops"] / (r["att_ms"] * 1e-3) / 1e12,
         "prologue_ms": r["pro_ms"], "prologue_gbs": pro_gbs,
         "prologue_hbm_frac": pro_gbs / peaks["hbm_gbs"],
-        "e2e": {"value": r["ops"] / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TOPS",
+        "e2e": {"value": fig["e2e"], "unit": "TOPS",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         "gpu_launches": r["launches"],
         "launches_per_step": r["launches_per_step"],
