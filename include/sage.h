@@ -180,8 +180,10 @@ SAGE_API sage_status sage_debug_e4m3(const float* in, uint8_t* out, int64_t n,
 SAGE_API void sage_debug_set_fault(int skip_kv_tile, uint64_t timeout_ns);
 
 /* Reads (synchronising `stream`) the device status word of workspace ws:
- * SAGE_OK, SAGE_ERR_DEVICE_TIMEOUT or SAGE_ERR_INVALID_ARG.  The prologue
- * clears it; the kernels only set bits. */
+ * SAGE_OK, SAGE_ERR_DEVICE_TIMEOUT, SAGE_ERR_INVALID_ARG, or
+ * SAGE_ERR_UNSUPPORTED for an internal inconsistency the prologue caught
+ * (a work item outside the call's plan, skipped).  The prologue clears it;
+ * the kernels only set bits. */
 SAGE_API sage_status sage_device_status(const void* ws, sage_stream_t stream);
 
 /* Allocation-free smoothing statistics (the pages have no counterpart: an

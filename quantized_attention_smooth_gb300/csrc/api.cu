@@ -63,7 +63,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Byte offsets of every workspace buffer.
 struct WsLayout {
-  size_t status, ksum, vmax, done, sync, zero_end, k_mean, s_v, v_inv, s_q, s_k, q16, k16,
+  size_t status, ksum, vmax, sync, zero_end, k_mean, s_v, v_inv, s_q, s_k, q16, k16,
       v8, total;
 };
 
@@ -77,8 +77,7 @@ WsLayout ws_layout(const SegGeo& g) {
   w.status = o; o += 256;
   w.ksum = o; o = align256(o + nstat * 8);
   w.vmax = o; o = align256(o + nstat * 4);
-  w.done = o; o = align256(o + g.nseg * g.Hkv * 4);
-  w.sync = o; o = align256(o + 3 * 64 * 4);
+  w.sync = o; o = align256(o + 4 * 64 * 4);
   // means and scales start at zero: a segment without keys keeps them so
   w.k_mean = o; o = align256(o + nstat * 4);
   w.s_v = o; o = align256(o + nstat * 4);
@@ -289,7 +288,6 @@ sage_status run_prologue(const SegGeo& g, const void* q, const void* k, const vo
   b.v_inv = reinterpret_cast<float*>(wsb + w.v_inv);
   b.ksum = wsb + w.ksum;
   b.vmax = reinterpret_cast<uint32_t*>(wsb + w.vmax);
-  b.done = reinterpret_cast<uint32_t*>(wsb + w.done);
   b.sync = reinterpret_cast<unsigned int*>(wsb + w.sync);
   b.timeout_ns = wait_timeout_ns();
   b.status = reinterpret_cast<uint32_t*>(wsb + w.status);
@@ -536,6 +534,9 @@ sage_status sage_device_status(const void* ws, sage_stream_t stream) {
     return fail(SAGE_ERR_DEVICE_TIMEOUT, "a device-side wait ran out (status 0x%x)", word);
   if (word & kStatusBadSeqlens)
     return fail(SAGE_ERR_INVALID_ARG, "cu_seqlens inconsistent with totals/maxima");
+  if (word & kStatusBadItem)
+    return fail(SAGE_ERR_UNSUPPORTED, "internal error: a prologue work item fell outside "
+                "the call's plan and was skipped");
   return ok();
 }
 

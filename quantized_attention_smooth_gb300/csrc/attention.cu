@@ -81,11 +81,6 @@ struct Layout {
   static constexpr int kAlloc = kBytes + 1024;
 };
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  const uint32_t a = smem_u32(p);
-  return p + ((1024u - (a & 1023u)) & 1023u);
-}
-
 // S (128x128 fp32 in TMEM) = Q tile . K tile^T, K dimension DP in steps of 16.
 // q_lo / k_lo: low descriptor words of the 1024-byte aligned operand tiles.
 template <int DP>

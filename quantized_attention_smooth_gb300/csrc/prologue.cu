@@ -20,23 +20,27 @@
 //             codes (stored as exact fp16 integers, the tensor-core operand),
 //             one scale per token;
 //   K         128 keys: smoothed K (k - mean, fp32) -> int8 codes, one scale
-//             per block (the unit's K mean is copied next to the tile);
-//   V         128 values: e4m3 per channel (multipliers next to the tile),
-//             transposed to channel-major.
-// The units are cut into groups whose K and V fit comfortably in L2, and
-// each group has two lists: A (its stats and Q tiles) and B (its K and V
-// tiles, which need the group's statistics).  A items never wait; a CTA that
-// has taken the last A item of group g arrives at the group's barrier (a
-// counter) once its stats tiles of the group are counted, and B items of the
-// group are taken only after every CTA has arrived, so they find their
-// statistics final and their K and V, read by the A list with an evict-last
-// hint, still in L2.  The A list runs at most one group ahead of the B list.
-// Consumers hand each finished stats tile to the helper warp, which counts it
-// for its unit; the count that completes a unit finalizes it (K mean, V
-// scale and reciprocal multiplier).  Nothing waits inside a list, and every
-// wait is bounded (timeout -> status bit).  Every 128-token tile of the
-// workspace is written in full (zeros past the sequence end and past D), so
-// the attention kernel never reads stale bytes.
+//             per block (the unit's K sums are copied next to the tile and
+//             turned into the mean there);
+//   V         128 values: e4m3 per channel (the unit's maxima are copied
+//             next to the tile and turned into multipliers there),
+//             transposed to channel-major;
+//   final     (statistics-only calls) the unit's K mean and V scales.
+// The units are cut into groups of about 12 MB of K and V, and each group
+// has two lists: A (its stats tiles) and B (its K and V tiles, or its final
+// items, which need the group's statistics).  A items never wait.  Once a
+// CTA's consumers are done with every A item of group g it has taken, its
+// helper warp arrives at the group's barrier (a counter, one release per
+// CTA and group); B items of the group are taken only after every CTA has
+// arrived, so they find the group's sums complete and their K and V, read
+// by the A list with an evict-last hint, still in L2.  The A list runs a
+// few groups ahead of the B list (about 48 MB of K and V held in L2), which
+// hides the barriers.  The Q tiles depend on nothing: they form one more
+// list, taken only when neither of the others has an item ready, so they
+// fill the barrier waits and the end.  Nothing waits inside a list, and
+// every wait is bounded (timeout -> status bit).  Every 128-token
+// tile of the workspace is written in full (zeros past the sequence end and
+// past D), so the attention kernel never reads stale bytes.
 //
 // Without 16-byte aligned rows (D % 8 != 0 or unaligned tensors) the same
 // kernel runs with element-wise global loads instead of tensor copies.
@@ -63,6 +67,8 @@ constexpr int kThreads = kConsumers + 64;
 constexpr int kStages = 3;
 constexpr int kQueue = 8;                    // finished stats tiles awaiting the helper
 constexpr int kMaxGroups = 64;               // counters per list in the workspace
+constexpr int64_t kGroupBytes = 12ll << 20;  // K and V bytes of a group (target)
+constexpr int64_t kL2Hold = 48ll << 20;      // K and V bytes held in L2 between reads
 constexpr int kTileBytes = 128 * 128 * 2;    // 128 rows of up to 128 16-bit values
 constexpr uint32_t kSleepNs = 20000;         // suspend hint of barrier waits
 // fp32 2^23 + 2^22 + 0x6600: adding it rounds to an integer n (ties to even)
@@ -70,24 +76,28 @@ constexpr uint32_t kSleepNs = 20000;         // suspend hint of barrier waits
 constexpr float kCodeMagic = 12609024.0f;
 constexpr float kRintMagic = 12582912.0f;    // 1.5 * 2^23
 
-enum ItemKind { kStatsK = 0, kStatsV = 1, kQ = 2, kK = 3, kV = 4, kEnd = 5, kGroupEnd = 6 };
+enum ItemKind {
+  kStatsK = 0, kStatsV = 1, kQ = 2, kK = 3, kV = 4, kEnd = 5, kGroupEnd = 6, kFinal = 7
+};
 
 // Work of one call (host-computed; every count fits in 31 bits).  The units
-// are cut into groups whose K and V fit comfortably in L2.  Each group has
-// two item lists with their own counters: A (stats and Q tiles, no
-// dependencies) and B (K and V tiles, which need the group's statistics).
-// A CTA that has taken its last A item of group g says so at group g's
-// barrier; once every CTA has (and has counted its stats tiles), the
-// group's statistics are final and its B items may be taken.  A items never
-// wait, and may run one group ahead of the B items, which bounds the K and V
-// held in L2 between their two reads.
+// are cut into groups.  Each group has two item lists with their own
+// counters: A (stats tiles, no dependencies) and B (K and V tiles, or one
+// final item per unit in a statistics-only call; they need the group's
+// sums).  A CTA whose consumers are done with its last A item of group g
+// says so at group g's barrier; once every CTA has, the group's sums are
+// complete and its B items may be taken.  A items never wait, and may run
+// `lead` groups ahead of the B items, which bounds the K and V held in L2
+// between their two reads.  Q tiles form a single list of their own.
 struct Plan {
   int32_t units;      // nseg * Hkv
   int32_t group;      // units per group
   int32_t groups;
+  int32_t lead;       // groups the A list may run ahead of the B list
   int32_t n_stats;    // stats items per unit (K and V tiles alternate)
   int32_t n_q;        // Q items per unit (query heads of the kv head x tiles)
   int32_t n_kv;       // K and V items per unit (K and V tiles alternate)
+  int32_t n_b;        // B items per unit: n_kv, or 1 (final) without quantisation
   int32_t nqt;        // 128-token tiles per query head
 };
 
@@ -107,10 +117,10 @@ struct ProParams {
   float* v_inv;
   void* ksum;                 // int64 (fp16) or double (bf16) per (unit, channel)
   uint32_t* vmax;             // float bits per (unit, channel)
-  uint32_t* done;             // stats tiles finished per unit
   unsigned int* cnt_a;        // [kMaxGroups] A-list counters
   unsigned int* cnt_b;        // [kMaxGroups] B-list counters
   unsigned int* gbar;         // [kMaxGroups] CTAs done with the group's A list
+  unsigned int* cnt_q;        // Q-list counter
   uint32_t* status;
   uint64_t timeout_ns;
   int32_t q_hnd, k_hnd;       // 1: tiles are (head, token) planes; 0: token-major
@@ -124,12 +134,14 @@ struct Slot {
 
 struct alignas(1024) PSmem {
   unsigned char tile[kStages][kTileBytes];
-  float aux[kStages][128];    // K items: the unit's K mean; V items: its V multipliers
+  alignas(16) unsigned char aux[kStages][1024];   // K items: the unit's K sums; V: its maxima
+  float coef[128];            // the current item's K mean or V multipliers
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t qfull[kQueue];
   uint64_t qempty[kQueue];
-  int32_t queue[kQueue];
+  int32_t queue[kQueue];      // unit of a finished stats tile, or a marker
+  int32_t qinfo[kQueue];      // stats tile: 2 * stage + (1 for V)
   Slot slot[kStages];
   float red[8];
   int abort;
@@ -139,28 +151,32 @@ __device__ __forceinline__ int group_units(const Plan& P, int g) {
   return min(P.units - g * P.group, P.group);
 }
 
-// Item i of group g's A list (stats tiles of each unit, then its Q tiles).
+// Item i of group g's A list (the stats tiles of each unit, K and V tiles
+// alternating).
 __device__ __forceinline__ void decode_a(const Plan& P, int g, int i, int* kind, int* unit,
                                          int* sub) {
-  const int a = P.n_stats + P.n_q;
-  const int u = i / a, off = i - u * a;
+  const int u = i / P.n_stats, off = i - u * P.n_stats;
   *unit = g * P.group + u;
-  if (off < P.n_stats) {
-    *kind = (off & 1) ? kStatsV : kStatsK;
-    *sub = off >> 1;
-  } else {
-    *kind = kQ;
-    *sub = off - P.n_stats;
-  }
+  *kind = (off & 1) ? kStatsV : kStatsK;
+  *sub = off >> 1;
 }
 
-// Item i of group g's B list (K and V tiles alternate).
+// Item i of the Q list (the Q tiles of each unit in turn).
+__device__ __forceinline__ void decode_q(const Plan& P, int i, int* kind, int* unit, int* sub) {
+  const int u = i / P.n_q;
+  *unit = u;
+  *kind = kQ;
+  *sub = i - u * P.n_q;
+}
+
+// Item i of group g's B list (K and V tiles alternate; without quantisation
+// one final item per unit).
 __device__ __forceinline__ void decode_b(const Plan& P, int g, int i, int* kind, int* unit,
                                          int* sub) {
-  const int u = i / P.n_kv, off = i - u * P.n_kv;
+  const int u = i / P.n_b, off = i - u * P.n_b;
   *unit = g * P.group + u;
-  *kind = (off & 1) ? kV : kK;
-  *sub = off >> 1;
+  *kind = P.n_kv == 0 ? kFinal : (off & 1) ? kV : kK;
+  *sub = P.n_kv == 0 ? 0 : off >> 1;
 }
 
 // ------------------------------------------------------------ memory ops
@@ -349,8 +365,7 @@ struct TileRows {
 
 // ------------------------------------------------------------- stats K
 template <bool kBf16, int DP, class Rows>
-__device__ __forceinline__ void stats_k(const ProParams& p, int unit, int nvalid,
-                                        const Rows& rows, unsigned char* scratch) {
+__device__ __forceinline__ void stats_k(int nvalid, const Rows& rows, unsigned char* scratch) {
   constexpr int G = DP / 8, R = kConsumers / G, P = kBlockN / R;   // P 8 or 4 rows
   const int lc = threadIdx.x % G, r = threadIdx.x / G, c0 = lc * 8;
   const bool full = nvalid == kBlockN;
@@ -409,9 +424,9 @@ __device__ __forceinline__ void stats_k(const ProParams& p, int unit, int nvalid
                         __float2int_rn(ls[j].y * 16777216.0f);
     }
   }
-  // lanes holding the same channels (warp shuffles), then the eight warps
-  // through shared memory (the stage, once every row has been read), one
-  // atomic per channel (per-warp atomics contend on the same addresses)
+  // lanes holding the same channels (warp shuffles), then one row per warp
+  // in shared memory (the stage, once every row has been read); the helper
+  // warp adds the eight rows and the result to the unit's sums
 #pragma unroll
   for (int o = G; o < 32; o <<= 1) {
 #pragma unroll
@@ -425,34 +440,19 @@ __device__ __forceinline__ void stats_k(const ProParams& p, int unit, int nvalid
     }
   }
   long long (*tab)[DP] = reinterpret_cast<long long (*)[DP]>(scratch);
-  csync();
+  csync();                                     // every row read: the stage is free
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   if (lane < G) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) tab[wid][c0 + j] = part[j];
   }
-  csync();
-  if (threadIdx.x < p.g.D) {
-    const int c = threadIdx.x;
-    if constexpr (kBf16) {
-      double sd = 0.0;
-#pragma unroll
-      for (int w = 0; w < kConsumers / 32; ++w) sd += __longlong_as_double(tab[w][c]);
-      atomicAdd(static_cast<double*>(p.ksum) + static_cast<int64_t>(unit) * DP + c, sd);
-    } else {
-      long long si = 0;
-#pragma unroll
-      for (int w = 0; w < kConsumers / 32; ++w) si += tab[w][c];
-      atomicAdd(static_cast<unsigned long long*>(p.ksum) + static_cast<int64_t>(unit) * DP + c,
-                static_cast<unsigned long long>(si));
-    }
-  }
 }
 
 // ------------------------------------------------------------- stats V
+// Per-channel max |v| of the tile, one row of packed pairs per warp in the
+// stage; the helper warp takes the maximum over the rows.
 template <bool kBf16, int DP, class Rows>
-__device__ __forceinline__ void stats_v(const ProParams& p, int unit, int nvalid,
-                                        const Rows& rows, unsigned char* scratch) {
+__device__ __forceinline__ void stats_v(int nvalid, const Rows& rows, unsigned char* scratch) {
   constexpr int G = DP / 8, R = kConsumers / G, P = kBlockN / R;
   const int lc = threadIdx.x % G, r = threadIdx.x / G, c0 = lc * 8;
   const bool full = nvalid == kBlockN;
@@ -471,20 +471,11 @@ __device__ __forceinline__ void stats_v(const ProParams& p, int unit, int nvalid
     for (int j = 0; j < 4; ++j) vm[j] = __vmaxu2(vm[j], __shfl_xor_sync(0xFFFFFFFFu, vm[j], o));
   }
   uint32_t (*tab)[DP / 2] = reinterpret_cast<uint32_t (*)[DP / 2]>(scratch);
-  csync();
+  csync();                                     // every row read: the stage is free
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   if (lane < G) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) tab[wid][c0 / 2 + j] = vm[j];
-  }
-  csync();
-  if (threadIdx.x < p.g.D) {
-    const int c = threadIdx.x;
-    uint32_t m = 0u;
-#pragma unroll
-    for (int w = 0; w < kConsumers / 32; ++w) m = __vmaxu2(m, tab[w][c >> 1]);
-    m = (c & 1) ? (m >> 16) : (m & 0xFFFFu);
-    atomicMax(p.vmax + static_cast<int64_t>(unit) * DP + c, __float_as_uint(mag_f32<kBf16>(m)));
   }
 }
 
@@ -634,6 +625,28 @@ __device__ __forceinline__ void v_tile(const ProParams& p, int nvalid, const Til
   }
 }
 
+// ---------------------------------------------------------- statistics
+// A unit's K mean of one channel from its exact sum (fp16: int64 fixed point
+// at 2^-24; bf16: fp64): the fp64 quotient by the key count, rounded to fp32.
+template <bool kBf16>
+__device__ __forceinline__ float k_mean_of(long long raw, int64_t len) {
+  if (len <= 0) return 0.0f;
+  double S;
+  if constexpr (kBf16) S = __longlong_as_double(raw);
+  else S = __ll2double_rn(raw) * 5.9604644775390625e-08;   // 2^-24, exact
+  return __double2float_rn(__ddiv_rn(S, static_cast<double>(len)));
+}
+
+// Per-channel V scale amax / 448 and multiplier 448 / amax (0 for a zero
+// channel) from the unit's maximum (float bits).
+__device__ __forceinline__ float v_scale_of(uint32_t m) {
+  return __fdiv_rn(__uint_as_float(m), 448.0f);
+}
+__device__ __forceinline__ float v_mul_of(uint32_t m) {
+  const float a = __uint_as_float(m);
+  return a > 0.0f ? __fdiv_rn(448.0f, a) : 0.0f;
+}
+
 // ------------------------------------------------------------- consumers
 template <bool kTma, bool kBf16, int DP>
 __device__ __forceinline__ void consume(const ProParams& p, const Slot& it, int stage,
@@ -661,7 +674,7 @@ __device__ __forceinline__ void consume(const ProParams& p, const Slot& it, int 
     q_tile<kBf16, DP>(p, it.nvalid, rows, p.q16 + (row0 + r) * DP + c0, p.s_q + row0);
     return;
   }
-  key_range(g, s, &start, &len);
+  const bool seg_ok = key_range(g, s, &start, &len);
   const int64_t t0 = static_cast<int64_t>(it.sub) * kBlockN;
   if constexpr (!kTma) {
     const uint16_t* src = (it.kind == kStatsK || it.kind == kK) ? p.k : p.v;
@@ -670,98 +683,111 @@ __device__ __forceinline__ void consume(const ProParams& p, const Slot& it, int 
     rows.tok_stride = g.k_tok_stride;
   }
   if (it.kind == kStatsK) {
-    stats_k<kBf16, DP>(p, it.unit, it.nvalid, rows, sm.tile[stage]);
+    stats_k<kBf16, DP>(it.nvalid, rows, sm.tile[stage]);
   } else if (it.kind == kStatsV) {
-    stats_v<kBf16, DP>(p, it.unit, it.nvalid, rows, sm.tile[stage]);
+    stats_v<kBf16, DP>(it.nvalid, rows, sm.tile[stage]);
   } else if (it.kind == kK) {
+    // the unit's K mean from its sums (copied next to the tile); the item of
+    // the first block also stores it
+    if (threadIdx.x < DP) {
+      const int c = threadIdx.x;
+      const float m = k_mean_of<kBf16>(reinterpret_cast<const long long*>(sm.aux[stage])[c], len);
+      sm.coef[c] = m;
+      if (it.sub == 0) p.k_mean[static_cast<int64_t>(it.unit) * DP + c] = m;
+    }
+    csync();
     const int64_t row0 = ws_seg_base(g.varlen, s, start, g.Hkv, g.k_head_rows) +
                          h * g.k_head_rows + t0;
-    k_tile<kBf16, DP>(p, it.nvalid, rows, sm.aux[stage], p.k16 + (row0 + r) * DP + c0,
+    k_tile<kBf16, DP>(p, it.nvalid, rows, sm.coef, p.k16 + (row0 + r) * DP + c0,
                       p.s_k + row0 / kBlockN, sm.red);
-  } else {
+  } else if (it.kind == kV) {
+    // the unit's V multipliers from its maxima; the first block's item also
+    // stores the scales
+    if (threadIdx.x < DP) {
+      const int c = threadIdx.x;
+      const uint32_t mx = reinterpret_cast<const uint32_t*>(sm.aux[stage])[c];
+      const float mul = v_mul_of(mx);
+      sm.coef[c] = mul;
+      if (it.sub == 0) {
+        p.s_v[static_cast<int64_t>(it.unit) * DP + c] = v_scale_of(mx);
+        p.v_inv[static_cast<int64_t>(it.unit) * DP + c] = mul;
+      }
+    }
+    csync();
     const int64_t vrow0 = (g.varlen ? 0 : s * g.Hkv * DP) + h * DP;
     const int64_t vcol0 = (g.varlen ? ws_seg_base(1, s, start, 0, 0) : 0) + t0;
-    v_tile<kTma, kBf16, DP>(p, it.nvalid, rows, sm.aux[stage], p.v8 + vrow0 * g.v_cols + vcol0,
+    v_tile<kTma, kBf16, DP>(p, it.nvalid, rows, sm.coef, p.v8 + vrow0 * g.v_cols + vcol0,
                             reinterpret_cast<uint32_t*>(sm.tile[stage]));
+  } else {
+    // final item (statistics only): the unit's K mean and V scales, read from
+    // L2 (the group's barrier, acquired by the producer, orders them)
+    if (threadIdx.x < DP) {
+      const int64_t i = static_cast<int64_t>(it.unit) * DP + threadIdx.x;
+      p.k_mean[i] = k_mean_of<kBf16>(__ldcg(static_cast<const long long*>(p.ksum) + i),
+                                     seg_ok ? len : 0);
+      const uint32_t mx = __ldcg(p.vmax + i);
+      p.s_v[i] = v_scale_of(mx);
+      p.v_inv[i] = v_mul_of(mx);
+    }
   }
 }
 
-// ---------------------------------------------------------- statistics
-// Turns a unit's sums into its K mean and V scales (one warp).  The caller
-// has acquired the unit's counter (or the unit has no keys), so every
-// accumulator update is visible.
-template <bool kBf16, int DP>
-__device__ __forceinline__ void finalize_unit(const ProParams& p, int unit, int64_t len) {
-  constexpr int C = DP / 32;                   // channels per lane
-  const int lane = threadIdx.x & 31;
-  const int64_t base = static_cast<int64_t>(unit) * DP + lane;
-  long long sum[C];
-  uint32_t vm[C];
-#pragma unroll
-  for (int j = 0; j < C; ++j) {                // every load in flight at once
-    sum[j] = __ldcg(static_cast<const long long*>(p.ksum) + base + 32 * j);
-    vm[j] = __ldcg(p.vmax + base + 32 * j);
-  }
-#pragma unroll
-  for (int j = 0; j < C; ++j) {
-    double S;
-    if constexpr (kBf16) S = __longlong_as_double(sum[j]);
-    else S = __ll2double_rn(sum[j]) * 5.9604644775390625e-08;   // 2^-24, exact
-    p.k_mean[base + 32 * j] =
-        len > 0 ? __double2float_rn(__ddiv_rn(S, static_cast<double>(len))) : 0.0f;
-    const float a = __uint_as_float(vm[j]);
-    p.s_v[base + 32 * j] = __fdiv_rn(a, 448.0f);
-    p.v_inv[base + 32 * j] = a > 0.0f ? __fdiv_rn(448.0f, a) : 0.0f;
-  }
-}
-
-// Target of a unit's done counter: its K and V stats tiles.
-__device__ __forceinline__ uint32_t stats_target(const SegGeo& g, int unit, int64_t* len) {
-  int64_t start;
-  if (!key_range(g, unit / g.Hkv, &start, len)) *len = 0;
-  return static_cast<uint32_t>(2 * ((*len + kBlockN - 1) / kBlockN));
-}
-
-// Counts a finished stats tile (handed over by the consumers, whose
-// accumulator updates precede the hand-over) for its unit; the add that
-// completes the count finalizes the unit, whose other tiles' updates its
-// acquire side makes visible.  Called by a whole warp.
-template <bool kBf16, int DP>
-__device__ __forceinline__ void count_tile(const ProParams& p, int unit) {
-  const int lane = threadIdx.x & 31;
-  int64_t len;
-  const uint32_t target = stats_target(p.g, unit, &len);
-  uint32_t last = 0;
-  if (lane == 0) {
-    uint32_t prev;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
-                 : "=r"(prev) : "l"(p.done + unit) : "memory");
-    last = prev + 1 == target;
-  }
-  last = __shfl_sync(0xFFFFFFFFu, last, 0);
-  if (last) {
-    __syncwarp();
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");   // acquire for lanes 1..31
-    finalize_unit<kBf16, DP>(p, unit, len);
-  }
-}
-
-// Markers the consumers hand to the helper besides finished stats tiles:
-// the end, and the end of group g's A list (kMarkGroup - g).
+// Markers the consumers hand to the helper: the end, and the end of group
+// g's A list (kMarkGroup - g).
 constexpr int kMarkEnd = -1;
 constexpr int kMarkGroup = -2;
 
-// Group g's barrier (helper lane 0): this CTA has taken its last A item of
-// the group and counted every stats tile of it; the release makes the units
-// it finalized visible to whoever acquires the barrier count.
+// Group g's barrier (helper lane 0): this CTA's consumers are done with
+// every A item of the group it took.  Their sums and maxima (relaxed
+// reductions, ordered before the hand-over by the consumers' barrier and
+// the queue's mbarrier) are released with the count.
 __device__ __forceinline__ void group_arrive(const ProParams& p, int g) {
   asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(p.gbar + g) : "memory");
 }
 
-// The helper warp takes what the consumers hand over, in order: a finished
-// stats tile is counted for its unit (count_tile); a group marker means the
-// CTA is done with the group's A list (every stats tile of it counted), so
-// the helper arrives at the group's barrier.  It never waits for other CTAs.
+// A finished stats tile's per-warp rows (in its stage) -> the unit's K sums
+// or V maxima (relaxed reductions, one per channel and lane).
+template <bool kBf16, int DP>
+__device__ __forceinline__ void flush_stats(const ProParams& p, int unit, bool is_v,
+                                            const unsigned char* scratch) {
+  const int lane = threadIdx.x & 31;
+  const int64_t base = static_cast<int64_t>(unit) * DP;
+#pragma unroll
+  for (int i = 0; i < DP / 32; ++i) {
+    const int c = lane + 32 * i;
+    if (c >= p.g.D) break;
+    if (is_v) {
+      const uint32_t (*tab)[DP / 2] = reinterpret_cast<const uint32_t (*)[DP / 2]>(scratch);
+      uint32_t m = 0u;
+#pragma unroll
+      for (int w = 0; w < kConsumers / 32; ++w) m = __vmaxu2(m, tab[w][c >> 1]);
+      m = (c & 1) ? (m >> 16) : (m & 0xFFFFu);
+      atomicMax(p.vmax + base + c, __float_as_uint(mag_f32<kBf16>(m)));
+    } else {
+      const long long (*tab)[DP] = reinterpret_cast<const long long (*)[DP]>(scratch);
+      if constexpr (kBf16) {
+        double sd = 0.0;
+#pragma unroll
+        for (int w = 0; w < kConsumers / 32; ++w) sd += __longlong_as_double(tab[w][c]);
+        atomicAdd(static_cast<double*>(p.ksum) + base + c, sd);
+      } else {
+        long long si = 0;
+#pragma unroll
+        for (int w = 0; w < kConsumers / 32; ++w) si += tab[w][c];
+        atomicAdd(static_cast<unsigned long long*>(p.ksum) + base + c,
+                  static_cast<unsigned long long>(si));
+      }
+    }
+  }
+}
+
+// The helper warp takes what the consumers hand over, in order.  A finished
+// stats tile: it adds the tile's rows to the unit's sums and maxima, then
+// releases the tile's stage.  A group marker: the CTA is done with the
+// group's A list, so every lane fences its own reductions (each lane orders
+// what it issued itself) and lane 0 arrives at the group's barrier.  The
+// fences wait for outstanding writes, which is why they run here and not on
+// a consumer thread.  The helper never waits for other CTAs.
 template <bool kBf16, int DP>
 __device__ __forceinline__ void helper(const ProParams& p, PSmem& sm) {
   const int lane = threadIdx.x & 31;
@@ -770,6 +796,7 @@ __device__ __forceinline__ void helper(const ProParams& p, PSmem& sm) {
   while (true) {
     if (!mbar_sleep_wait(&sm.qfull[q], qph, &sm.abort, p.status, p.timeout_ns)) return;
     const int unit = sm.queue[q];
+    const int info = sm.qinfo[q];
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.qempty[q]);
     if (++q == kQueue) {
@@ -778,20 +805,26 @@ __device__ __forceinline__ void helper(const ProParams& p, PSmem& sm) {
     }
     if (unit == kMarkEnd) return;
     if (unit <= kMarkGroup) {
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
+      __syncwarp();
       if (lane == 0) group_arrive(p, kMarkGroup - unit);
       continue;
     }
-    count_tile<kBf16, DP>(p, unit);
+    const int stage = info >> 1;
+    flush_stats<kBf16, DP>(p, unit, (info & 1) != 0, sm.tile[stage]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[stage]);     // the stage may be refilled
   }
 }
 
 // Consumer thread 0 hands a finished stats tile (unit >= 0) or a marker to
 // the helper warp.
-__device__ __forceinline__ bool hand_over(const ProParams& p, PSmem& sm, int unit, int* q,
-                                          uint32_t* ph) {
+__device__ __forceinline__ bool hand_over(const ProParams& p, PSmem& sm, int unit, int info,
+                                          int* q, uint32_t* ph) {
   if (!mbar_sleep_wait(&sm.qempty[*q], *ph ^ 1u, &sm.abort, p.status, p.timeout_ns))
     return false;
   sm.queue[*q] = unit;
+  sm.qinfo[*q] = info;
   mbar_arrive(&sm.qfull[*q]);
   if (++*q == kQueue) {
     *q = 0;
@@ -815,13 +848,15 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
   bool b_open = false;     // group gb's statistics are final
   uint32_t poll = 0;       // group gb's barrier count, read on the previous turn
   bool polled = false;
-  int a_idx = 0, b_idx = 0;  // claims taken ahead (lane 0), valid when *_pend
-  bool a_pend = false, b_pend = false;
+  int a_idx = 0, b_idx = 0, q_idx = 0;  // claims taken ahead (lane 0), valid when *_pend
+  bool a_pend = false, b_pend = false, q_pend = false;
+  bool q_left = P.n_q > 0;   // the Q list may still have items
   const uint32_t grid = gridDim.x;
   uint64_t idle0 = 0;
   while (ok) {
     // ---- choose the next item: a B item if its group is final, else an A
-    // item (at most one group ahead of the B list), else poll and wait
+    // item (at most `lead` groups ahead of the B list), else a Q item, else
+    // poll and wait
     Slot it{-1, 0, 0, 0};
     bool marker = false;
     while (gb < P.groups) {
@@ -844,7 +879,7 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
       if (!b_pend && lane == 0) b_idx = static_cast<int>(atomicAdd(p.cnt_b + gb, 1u));
       const int idx = __shfl_sync(0xFFFFFFFFu, b_idx, 0);
       b_pend = false;
-      if (idx < group_units(P, gb) * P.n_kv) {
+      if (idx < group_units(P, gb) * P.n_b) {
         decode_b(P, gb, idx, &it.kind, &it.unit, &it.sub);
         // claim the group's next B item now; it is used on the next turn
         if (lane == 0) b_idx = static_cast<int>(atomicAdd(p.cnt_b + gb, 1u));
@@ -854,11 +889,11 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
       ++gb;
       b_open = false;
     }
-    if (it.kind < 0 && ga < P.groups && (P.n_kv == 0 || ga <= gb + 1)) {
+    if (it.kind < 0 && ga < P.groups && ga <= gb + P.lead) {
       if (!a_pend && lane == 0) a_idx = static_cast<int>(atomicAdd(p.cnt_a + ga, 1u));
       const int idx = __shfl_sync(0xFFFFFFFFu, a_idx, 0);
       a_pend = false;
-      if (idx < group_units(P, ga) * (P.n_stats + P.n_q)) {
+      if (idx < group_units(P, ga) * P.n_stats) {
         decode_a(P, ga, idx, &it.kind, &it.unit, &it.sub);
         // claim the group's next A item now (A items never wait, so holding
         // the claim cannot hold up a barrier)
@@ -871,8 +906,20 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
         ++ga;
       }
     }
+    if (it.kind < 0 && q_left) {
+      if (!q_pend && lane == 0) q_idx = static_cast<int>(atomicAdd(p.cnt_q, 1u));
+      const int idx = __shfl_sync(0xFFFFFFFFu, q_idx, 0);
+      q_pend = false;
+      if (idx < P.units * P.n_q) {
+        decode_q(P, idx, &it.kind, &it.unit, &it.sub);
+        if (lane == 0) q_idx = static_cast<int>(atomicAdd(p.cnt_q, 1u));
+        q_pend = true;
+      } else {
+        q_left = false;
+      }
+    }
     if (it.kind < 0) {
-      if (ga >= P.groups && (P.n_kv == 0 || gb >= P.groups)) {
+      if (ga >= P.groups && gb >= P.groups && !q_left) {
         it.kind = kEnd;
         marker = true;
       } else {
@@ -903,6 +950,14 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
       polled = true;
     }
 
+    // every decoded item must name a unit of the plan: anything else is an
+    // internal error, reported and skipped rather than followed
+    if (!marker && (it.unit < 0 || it.unit >= P.units)) {
+      if (lane == 0) atomicOr(p.status, kStatusBadItem);
+      continue;
+    }
+    // a final item loads nothing: it is passed on like a marker
+    if (it.kind == kFinal) marker = true;
     int64_t s = 0, h = 0, start = 0, len = 0, t0 = 0;
     if (!marker) {
       s = it.unit / g.Hkv;
@@ -920,12 +975,7 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
         if (lane == 0 && it.sub == 0) atomicOr(p.status, kStatusBadSeqlens);
         len = 0;
       }
-      if (t0 >= len) {
-        // nothing to load or quantise; an empty unit's statistics are final
-        // (all zero) at once
-        if (it.kind == kStatsK && it.sub == 0) finalize_unit<kBf16, DP>(p, it.unit, 0);
-        continue;
-      }
+      if (t0 >= len) continue;               // nothing to load or quantise
       it.nvalid = static_cast<int32_t>(len - t0 < kBlockN ? len - t0 : kBlockN);
     }
     // wait until the consumers have released this stage's previous item
@@ -946,7 +996,7 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
     }
     if (lane == 0) {
       const bool kv = it.kind == kK || it.kind == kV;
-      const uint32_t aux_bytes = kv ? DP * 4 : 0;
+      const uint32_t aux_bytes = it.kind == kK ? DP * 8 : it.kind == kV ? DP * 4 : 0;
       if constexpr (kTma) {
         const CUtensorMap* map = it.kind == kQ ? &p.mq
                                : (it.kind == kStatsK || it.kind == kK) ? &p.mk : &p.mv;
@@ -968,9 +1018,12 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
         mbar_expect_tx(&sm.full[stage], aux_bytes);
       }
       if (kv) {
-        // the unit's K mean or V multipliers, final since its group's barrier
-        const float* src =
-            (it.kind == kK ? p.k_mean : p.v_inv) + static_cast<int64_t>(it.unit) * DP;
+        // the unit's K sums or V maxima, complete since its group's barrier
+        const void* src =
+            it.kind == kK
+                ? static_cast<const void*>(static_cast<const long long*>(p.ksum) +
+                                           static_cast<int64_t>(it.unit) * DP)
+                : static_cast<const void*>(p.vmax + static_cast<int64_t>(it.unit) * DP);
         bulk_load(sm.aux[stage], src, aux_bytes, &sm.full[stage]);
       }
     }
@@ -990,9 +1043,8 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
 template <bool kTma, bool kBf16, int DP>
 __global__ void __launch_bounds__(kThreads, 2)
 prologue_kernel(const __grid_constant__ ProParams p) {
-  extern __shared__ unsigned char smem_raw[];
-  PSmem& sm = *reinterpret_cast<PSmem*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ uint8_t smem_raw[];
+  PSmem& sm = *reinterpret_cast<PSmem*>(align1024(smem_raw));
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
@@ -1031,16 +1083,21 @@ prologue_kernel(const __grid_constant__ ProParams p) {
     if (it.kind != kGroupEnd) consume<kTma, kBf16, DP>(p, it, stage, sm);
     csync();                                    // every consumer is done with the stage
     if (threadIdx.x == 0) {
-      mbar_arrive(&sm.empty[stage]);
-      if (it.kind <= kStatsV) hand_over(p, sm, it.unit, &q, &qph);
-      else if (it.kind == kGroupEnd) hand_over(p, sm, kMarkGroup - it.unit, &q, &qph);
+      if (it.kind <= kStatsV) {
+        // the helper adds the tile's rows to the unit's statistics and then
+        // releases the stage
+        hand_over(p, sm, it.unit, 2 * stage + (it.kind == kStatsV ? 1 : 0), &q, &qph);
+      } else {
+        mbar_arrive(&sm.empty[stage]);
+        if (it.kind == kGroupEnd) hand_over(p, sm, kMarkGroup - it.unit, 0, &q, &qph);
+      }
     }
     if (++stage == kStages) {
       stage = 0;
       phase ^= 1u;
     }
   }
-  if (threadIdx.x == 0) hand_over(p, sm, kMarkEnd, &q, &qph);   // the helper may stop
+  if (threadIdx.x == 0) hand_over(p, sm, kMarkEnd, 0, &q, &qph);   // the helper may stop
 }
 
 constexpr size_t kSmemBytes = sizeof(PSmem) + 1024;   // + alignment slack
@@ -1056,26 +1113,30 @@ bool make_plan(const SegGeo& g, bool with_quant, Plan* out) {
   const int64_t nqt = (maxq + kBlockM - 1) / kBlockM;
   const int64_t n_q = with_quant ? (g.Hq / g.Hkv) * nqt : 0;
   const int64_t n_kv = with_quant ? 2 * nkb : 0;
-  const int64_t per = n_stats + n_q + n_kv;
+  const int64_t per = n_stats + n_q + (n_kv > 0 ? n_kv : 1);
   if (units * per >= (int64_t(1) << 31)) return false;
-  int64_t group = units;
+  int64_t group = units, lead = 1;
   if (n_kv > 0) {
-    // a group's K and V are read in one phase and again (from L2) in the
-    // next, while the following group streams in: two groups must fit
+    // a group's K and V are read by its A list and again (from L2) by its B
+    // list, which runs up to `lead` groups behind: lead + 1 groups must fit
     const int64_t unit_bytes = 4 * maxk * g.D;
-    const int64_t l2_budget = 24ll << 20;
-    group = unit_bytes > 0 ? l2_budget / unit_bytes : units;
+    group = unit_bytes > 0 ? kGroupBytes / unit_bytes : units;
     if (group < 1) group = 1;
     if (group > units) group = units;
     if ((units + group - 1) / group > kMaxGroups) group = (units + kMaxGroups - 1) / kMaxGroups;
+    const int64_t gbytes = group * unit_bytes;
+    lead = gbytes > 0 ? kL2Hold / gbytes - 1 : 1;
+    if (lead < 1) lead = 1;
   }
   const int64_t groups = units > 0 ? (units + group - 1) / group : 0;
   P.units = static_cast<int32_t>(units);
   P.group = static_cast<int32_t>(group);
   P.groups = static_cast<int32_t>(groups);
+  P.lead = static_cast<int32_t>(lead < groups ? lead : (groups > 0 ? groups : 1));
   P.n_stats = static_cast<int32_t>(n_stats);
   P.n_q = static_cast<int32_t>(n_q);
   P.n_kv = static_cast<int32_t>(n_kv);
+  P.n_b = static_cast<int32_t>(n_kv > 0 ? n_kv : 1);
   P.nqt = static_cast<int32_t>(nqt);
   *out = P;
   return true;
@@ -1179,8 +1240,9 @@ cudaError_t launch_prologue(const SegGeo& g, const PrologueBuffers& b,
   prm.q16 = b.q16; prm.k16 = b.k16; prm.v8 = b.v8;
   prm.s_q = b.s_q; prm.s_k = b.s_k; prm.s_v = b.s_v;
   prm.k_mean = b.k_mean; prm.v_inv = b.v_inv;
-  prm.ksum = b.ksum; prm.vmax = b.vmax; prm.done = b.done;
+  prm.ksum = b.ksum; prm.vmax = b.vmax;
   prm.cnt_a = b.sync; prm.cnt_b = b.sync + kMaxGroups; prm.gbar = b.sync + 2 * kMaxGroups;
+  prm.cnt_q = b.sync + 3 * kMaxGroups;
   prm.status = b.status; prm.timeout_ns = b.timeout_ns;
   prm.one = 1.0f;
   return launch_any(prm, vec, true, st);
@@ -1188,14 +1250,13 @@ cudaError_t launch_prologue(const SegGeo& g, const PrologueBuffers& b,
 
 // ------------------------------------------- statistics without allocation
 // Scratch of the allocation-free statistics entry point: a header (status
-// word, per-unit done counters, list counters and group-barrier counters), then
+// word, list counters and group-barrier counters), then
 // per-channel K sums (8 B), V maxima (4 B) and V multipliers (4 B) for at
 // most kStaticStatEntries (segment, kv head, channel) triples.  It lives in
 // the module image, so every device that loads this library holds it until
 // the process exits; concurrent calls share it.
 namespace {
-constexpr int64_t kMaxStaticUnits = kStaticStatEntries / 64;
-constexpr size_t kStaticHeader = 256 + 4 * kMaxStaticUnits + 12 * kMaxGroups;
+constexpr size_t kStaticHeader = 256 + 16 * kMaxGroups;
 __device__ __align__(256) unsigned char g_stats_scratch[
     kStaticHeader + kStaticStatEntries * (8 + 4 + 4)];
 
@@ -1234,10 +1295,10 @@ cudaError_t launch_kv_stats_static(const SegGeo& g, const uint16_t* k,
   prm.k = k; prm.v = v;
   prm.k_mean = k_mean; prm.s_v = s_v;
   prm.status = reinterpret_cast<uint32_t*>(base);
-  prm.done = reinterpret_cast<uint32_t*>(base + 256);
-  prm.cnt_a = reinterpret_cast<unsigned int*>(base + 256 + 4 * kMaxStaticUnits);
+  prm.cnt_a = reinterpret_cast<unsigned int*>(base + 256);
   prm.cnt_b = prm.cnt_a + kMaxGroups;
   prm.gbar = prm.cnt_a + 2 * kMaxGroups;
+  prm.cnt_q = prm.cnt_a + 3 * kMaxGroups;
   prm.ksum = base + kStaticHeader;
   prm.vmax = reinterpret_cast<uint32_t*>(base + kStaticHeader + kStaticStatEntries * 8);
   prm.v_inv = reinterpret_cast<float*>(base + kStaticHeader + kStaticStatEntries * 12);

@@ -16,6 +16,7 @@ namespace sage {
 // Status bits of the workspace's device status word.
 constexpr uint32_t kStatusTimeout = 1u;      // a bounded wait ran out
 constexpr uint32_t kStatusBadSeqlens = 2u;   // cu_seqlens inconsistent
+constexpr uint32_t kStatusBadItem = 4u;      // a work item decoded outside the call's plan
 
 struct SegGeo {
   int64_t nseg, Hq, Hkv, Lq, Lk, D, Dp;

@@ -33,8 +33,7 @@ struct PrologueBuffers {
   float* v_inv;
   void* ksum;        // int64 (fp16 inputs) or double (bf16), [nseg][Hkv][Dp]
   uint32_t* vmax;    // float bits, [nseg][Hkv][Dp]
-  uint32_t* done;    // stats tiles finished per (segment, kv head), zeroed
-  unsigned int* sync;         // 3 x 64 counters (A lists, B lists, group barriers), zeroed
+  unsigned int* sync;         // 4 x 64 counters (A lists, B lists, group barriers, Q list), zeroed
   uint32_t* status;
   uint64_t timeout_ns;        // bound of every wait
 };
