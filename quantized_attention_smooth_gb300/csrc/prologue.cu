@@ -373,27 +373,9 @@ __device__ __forceinline__ void stats_k(int nvalid, const Rows& rows, unsigned c
   // into hi = rint(16 k) and lo = k - hi / 16 (a multiple of 2^-24, |lo| <=
   // 1/32); up to 16 of either sum exactly in fp32 (|sum hi| < 2^24, |sum lo|
   // * 2^24 <= 2^23).  The FP64 pipe (slow on GB300) stays out of the loop.
-  // bf16 keys: fp64 sums.
+  static_assert(!kBf16, "bf16 keys take stats_k_bf16");
   long long part[8];
-  if constexpr (kBf16) {
-    double ds[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) ds[j] = 0.0;
-#pragma unroll
-    for (int i = 0; i < P; ++i) {
-      if (full || r + R * i < nvalid) {
-        const uint4 u = rows.template get<R>(i);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 x = cvt2<true>(word(u, j));
-          ds[2 * j] += static_cast<double>(x.x);
-          ds[2 * j + 1] += static_cast<double>(x.y);
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) part[j] = __double_as_longlong(ds[j]);
-  } else {
+  {
     float2 hs[4], ls[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -430,14 +412,7 @@ __device__ __forceinline__ void stats_k(int nvalid, const Rows& rows, unsigned c
 #pragma unroll
   for (int o = G; o < 32; o <<= 1) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const long long other = __shfl_xor_sync(0xFFFFFFFFu, part[j], o);
-      if constexpr (kBf16)
-        part[j] = __double_as_longlong(__longlong_as_double(part[j]) +
-                                       __longlong_as_double(other));
-      else
-        part[j] += other;
-    }
+    for (int j = 0; j < 8; ++j) part[j] += __shfl_xor_sync(0xFFFFFFFFu, part[j], o);
   }
   long long (*tab)[DP] = reinterpret_cast<long long (*)[DP]>(scratch);
   csync();                                     // every row read: the stage is free
@@ -445,6 +420,110 @@ __device__ __forceinline__ void stats_k(int nvalid, const Rows& rows, unsigned c
   if (lane < G) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) tab[wid][c0 + j] = part[j];
+  }
+}
+
+// bf16 keys.  A bf16 value is (128 + m) 2^(E - 134) with E its exponent
+// field (m < 128), so when the nonzero values of a thread's rows of a
+// channel lie within 13 binades (E_max - E_min <= 13) and E_max <= 250,
+// every partial sum is a multiple of 2^(E_min - 134) below 2^(E_min - 110)
+// in magnitude: the fp32 sum of at most 8 of them is exact.  Otherwise
+// (rare: a value near zero next to large ones, subnormals, huge values) the
+// thread sums that channel in fp64 (exact for 8 values), adds it to the
+// unit's sum itself and fences the reduction.  The exact fp32 partials go
+// to the stage, one row per thread of a channel group; then one thread per
+// channel puts them on the integer grid 2^(g - 150), g = (largest exponent
+// field) - 34, where each is below 2^58 and their sum below 2^63, and adds
+// them exactly (a partial further below, subnormal or not finite goes to
+// the unit's sum in fp64 by itself, fenced).  The helper warp turns the
+// integer sums into fp64 reductions (flush_stats).
+template <int DP, class Rows>
+__device__ __forceinline__ void stats_k_bf16(const ProParams& p, int unit, int nvalid,
+                                             const Rows& rows, unsigned char* scratch) {
+  constexpr int G = DP / 8, R = kConsumers / G, P = kBlockN / R;
+  const int lc = threadIdx.x % G, r = threadIdx.x / G, c0 = lc * 8;
+  const bool full = nvalid == kBlockN;
+  float2 fs[4];
+  uint32_t emax[4], emin[4];       // packed exponent fields (max, min over nonzero)
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    fs[j] = make_float2(0.0f, 0.0f);
+    emax[j] = 0u;
+    emin[j] = 0x00FF00FFu;
+  }
+#pragma unroll
+  for (int i = 0; i < P; ++i) {
+    if (full || r + R * i < nvalid) {
+      const uint4 u = rows.template get<R>(i);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t w = word(u, j);
+        fs[j] = __fadd2_rn(fs[j], cvt2<true>(w));
+        const uint32_t e2 = (w >> 7) & 0x00FF00FFu;
+        const uint32_t zero = __vcmpeq2(w & 0x7FFF7FFFu, 0u);   // 0xFFFF in zero halves
+        emax[j] = __vmaxu2(emax[j], e2);
+        emin[j] = __vminu2(emin[j], e2 | (zero & 0x00FF00FFu));
+      }
+    }
+  }
+  float part[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t hi = h ? (emax[j] >> 16) : (emax[j] & 0xFFFFu);
+      const uint32_t lo = h ? (emin[j] >> 16) : (emin[j] & 0xFFFFu);
+      float v = h ? fs[j].y : fs[j].x;
+      if (hi > 250u || (lo <= hi && hi - lo > 13u)) {
+        double d = 0.0;
+        for (int i = 0; i < P; ++i) {
+          if (full || r + R * i < nvalid) {
+            const float2 x = cvt2<true>(word(rows.template get<R>(i), j));
+            d += static_cast<double>(h ? x.y : x.x);
+          }
+        }
+        atomicAdd(static_cast<double*>(p.ksum) + static_cast<int64_t>(unit) * DP + c0 + 2 * j + h,
+                  d);
+        __threadfence();
+        v = 0.0f;
+      }
+      part[2 * j + h] = v;
+    }
+  }
+  float (*tab)[DP] = reinterpret_cast<float (*)[DP]>(scratch);
+  csync();                                     // every row read: the stage is free
+  float4* dst = reinterpret_cast<float4*>(&tab[r][c0]);
+  dst[0] = make_float4(part[0], part[1], part[2], part[3]);
+  dst[1] = make_float4(part[4], part[5], part[6], part[7]);
+  csync();                                     // the table is complete
+  if (threadIdx.x < DP) {
+    const int c = threadIdx.x;
+    int emax = 0;
+#pragma unroll 8
+    for (int w = 0; w < R; ++w)
+      emax = max(emax, static_cast<int>((__float_as_uint(tab[w][c]) >> 23) & 0xFFu));
+    const int g = emax - 34;
+    long long acc = 0;
+    bool fenced = false;
+#pragma unroll 8
+    for (int w = 0; w < R; ++w) {
+      const uint32_t b = __float_as_uint(tab[w][c]);
+      const int e = static_cast<int>((b >> 23) & 0xFFu);
+      if ((b & 0x7FFFFFFFu) == 0u) continue;
+      if (e == 0 || e == 255 || e < g) {
+        atomicAdd(static_cast<double*>(p.ksum) + static_cast<int64_t>(unit) * DP + c,
+                  static_cast<double>(__uint_as_float(b)));
+        fenced = true;
+        continue;
+      }
+      const long long v = static_cast<long long>((b & 0x7FFFFFu) | 0x800000u) << (e - g);
+      acc += (b >> 31) ? -v : v;
+    }
+    if (fenced) __threadfence();
+    long long* accs = reinterpret_cast<long long*>(scratch + R * DP * 4);
+    int* gs = reinterpret_cast<int*>(scratch + R * DP * 4 + DP * 8);
+    accs[c] = acc;
+    gs[c] = g;
   }
 }
 
@@ -683,7 +762,8 @@ __device__ __forceinline__ void consume(const ProParams& p, const Slot& it, int 
     rows.tok_stride = g.k_tok_stride;
   }
   if (it.kind == kStatsK) {
-    stats_k<kBf16, DP>(it.nvalid, rows, sm.tile[stage]);
+    if constexpr (kBf16) stats_k_bf16<DP>(p, it.unit, it.nvalid, rows, sm.tile[stage]);
+    else stats_k<kBf16, DP>(it.nvalid, rows, sm.tile[stage]);
   } else if (it.kind == kStatsV) {
     stats_v<kBf16, DP>(it.nvalid, rows, sm.tile[stage]);
   } else if (it.kind == kK) {
@@ -763,14 +843,19 @@ __device__ __forceinline__ void flush_stats(const ProParams& p, int unit, bool i
       for (int w = 0; w < kConsumers / 32; ++w) m = __vmaxu2(m, tab[w][c >> 1]);
       m = (c & 1) ? (m >> 16) : (m & 0xFFFFu);
       atomicMax(p.vmax + base + c, __float_as_uint(mag_f32<kBf16>(m)));
+    } else if constexpr (kBf16) {
+      // the channel's exact integer sum on the grid 2^(g - 150) (stats_k_bf16)
+      constexpr int R = kConsumers / (DP / 8);
+      const long long acc = reinterpret_cast<const long long*>(scratch + R * DP * 4)[c];
+      const int g = reinterpret_cast<const int*>(scratch + R * DP * 4 + DP * 8)[c];
+      if (acc != 0) {
+        // exact when |acc| < 2^53; 2^(g - 150) is a normal double (g >= -33)
+        const double scale = __longlong_as_double(static_cast<long long>(g - 150 + 1023) << 52);
+        atomicAdd(static_cast<double*>(p.ksum) + base + c, __ll2double_rn(acc) * scale);
+      }
     } else {
       const long long (*tab)[DP] = reinterpret_cast<const long long (*)[DP]>(scratch);
-      if constexpr (kBf16) {
-        double sd = 0.0;
-#pragma unroll
-        for (int w = 0; w < kConsumers / 32; ++w) sd += __longlong_as_double(tab[w][c]);
-        atomicAdd(static_cast<double*>(p.ksum) + base + c, sd);
-      } else {
+      {
         long long si = 0;
 #pragma unroll
         for (int w = 0; w < kConsumers / 32; ++w) si += tab[w][c];

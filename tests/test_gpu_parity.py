@@ -119,6 +119,36 @@ def test_small_shapes_bit_exact_and_all_rows(sage, orc, w):
     assert cmin >= H.COS_EXACT, cmin
 
 
+def test_bf16_key_means_exact_over_extreme_ranges(sage, orc):
+    """bf16 key sums where a channel mixes magnitudes far apart: partial sums
+    that fp32 cannot hold exactly, partials more than 34 binades apart,
+    subnormals, all-zero channels and values near the top of the range.  The
+    K mean (and every code that depends on it) must still match the oracle's
+    fp64 sum bit for bit."""
+    w = _small("bf16_extreme", D=64, Lq=128, Lk=300, dtype=wl.BF16, seed=21,
+               k_offset_sigma=0.0)
+    inp = wl.make_inputs(w)
+    k = wl.bits_to_float(inp["k"], wl.BF16).copy()          # (B, H, L, D)
+    # (the oracle sums exactly in 128 bits, so each channel keeps its
+    # exponent span within that)
+    k[:, :, ::37, 0] = 2.0 ** 30                               # fp32 partials inexact
+    k[:, :, 5::53, 0] = 2.0 ** -40
+    k[:, :, 3::101, 1] = 2.0 ** 40                             # partials > 34 binades apart
+    k[:, :, :, 2] = 0.0                                        # subnormals only
+    k[:, :, :, 3] = 0.0                                        # all zero
+    k[:, :, :, 4] = 0.0                                        # near the top of the range
+    k[:, :, 11::97, 4] = 2.0 ** 124
+    k[:, :, 13::89, 4] = -(2.0 ** 123)
+    k[:, 1, 17, 5] = -(2.0 ** 60)
+    bits = wl.to_bits(k, wl.BF16)
+    bits[0, 0, 7, 2] = 0x0001
+    bits[0, 1, 9, 2] = 0x8003
+    bits[0, 0, 200, 2] = 0x0042
+    inp["k"] = bits
+    d = H.device_inputs(w, inp)
+    _check_prologue(sage, orc, w, inp, d)
+
+
 FULL = ["small_d64", "b2_h24_l4096_d128", "gqa_causal_b4_l8192", "dit_self_l32768",
         "dit_cross_l32768x512", "varlen_d80", "varlen_d40"]
 
