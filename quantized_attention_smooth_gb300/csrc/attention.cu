@@ -123,9 +123,29 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
   const SegGeo& g = p.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- which pair of query tiles (heaviest causal pairs first)
-  const int64_t s = blockIdx.z, h = blockIdx.y;
-  const int64_t pair = p.causal ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;
+  // ---- which query tiles: a pair (heaviest causal pairs first), or, for
+  // the balanced dense launch (flat_pairs >= 0), a 1D list of pairs in
+  // (segment, head, pair) order followed by the single tiles of the pairs
+  // that would have formed the last partial wave
+  int64_t s, h, qt0;
+  int ntile = 2;
+  if (p.flat_pairs >= 0) {
+    const int64_t npairs = ((g.Lq + kBlockM - 1) / kBlockM + 1) / 2;
+    int64_t pu = blockIdx.x, sub = 0;
+    if (pu >= p.flat_pairs) {
+      sub = (pu - p.flat_pairs) & 1;
+      pu = p.flat_pairs + (pu - p.flat_pairs) / 2;
+      ntile = 1;
+    }
+    const int64_t sh = pu / npairs;
+    h = sh % g.Hq;
+    s = sh / g.Hq;
+    qt0 = 2 * (pu % npairs) + sub;
+  } else {
+    s = blockIdx.z;
+    h = blockIdx.y;
+    qt0 = 2 * static_cast<int64_t>(p.causal ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x);
+  }
   int64_t qstart = 0, len_q = g.Lq, kstart = 0, len_k = g.Lk;
   if (g.varlen) {
     const bool okq = seg_range(g.cu_q, s, g.total_q, g.max_q, &qstart, &len_q);
@@ -135,15 +155,16 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
       return;
     }
   }
-  const int64_t qt0 = 2 * pair;
   if (qt0 * kBlockM >= len_q) return;
+  // query rows this CTA owns: a single tile leaves the next one to its neighbour
+  const int64_t qlim = ntile == 2 ? len_q : min(len_q, (qt0 + 1) * kBlockM);
   const int64_t hk = h / (g.Hq / g.Hkv);
   const int nk_all = static_cast<int>((len_k + kBlockN - 1) / kBlockN);
   int n_t[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int64_t qt = qt0 + t;
-    if (qt * kBlockM >= len_q) n_t[t] = 0;
+    if (qt * kBlockM >= qlim) n_t[t] = 0;
     else n_t[t] = (p.causal && nk_all > qt + 1) ? static_cast<int>(qt + 1) : nk_all;
   }
   const int n_max = n_t[0] > n_t[1] ? n_t[0] : n_t[1];
@@ -361,7 +382,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int D = static_cast<int>(g.D);
     const int64_t seg_off = g.varlen ? qstart * p.out_tok_stride : s * p.out_seg_stride;
     for (int t = 0; ok && t < 2; ++t) {
-      if ((qt0 + t) * kBlockM >= len_q) continue;
+      if ((qt0 + t) * kBlockM >= qlim) continue;
       const int64_t qi = (qt0 + t) * kBlockM + r;
       float* orow = p.out + seg_off + h * p.out_head_stride + qi * p.out_tok_stride;
       if (n_t[t] == 0) {          // no visible key (empty key sequence): zeros
@@ -607,7 +628,34 @@ cudaError_t launch_attention_t(const AttnMaps& maps, const AttnParams& p,
   const int64_t nqt = (maxq + kBlockM - 1) / kBlockM;      // query tiles, two per CTA
   dim3 grid(static_cast<unsigned>((nqt + 1) / 2), static_cast<unsigned>(p.g.Hq),
             static_cast<unsigned>(p.g.nseg));
-  attn_kernel<DP><<<grid, kThreads, Layout<DP>::kAlloc, st>>>(maps.q, maps.k, maps.v, p);
+  AttnParams prm = p;
+  prm.flat_pairs = -1;
+  if (!p.g.varlen && !p.causal) {
+    // Uniform pairs run in waves of one CTA per SM.  When the last wave is
+    // at most half full, its pairs run as single tiles instead (launched
+    // last), which shortens that wave to one tile's time.
+    static int sms[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && sms[dev] == 0) {
+      int n = 0, per = 0;
+      e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, attn_kernel<DP>, kThreads,
+                                                        Layout<DP>::kAlloc);
+      if (e != cudaSuccess) return e;
+      sms[dev] = n * (per > 0 ? per : 1);
+    }
+    const int64_t wave = (dev >= 0 && dev < 64) ? sms[dev] : 0;
+    const int64_t pairs = static_cast<int64_t>(grid.x) * grid.y * grid.z;
+    const int64_t tail = wave > 0 ? pairs % wave : 0;
+    if (tail > 0 && 2 * tail <= wave && pairs + tail < (int64_t(1) << 31)) {
+      prm.flat_pairs = pairs - tail;
+      grid = dim3(static_cast<unsigned>(pairs + tail), 1, 1);
+    }
+  }
+  attn_kernel<DP><<<grid, kThreads, Layout<DP>::kAlloc, st>>>(maps.q, maps.k, maps.v, prm);
   note_launch();
   return cudaGetLastError();
 }

@@ -61,6 +61,8 @@ struct AttnParams {
   float scale_log2;          // sm_scale * log2(e)
   int32_t causal;
   int32_t skip_kv_tile;      // failure-injection hook, -1 = off
+  int32_t flat_pairs;        // >= 0: 1D grid of this many pairs, then single tiles;
+                             // -1: (pair, head, segment) grid (set by the launcher)
   uint64_t timeout_ns;
   uint32_t* status;
 };
