@@ -134,6 +134,26 @@ SAGE_API sage_status sage_quant_prologue_varlen(
     int64_t Hkv, int64_t D, void* ws, size_t ws_bytes, sage_quantized* qt,
     sage_stream_t stream);
 
+/* Prologue on strided views ([RD] v0.3.0, "Fused q/k/v views"): q, k and v
+ * may be views into larger tensors, such as the three slices of one fused
+ * projection, whose token stride is then 3*H*D instead of H*D.
+ *   q_strides : host int64[3], q's {batch, head, token} strides in elements;
+ *   kv_strides: host int64[3], the same for k and v, which share them;
+ *   the channel stride is 1 and every other stride must be positive.
+ * Views with a 16-byte aligned base, strides that are multiples of 8
+ * elements and D % 8 == 0 are copied by the tensor engine; any other
+ * positive strides are read element by element.  A view this call cannot
+ * serve is refused before any launch with SAGE_ERR_UNSUPPORTED (or
+ * SAGE_ERR_INVALID_ARG for missing strides) and the reason in
+ * sage_last_error(); nothing falls back silently.  The workspace
+ * (sage_workspace_bytes) and the quantised operands are those of
+ * sage_quant_prologue. */
+SAGE_API sage_status sage_quant_prologue_strided(
+    const void* q, const void* k, const void* v, int dtype, int64_t B, int64_t Hq,
+    int64_t Hkv, int64_t Lq, int64_t Lk, int64_t D, const int64_t* q_strides,
+    const int64_t* kv_strides, void* ws, size_t ws_bytes, sage_quantized* qt,
+    sage_stream_t stream);
+
 /* Fused attention on quantised operands ([SD] kernel table: INT8 QK^T,
  * FP8 PV with an fp32 accumulator; [OV] Core features): per 128x128 tile,
  * exact integer S = q8 k8^T on the tensor cores, logits S*s_q*s_k*sm_scale
@@ -151,6 +171,14 @@ SAGE_API sage_status sage_attn_fwd(const void* q, const void* k, const void* v,
                           int64_t Lq, int64_t Lk, int64_t D, int layout,
                           int is_causal, float sm_scale, int dtype, void* ws,
                           size_t ws_bytes, sage_stream_t stream);
+
+/* Prologue + attention in one call on strided views (see
+ * sage_quant_prologue_strided); out is dense fp32 in `layout`. */
+SAGE_API sage_status sage_attn_fwd_strided(
+    const void* q, const void* k, const void* v, float* out, int64_t B, int64_t Hq,
+    int64_t Hkv, int64_t Lq, int64_t Lk, int64_t D, const int64_t* q_strides,
+    const int64_t* kv_strides, int layout, int is_causal, float sm_scale, int dtype,
+    void* ws, size_t ws_bytes, sage_stream_t stream);
 
 /* Prologue + attention in one call (packed varlen, [OV] "variable-length
  * sequences via sageattn_varlen"). */

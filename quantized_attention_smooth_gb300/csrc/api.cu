@@ -127,6 +127,31 @@ SegGeo dense_geo(int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk,
   return g;
 }
 
+// Dense geometry of strided views: q_strides / kv_strides are {batch, head,
+// token} in elements (channel stride 1).  Refuses, with the reason, views
+// the prologue cannot read.
+sage_status strided_geo(int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk, int64_t D,
+                        int dtype, const int64_t* qs, const int64_t* kvs, SegGeo* g) {
+  if (qs == nullptr || kvs == nullptr)
+    return fail(SAGE_ERR_INVALID_ARG, "q_strides and kv_strides must be host int64[3] arrays");
+  for (int i = 0; i < 3; ++i) {
+    if (qs[i] <= 0 || kvs[i] <= 0)
+      return fail(SAGE_ERR_UNSUPPORTED,
+                  "strided views need positive strides (q {%lld, %lld, %lld}, k/v {%lld, "
+                  "%lld, %lld}); zero (broadcast) or negative strides are not served",
+                  (long long)qs[0], (long long)qs[1], (long long)qs[2], (long long)kvs[0],
+                  (long long)kvs[1], (long long)kvs[2]);
+    if (qs[i] >= (int64_t(1) << 39) || kvs[i] >= (int64_t(1) << 39))
+      return fail(SAGE_ERR_UNSUPPORTED,
+                  "a stride of 2^39 elements or more is not served (tensor-copy limit)");
+  }
+  *g = dense_geo(B, Hq, Hkv, Lq, Lk, D, dtype, SAGE_HND);
+  g->strided = 1;
+  g->q_seg_stride = qs[0]; g->q_head_stride = qs[1]; g->q_tok_stride = qs[2];
+  g->k_seg_stride = kvs[0]; g->k_head_stride = kvs[1]; g->k_tok_stride = kvs[2];
+  return SAGE_OK;
+}
+
 SegGeo varlen_geo(int64_t nseq, int64_t total_q, int64_t total_k, int max_q,
                   int max_k, int64_t Hq, int64_t Hkv, int64_t D, int dtype,
                   const int32_t* cu_q, const int32_t* cu_k) {
@@ -291,7 +316,12 @@ sage_status run_prologue(const SegGeo& g, const void* q, const void* k, const vo
   b.sync = reinterpret_cast<unsigned int*>(wsb + w.sync);
   b.timeout_ns = wait_timeout_ns();
   b.status = reinterpret_cast<uint32_t*>(wsb + w.status);
-  const bool vec = (g.D % 8 == 0) && aligned(q, 16) && aligned(k, 16) && aligned(v, 16);
+  // tensor copies need 16-byte aligned rows: base, channel count and every
+  // stride (for views) in whole 16-byte units
+  const bool vec = (g.D % 8 == 0) && aligned(q, 16) && aligned(k, 16) && aligned(v, 16) &&
+                   g.q_seg_stride % 8 == 0 && g.q_head_stride % 8 == 0 &&
+                   g.q_tok_stride % 8 == 0 && g.k_seg_stride % 8 == 0 &&
+                   g.k_head_stride % 8 == 0 && g.k_tok_stride % 8 == 0;
   e = launch_prologue(g, b, vec, st);
   if (e != cudaSuccess) return cuda_fail(e, "prologue launch");
   return ok();
@@ -407,6 +437,27 @@ sage_status sage_quant_prologue_varlen(const void* q, const void* k, const void*
                       q, k, v, ws, ws_bytes, qt, reinterpret_cast<cudaStream_t>(stream));
 }
 
+sage_status sage_quant_prologue_strided(const void* q, const void* k, const void* v,
+                                        int dtype, int64_t B, int64_t Hq, int64_t Hkv,
+                                        int64_t Lq, int64_t Lk, int64_t D,
+                                        const int64_t* q_strides, const int64_t* kv_strides,
+                                        void* ws, size_t ws_bytes, sage_quantized* qt,
+                                        sage_stream_t stream) {
+  if (qt == nullptr) return fail(SAGE_ERR_INVALID_ARG, "qt must not be null");
+  sage_status s = SAGE_OK;
+  if (B < 0 || Lq < 0 || Lk < 0)
+    return fail(SAGE_ERR_INVALID_ARG, "negative size (B=%lld Lq=%lld Lk=%lld)",
+                (long long)B, (long long)Lq, (long long)Lk);
+  if (!check_dims(Hq, Hkv, D, &s)) return s;
+  if ((s = check_common(q, k, v, dtype)) != SAGE_OK) return s;
+  if (B == 0 || Lq == 0 || Lk == 0)
+    return fail(SAGE_ERR_INVALID_ARG, "the prologue needs B, Lq and Lk > 0");
+  SegGeo g;
+  if ((s = strided_geo(B, Hq, Hkv, Lq, Lk, D, dtype, q_strides, kv_strides, &g)) != SAGE_OK)
+    return s;
+  return run_prologue(g, q, k, v, ws, ws_bytes, qt, reinterpret_cast<cudaStream_t>(stream));
+}
+
 sage_status sage_attn_quantized(const sage_quantized* qt, float* out, int layout,
                                 int is_causal, float sm_scale, sage_stream_t stream) {
   if (qt == nullptr || qt->q16 == nullptr || qt->status == nullptr)
@@ -449,6 +500,39 @@ sage_status sage_attn_fwd(const void* q, const void* k, const void* v, float* ou
   s = run_prologue(dense_geo(B, Hq, Hkv, Lq, Lk, D, dtype, layout), q, k, v, ws, ws_bytes,
                    &qt, st);
   if (s != SAGE_OK) return s;
+  if (qt.nseg > 65535 || qt.Hq > 65535)
+    return fail(SAGE_ERR_UNSUPPORTED, "more than 65535 segments or heads");
+  return launch_attn(&qt, out, layout, is_causal, sm_scale, st);
+}
+
+sage_status sage_attn_fwd_strided(const void* q, const void* k, const void* v, float* out,
+                                  int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk,
+                                  int64_t D, const int64_t* q_strides,
+                                  const int64_t* kv_strides, int layout, int is_causal,
+                                  float sm_scale, int dtype, void* ws, size_t ws_bytes,
+                                  sage_stream_t stream) {
+  sage_status s = SAGE_OK;
+  if (layout != SAGE_HND && layout != SAGE_NHD)
+    return fail(SAGE_ERR_INVALID_ARG, "layout %d is neither SAGE_HND nor SAGE_NHD", layout);
+  if (B < 0 || Lq < 0 || Lk < 0)
+    return fail(SAGE_ERR_INVALID_ARG, "negative size (B=%lld Lq=%lld Lk=%lld)",
+                (long long)B, (long long)Lq, (long long)Lk);
+  if (!check_dims(Hq, Hkv, D, &s)) return s;
+  SegGeo g;
+  if ((s = strided_geo(B, Hq, Hkv, Lq, Lk, D, dtype, q_strides, kv_strides, &g)) != SAGE_OK)
+    return s;
+  if (B == 0 || Lq == 0) return ok();                 // nothing to compute
+  if ((s = check_common(q, Lk == 0 ? q : k, Lk == 0 ? q : v, dtype)) != SAGE_OK) return s;
+  if (out == nullptr || !aligned(out, 4))
+    return fail(SAGE_ERR_INVALID_ARG, "out must be a 4-byte aligned device pointer");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (Lk == 0) {                                      // empty softmax: zeros
+    if ((s = check_device()) != SAGE_OK) return s;
+    cudaError_t e = cudaMemsetAsync(out, 0, out_elems_dense(B, Hq, Lq, D) * 4, st);
+    return e == cudaSuccess ? ok() : cuda_fail(e, "cudaMemsetAsync");
+  }
+  sage_quantized qt;
+  if ((s = run_prologue(g, q, k, v, ws, ws_bytes, &qt, st)) != SAGE_OK) return s;
   if (qt.nseg > 65535 || qt.Hq > 65535)
     return fail(SAGE_ERR_UNSUPPORTED, "more than 65535 segments or heads");
   return launch_attn(&qt, out, layout, is_causal, sm_scale, st);

@@ -202,6 +202,17 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d_hint(void* dst, const CUtensorMap* map, int32_t x,
+                                                 int32_t y, int32_t z, int32_t w,
+                                                 uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
+      :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z),
+         "r"(w), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
 // Contiguous global -> shared copy (16-byte aligned ends) completing on bar.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
@@ -1097,6 +1108,11 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
           zc = static_cast<int32_t>((g.varlen ? start : s * L) + t0);
         }
         mbar_expect_tx(&sm.full[stage], static_cast<uint32_t>(kBlockN * DP * 2) + aux_bytes);
+        if (g.strided)           // views: (channel, token, head, batch) maps
+          tma_load_4d_hint(sm.tile[stage], map, 0, static_cast<int32_t>(t0),
+                           static_cast<int32_t>(h), static_cast<int32_t>(s), &sm.full[stage],
+                           it.kind <= kStatsV ? keep : once);
+        else
         tma_load_3d_hint(sm.tile[stage], map, 0, y, zc, &sm.full[stage],
                          it.kind <= kStatsV ? keep : once);
       } else {
@@ -1254,6 +1270,20 @@ bool input_map(CUtensorMap* map, const uint16_t* base, int64_t D, int64_t Dp, in
                       dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+// 4D map of a strided view: (channel, token, head, batch) with the caller's
+// strides (elements, each a multiple of 8); boxes are 128 tokens of Dp
+// channels, channels past D zero-filled.
+bool view_map(CUtensorMap* map, const uint16_t* base, int64_t D, int64_t Dp, int64_t L,
+              int64_t H, int64_t B, int64_t tok, int64_t head, int64_t batch) {
+  uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(L),
+                      static_cast<uint64_t>(H), static_cast<uint64_t>(B)};
+  uint64_t strides[3] = {static_cast<uint64_t>(tok) * 2, static_cast<uint64_t>(head) * 2,
+                         static_cast<uint64_t>(batch) * 2};
+  uint32_t box[4] = {static_cast<uint32_t>(Dp), 128, 1, 1};
+  return encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<uint16_t*>(base),
+                      dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 template <bool kTma, bool kBf16, int DP>
 cudaError_t launch_t(ProParams& prm, bool with_quant, cudaStream_t st) {
   static int per_sm[64] = {};                  // resident CTAs per SM, per device
@@ -1298,12 +1328,23 @@ cudaError_t launch_any(ProParams& prm, bool vec, bool with_quant, cudaStream_t s
     prm.k_hnd = !g.varlen && g.k_tok_stride == g.D;
     const int64_t ntq = g.varlen ? g.total_q : g.nseg * g.Lq;
     const int64_t ntk = g.varlen ? g.total_k : g.nseg * g.Lk;
-    if (prm.q != nullptr && ntq > 0 &&
-        !input_map(&prm.mq, prm.q, g.D, g.Dp, g.Hq, g.Lq, ntq, prm.q_hnd))
-      return cudaErrorInvalidValue;
-    if (ntk > 0 && (!input_map(&prm.mk, prm.k, g.D, g.Dp, g.Hkv, g.Lk, ntk, prm.k_hnd) ||
-                    !input_map(&prm.mv, prm.v, g.D, g.Dp, g.Hkv, g.Lk, ntk, prm.k_hnd)))
-      return cudaErrorInvalidValue;
+    if (g.strided) {
+      if ((prm.q != nullptr && ntq > 0 &&
+           !view_map(&prm.mq, prm.q, g.D, g.Dp, g.Lq, g.Hq, g.nseg, g.q_tok_stride,
+                     g.q_head_stride, g.q_seg_stride)) ||
+          (ntk > 0 && (!view_map(&prm.mk, prm.k, g.D, g.Dp, g.Lk, g.Hkv, g.nseg, g.k_tok_stride,
+                                 g.k_head_stride, g.k_seg_stride) ||
+                       !view_map(&prm.mv, prm.v, g.D, g.Dp, g.Lk, g.Hkv, g.nseg, g.k_tok_stride,
+                                 g.k_head_stride, g.k_seg_stride))))
+        return cudaErrorInvalidValue;
+    } else {
+      if (prm.q != nullptr && ntq > 0 &&
+          !input_map(&prm.mq, prm.q, g.D, g.Dp, g.Hq, g.Lq, ntq, prm.q_hnd))
+        return cudaErrorInvalidValue;
+      if (ntk > 0 && (!input_map(&prm.mk, prm.k, g.D, g.Dp, g.Hkv, g.Lk, ntk, prm.k_hnd) ||
+                      !input_map(&prm.mv, prm.v, g.D, g.Dp, g.Hkv, g.Lk, ntk, prm.k_hnd)))
+        return cudaErrorInvalidValue;
+    }
     if (bf16) return d64 ? launch_t<true, true, 64>(prm, with_quant, st)
                          : launch_t<true, true, 128>(prm, with_quant, st);
     return d64 ? launch_t<true, false, 64>(prm, with_quant, st)

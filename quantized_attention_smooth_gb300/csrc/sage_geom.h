@@ -21,6 +21,7 @@ constexpr uint32_t kStatusBadItem = 4u;      // a work item decoded outside the 
 struct SegGeo {
   int64_t nseg, Hq, Hkv, Lq, Lk, D, Dp;
   int32_t dtype, varlen;
+  int32_t strided;            // dense inputs given as arbitrary views (per-tensor strides)
   const int32_t* cu_q;
   const int32_t* cu_k;
   int64_t total_q, total_k;

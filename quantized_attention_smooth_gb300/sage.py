@@ -23,7 +23,8 @@ EXPORTS = (
     "sage_quant_prologue_varlen", "sage_attn_quantized", "sage_attn_fwd",
     "sage_attn_fwd_varlen", "sage_debug_qk_int32", "sage_debug_e4m3",
     "sage_debug_set_fault", "sage_device_status", "sage_last_error",
-    "sage_kv_stats_noalloc", "sage_launch_count",
+    "sage_kv_stats_noalloc", "sage_launch_count", "sage_quant_prologue_strided",
+    "sage_attn_fwd_strided",
 )
 
 
@@ -67,6 +68,10 @@ def _load():
         "sage_quant_prologue": ([P, P, P, I, I, I64, I64, I64, I64, I64, I64, P, SZ, QP, P], I),
         "sage_quant_prologue_varlen": ([P, P, P, I, P, P, I64, I64, I64, I, I, I64, I64, I64,
                                         P, SZ, QP, P], I),
+        "sage_quant_prologue_strided": ([P, P, P, I, I64, I64, I64, I64, I64, I64, P, P, P, SZ,
+                                         QP, P], I),
+        "sage_attn_fwd_strided": ([P, P, P, P, I64, I64, I64, I64, I64, I64, P, P, I, I, F, I,
+                                   P, SZ, P], I),
         "sage_attn_quantized": ([QP, P, I, I, F, P], I),
         "sage_attn_fwd": ([P, P, P, P, I64, I64, I64, I64, I64, I64, I, I, F, I, P, SZ, P], I),
         "sage_attn_fwd_varlen": ([P, P, P, P, P, P, I64, I64, I64, I, I, I64, I64, I64, I, F,
@@ -227,11 +232,68 @@ def attn_fwd_varlen(q, k, v, out, cu_q, cu_k, max_q, max_k, is_causal=False,
     return out
 
 
+def view_strides(t, layout) -> tuple:
+    """(batch, head, token) strides in elements of a q/k/v view in `layout`;
+    the channel stride must be 1."""
+    lay = _layout_code(layout)
+    st = t.stride()
+    if st[3] != 1:
+        raise ValueError(f"strided views need contiguous channels (channel stride {st[3]})")
+    return (st[0], st[1], st[2]) if lay == HND else (st[0], st[2], st[1])
+
+
+def _strides_arg(vals):
+    return (ctypes.c_int64 * 3)(*[int(x) for x in vals])
+
+
+def _kv_strides(k, v, layout):
+    ks, vs = view_strides(k, layout), view_strides(v, layout)
+    if ks != vs:
+        raise ValueError(f"k and v views must share their strides (k {ks}, v {vs})")
+    return ks
+
+
+def quant_prologue_strided(q, k, v, layout="HND", ws=None, stream=None) -> Quantized:
+    """Prologue on q/k/v views (e.g. slices of one fused projection)."""
+    lay = _layout_code(layout)
+    B, Hq, Hkv, Lq, Lk, D = _dims(q, k, lay)
+    if ws is None:
+        ws = alloc_workspace(workspace_bytes(B, Hq, Hkv, Lq, Lk, D), q.device)
+    qt = Quantized()
+    rc = _lib.sage_quant_prologue_strided(
+        _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, Hq, Hkv, Lq, Lk, D,
+        _strides_arg(view_strides(q, lay)), _strides_arg(_kv_strides(k, v, lay)), _ptr(ws),
+        ws.numel(), ctypes.byref(qt), _stream(stream))
+    _check(rc, "sage_quant_prologue_strided")
+    qt._ws = ws
+    return qt
+
+
+def attn_fwd_strided(q, k, v, out, layout="HND", is_causal=False, sm_scale=None, ws=None,
+                     stream=None):
+    """Prologue + attention on q/k/v views; out is dense fp32 in `layout`."""
+    lay = _layout_code(layout)
+    B, Hq, Hkv, Lq, Lk, D = _dims(q, k, lay)
+    if ws is None:
+        ws = alloc_workspace(workspace_bytes(B, Hq, Hkv, Lq, Lk, D), q.device)
+    rc = _lib.sage_attn_fwd_strided(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, Lq, Lk, D,
+        _strides_arg(view_strides(q, lay)), _strides_arg(_kv_strides(k, v, lay)), lay,
+        int(bool(is_causal)), float(sm_scale or 0.0), _dtype_code(q), _ptr(ws), ws.numel(),
+        _stream(stream))
+    _check(rc, "sage_attn_fwd_strided")
+    return out
+
+
 def sageattn(q, k, v, tensor_layout="HND", is_causal=False, sm_scale=None):
-    """Drop-in style call: fp16/bf16 q, k, v on the GPU -> fp32 output."""
+    """Drop-in style call: fp16/bf16 q, k, v on the GPU -> fp32 output.  Views
+    (for instance the slices of a fused qkv projection) go through the
+    strided entry point; a view it cannot serve raises with the reason."""
     import torch
     out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
-    return attn_fwd(q, k, v, out, tensor_layout, is_causal, sm_scale)
+    if q.is_contiguous() and k.is_contiguous() and v.is_contiguous():
+        return attn_fwd(q, k, v, out, tensor_layout, is_causal, sm_scale)
+    return attn_fwd_strided(q, k, v, out, tensor_layout, is_causal, sm_scale)
 
 
 def debug_qk_int32(qt: Quantized, seg, hq, qtile, ktile, out=None, stream=None):

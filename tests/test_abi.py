@@ -106,3 +106,40 @@ def test_quantized_call_rejects_unfilled_struct():
 def test_sage_error_carries_reason():
     with pytest.raises(sage.SageError, match="head_dim"):
         sage._check(_fwd(D=200), "sage_attn_fwd")
+
+
+def _strided(qs, kvs, **kw):
+    a = dict(B=1, Hq=2, Hkv=2, Lq=128, Lk=128, D=64, layout=0)
+    a.update(kw)
+    arr = lambda x: None if x is None else (ctypes.c_int64 * 3)(*x)
+    return sage.lib.sage_attn_fwd_strided(FAKE, FAKE, FAKE, FAKE, a["B"], a["Hq"], a["Hkv"],
+                                          a["Lq"], a["Lk"], a["D"], arr(qs), arr(kvs),
+                                          a["layout"], 0, 0.0, 0, FAKE, 1 << 30, None)
+
+
+@pytest.mark.parametrize("qs,kvs,status,needle", [
+    (None, (1, 1, 1), sage.ERR_INVALID_ARG, "strides"),
+    ((0, 64, 384), (24576, 64, 384), sage.ERR_UNSUPPORTED, "zero (broadcast)"),
+    ((24576, 64, 384), (24576, -64, 384), sage.ERR_UNSUPPORTED, "positive"),
+    ((1 << 39, 64, 384), (24576, 64, 384), sage.ERR_UNSUPPORTED, "2^39"),
+])
+def test_strided_views_refused_with_a_reason(qs, kvs, status, needle):
+    """Views the strided entry cannot serve are refused before any launch,
+    with the reason in the error text (the pages' fused q/k/v note: a refusal
+    carries its reason)."""
+    rc = _strided(qs, kvs)
+    assert rc == status
+    assert needle in sage.last_error()
+
+
+def test_view_strides_of_fused_projection_slices():
+    torch = pytest.importorskip("torch")
+    B, L, H, D = 2, 5, 3, 8
+    qkv = torch.empty(B, L, 3, H, D, dtype=torch.float16)
+    q, k, v = qkv.unbind(2)                       # NHD views, token stride 3*H*D
+    assert sage.view_strides(q, "NHD") == (L * 3 * H * D, D, 3 * H * D)
+    assert sage.view_strides(k, "NHD") == sage.view_strides(v, "NHD")
+    t = torch.empty(B, H, L, 2 * D, dtype=torch.float16)[..., :D]   # HND, token stride 2D
+    assert sage.view_strides(t, "HND") == (H * L * 2 * D, L * 2 * D, 2 * D)
+    with pytest.raises(ValueError, match="contiguous channels"):
+        sage.view_strides(torch.empty(B, H, L, D, dtype=torch.float16).transpose(2, 3), "HND")
