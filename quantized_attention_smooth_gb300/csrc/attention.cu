@@ -360,16 +360,34 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
           const float alpha = alpha_s[(2 * t + (j & 1)) * kBlockM + r];
           if (__any_sync(kFull, alpha < 1.0f)) {
             const uint32_t to = tbase + lane_off + 256 + t * DP;
-#pragma unroll 1
-            for (int cc = 0; cc < DP / 32; ++cc) {
-              uint32_t o[32];
-              tmem_ld32(to + 32 * cc, o);
-              tmem_ld_wait();
-              reg_fence(o);
+            // 16-column chunks, the next chunk's load in flight while this
+            // one is scaled; a buffer is reloaded only after its store
+            // has completed
+            constexpr int NC = DP / 16;
+            const float2 a2 = make_float2(alpha, alpha);
+            uint32_t ob[2][16];
+            tmem_ld16(to, ob[0]);
+            tmem_ld_wait();
+            reg_fence(ob[0]);
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st32(to + 32 * cc, o);
+            for (int cc = 0; cc < NC; ++cc) {
+              uint32_t (&cur)[16] = ob[cc & 1];
+              if (cc + 1 < NC) {
+                if (cc >= 1) tmem_st_wait();
+                tmem_ld16(to + 16 * (cc + 1), ob[(cc + 1) & 1]);
+              }
+#pragma unroll
+              for (int i = 0; i < 16; i += 2) {     // packed multiplies, same rounding
+                const float2 v = __fmul2_rn(
+                    make_float2(__uint_as_float(cur[i]), __uint_as_float(cur[i + 1])), a2);
+                cur[i] = __float_as_uint(v.x);
+                cur[i + 1] = __float_as_uint(v.y);
+              }
+              tmem_st16(to + 16 * cc, cur);
+              if (cc + 1 < NC) {
+                tmem_ld_wait();
+                reg_fence(ob[(cc + 1) & 1]);
+              }
             }
             tmem_st_wait();
           }
@@ -492,21 +510,26 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
 
       // 448 P = 2^(S c - m' + log2 448), quantised to e4m3
       const float bias = kLog2_448 - m_new;
-      float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+      // packed fp32 pairs: the fused multiply-add rounds like fmaf, and the
+      // two packed sums keep the four chains (element i goes to chain i % 4)
+      const float2 c2 = make_float2(c, c), b2 = make_float2(bias, bias);
+      float2 a01 = make_float2(0.0f, 0.0f), a23 = make_float2(0.0f, 0.0f);
       uint32_t w[32];
 #pragma unroll
       for (int q4 = 0; q4 < 32; ++q4) {
         const int i = 4 * q4;
-        const float p0 = fast_exp2(fmaf(__uint_as_float(sr[i >> 5][i & 31]), c, bias));
-        const float p1 = fast_exp2(fmaf(__uint_as_float(sr[i >> 5][(i & 31) + 1]), c, bias));
-        const float p2 = fast_exp2(fmaf(__uint_as_float(sr[i >> 5][(i & 31) + 2]), c, bias));
-        const float p3 = fast_exp2(fmaf(__uint_as_float(sr[i >> 5][(i & 31) + 3]), c, bias));
-        a0 += p0;
-        a1 += p1;
-        a2 += p2;
-        a3 += p3;
-        w[q4] = pack_e4m3x2(p0, p1) | (pack_e4m3x2(p2, p3) << 16);
+        const uint32_t* src = &sr[i >> 5][i & 31];
+        const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(src[0]), __uint_as_float(src[1])),
+                                      c2, b2);
+        const float2 x23 = __ffma2_rn(make_float2(__uint_as_float(src[2]), __uint_as_float(src[3])),
+                                      c2, b2);
+        const float2 p01 = make_float2(fast_exp2(x01.x), fast_exp2(x01.y));
+        const float2 p23 = make_float2(fast_exp2(x23.x), fast_exp2(x23.y));
+        a01 = __fadd2_rn(a01, p01);
+        a23 = __fadd2_rn(a23, p23);
+        w[q4] = pack_e4m3x2(p01.x, p01.y) | (pack_e4m3x2(p23.x, p23.y) << 16);
       }
+      const float a0 = a01.x, a1 = a01.y, a2 = a23.x, a3 = a23.y;
       // the P~ buffer is free once PV(j-1) has read it
       if (j > 0) {
         ok = wait_all(&o_done[t], (j - 1) & 1, abort_flag, p.status, p.timeout_ns);
