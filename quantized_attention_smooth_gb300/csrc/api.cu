@@ -343,7 +343,7 @@ float resolve_scale(float sm_scale, int64_t D) {
 
 sage_status launch_attn(const sage_quantized* qt, float* out, int layout, int is_causal,
                         float sm_scale, cudaStream_t st) {
-  AttnMaps maps;
+  AttnMaps maps{};
   sage_status s = make_maps(qt, &maps);
   if (s != SAGE_OK) return s;
   AttnParams p{};
@@ -361,6 +361,38 @@ sage_status launch_attn(const sage_quantized* qt, float* out, int layout, int is
   }
   p.scale_log2 = resolve_scale(sm_scale, qt->D) * 1.44269504088896340736f;
   p.causal = is_causal ? 1 : 0;
+  // the output as a tensor-store target (32-column boxes of 128 rows): rows
+  // of a dense tile are clipped at Lq, columns at D; needs 16-byte rows
+  p.out_tma = 0;
+  if (qt->D % 4 == 0 && aligned(out, 16)) {
+    const uint64_t D = static_cast<uint64_t>(qt->D), Hq = static_cast<uint64_t>(qt->Hq);
+    uint64_t dims[4], strides[3];
+    uint32_t box[4];
+    uint32_t rank = 4;
+    int kind;
+    if (qt->varlen) {
+      rank = 3;
+      kind = 3;
+      dims[0] = D; dims[1] = Hq; dims[2] = static_cast<uint64_t>(qt->total_q);
+      strides[0] = D * 4; strides[1] = Hq * D * 4;
+      box[0] = 32; box[1] = 1; box[2] = 128;
+    } else if (layout == SAGE_HND) {
+      kind = 1;
+      const uint64_t Lq = static_cast<uint64_t>(qt->Lq);
+      dims[0] = D; dims[1] = Lq; dims[2] = Hq; dims[3] = static_cast<uint64_t>(qt->nseg);
+      strides[0] = D * 4; strides[1] = Lq * D * 4; strides[2] = Hq * Lq * D * 4;
+      box[0] = 32; box[1] = 128; box[2] = 1; box[3] = 1;
+    } else {
+      kind = 2;
+      const uint64_t Lq = static_cast<uint64_t>(qt->Lq);
+      dims[0] = D; dims[1] = Hq; dims[2] = Lq; dims[3] = static_cast<uint64_t>(qt->nseg);
+      strides[0] = D * 4; strides[1] = Hq * D * 4; strides[2] = Lq * Hq * D * 4;
+      box[0] = 32; box[1] = 1; box[2] = 128; box[3] = 1;
+    }
+    if (encode_tiled(&maps.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, out, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+      p.out_tma = kind;
+  }
   p.skip_kv_tile = g_skip_kv_tile.load();
   p.timeout_ns = wait_timeout_ns();
   p.status = qt->status;

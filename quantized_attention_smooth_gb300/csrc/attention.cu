@@ -71,8 +71,8 @@ struct Layout {
   static constexpr int kPOff = kVOff + kVStages * kVBytes;
   static constexpr int kBarOff = kPOff + 2 * kPBytes;
   // q_full, k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], then per tile:
-  // s_full, s_free, alpha_ready[2], pv_ready, o_done, l_ready, drain
-  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 * 8;
+  // s_full, s_free, alpha_ready[2], pv_ready, o_done, l_ready, drain, epi_full, epi_free
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 * 10;
   static constexpr int kAlphaOff = (kBarOff + kNumBars * 8 + 15) / 16 * 16;
   static constexpr int kLOff = kAlphaOff + 4 * kBlockM * 4;
   static constexpr int kSvOff = kLOff + 2 * kBlockM * 4;
@@ -116,7 +116,8 @@ template <int DP>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_kernel(const __grid_constant__ CUtensorMap tm_q,
             const __grid_constant__ CUtensorMap tm_k,
-            const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+            const __grid_constant__ CUtensorMap tm_v,
+            const __grid_constant__ CUtensorMap tm_o, const AttnParams p) {
   using L = Layout<DP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -190,6 +191,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
   uint64_t* o_done = pv_ready + 2;            // [2]
   uint64_t* l_ready = o_done + 2;             // [2]
   uint64_t* drain = l_ready + 2;              // [2]
+  // epilogue staging: a chunk's rows are in shared memory; a reused staging
+  // buffer has been read by its tensor store
+  uint64_t* epi_full = drain + 2;             // [2]
+  uint64_t* epi_free = epi_full + 2;          // [2]
   float* alpha_s = reinterpret_cast<float*>(smem + L::kAlphaOff);   // [2][2][128]
   float* l_s = reinterpret_cast<float*>(smem + L::kLOff);           // [2][128]
   float* sv_cache = reinterpret_cast<float*>(smem + L::kSvOff);
@@ -216,6 +221,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_init(&pv_ready[t], 2 * kBlockM);
       mbar_init(&o_done[t], 1);
       mbar_init(&l_ready[t], kBlockM);
+      mbar_init(&epi_full[t], kBlockM);
+      mbar_init(&epi_free[t], 1);
       mbar_init(&drain[t], 1);
     }
     mbar_fence_init();
@@ -398,6 +405,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     // epilogue: out = O * s_v / (448 l), the caller's D channels only
     const int D = static_cast<int>(g.D);
+    int stores = 0;                 // tensor stores issued (thread r == 0)
     const int64_t seg_off = g.varlen ? qstart * p.out_tok_stride : s * p.out_seg_stride;
     for (int t = 0; ok && t < 2; ++t) {
       if ((qt0 + t) * kBlockM >= qlim) continue;
@@ -415,6 +423,67 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
       const float l448 = l_s[t * kBlockM + r];
       const float inv = l448 > 0.0f ? __fdiv_rn(1.0f, l448) : 0.0f;
       const bool valid = qi < len_q;
+      const int64_t qtile = qt0 + t;
+      if (p.out_tma != 0 && (!g.varlen || (qtile + 1) * kBlockM <= len_q)) {
+        // tensor stores where their clipping is exact (dense outputs end at
+        // Lq; full tiles of a packed sequence), from staging chunks of 128
+        // rows x 32 fp32 in the 128-byte swizzle layout, held in Q_t and
+        // P~_t, which the tensor cores no longer read
+        constexpr int kBufs = DP == 128 ? 3 : 2;
+        uint8_t* const q_t = smem + L::kQOff + t * L::kQBytes;
+        uint8_t* const p_t = smem + L::kPOff + t * L::kPBytes;
+        const uint32_t to = tbase + lane_off + 256 + t * DP;
+        for (int cc = 0; ok && cc < DP / 32 && 32 * cc < D; ++cc) {
+          uint8_t* buf = cc % kBufs == kBufs - 1 ? p_t : q_t + (cc % kBufs) * 16384;
+          if (cc >= kBufs) {      // the store of chunk cc - kBufs must have read it
+            if (r == 0) {
+              bulk_wait_read<kBufs - 1>();
+              mbar_arrive(&epi_free[t]);
+            }
+            ok = wait_all(&epi_free[t], (cc - kBufs) & 1, abort_flag, p.status, p.timeout_ns);
+            if (!ok) break;
+          }
+          uint4* row = reinterpret_cast<uint4*>(buf + r * 128);
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {   // 16 columns at a time
+            uint32_t o[16];
+            tmem_ld16(to + 32 * cc + 16 * half, o);
+            tmem_ld_wait();
+            reg_fence(o);
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const int c = 32 * cc + 16 * half + 4 * k4;
+              uint4 v;
+              v.x = __float_as_uint(__uint_as_float(o[4 * k4]) * sv_cache[c] * inv);
+              v.y = __float_as_uint(__uint_as_float(o[4 * k4 + 1]) * sv_cache[c + 1] * inv);
+              v.z = __float_as_uint(__uint_as_float(o[4 * k4 + 2]) * sv_cache[c + 2] * inv);
+              v.w = __float_as_uint(__uint_as_float(o[4 * k4 + 3]) * sv_cache[c + 3] * inv);
+              row[(4 * half + k4) ^ (r & 7)] = v;
+            }
+          }
+          fence_proxy_async_smem();
+          // every row of the chunk is staged (all threads wait, so none can
+          // arrive twice in one phase)
+          mbar_arrive(&epi_full[t]);
+          ok = wait_all(&epi_full[t], cc & 1, abort_flag, p.status, p.timeout_ns);
+          if (!ok) break;
+          if (r == 0) {
+            const int32_t row0 = static_cast<int32_t>(qtile * kBlockM);
+            if (p.out_tma == 3)
+              tma_store_3d(&tm_o, buf, 32 * cc, static_cast<int32_t>(h),
+                           static_cast<int32_t>(qstart) + row0);
+            else if (p.out_tma == 1)
+              tma_store_4d(&tm_o, buf, 32 * cc, row0, static_cast<int32_t>(h),
+                           static_cast<int32_t>(s));
+            else
+              tma_store_4d(&tm_o, buf, 32 * cc, static_cast<int32_t>(h), row0,
+                           static_cast<int32_t>(s));
+            bulk_commit();
+            ++stores;
+          }
+        }
+        continue;
+      }
       const bool vec = (D % 4 == 0) && ((reinterpret_cast<uintptr_t>(orow) & 15) == 0);
 #pragma unroll 1
       for (int cc = 0; cc < DP / 32; ++cc) {
@@ -445,6 +514,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
       }
     }
+    // the tensor stores must be complete before the CTA ends
+    if (r == 0 && stores > 0) bulk_wait_all();
   } else {
     // ================================================ softmax of tile wg
     regs_increase<kSoftmaxRegs>();
@@ -678,7 +749,8 @@ cudaError_t launch_attention_t(const AttnMaps& maps, const AttnParams& p,
       grid = dim3(static_cast<unsigned>(pairs + tail), 1, 1);
     }
   }
-  attn_kernel<DP><<<grid, kThreads, Layout<DP>::kAlloc, st>>>(maps.q, maps.k, maps.v, prm);
+  attn_kernel<DP><<<grid, kThreads, Layout<DP>::kAlloc, st>>>(maps.q, maps.k, maps.v, maps.o,
+                                                               prm);
   note_launch();
   return cudaGetLastError();
 }

@@ -61,6 +61,8 @@ struct AttnParams {
   float scale_log2;          // sm_scale * log2(e)
   int32_t causal;
   int32_t skip_kv_tile;      // failure-injection hook, -1 = off
+  int32_t out_tma;           // output map: 0 none (per-row stores), 1 dense HND,
+                             // 2 dense NHD, 3 packed (varlen)
   int32_t flat_pairs;        // >= 0: 1D grid of this many pairs, then single tiles;
                              // -1: (pair, head, segment) grid (set by the launcher)
   uint64_t timeout_ns;
@@ -69,6 +71,7 @@ struct AttnParams {
 
 struct AttnMaps {
   CUtensorMap q, k, v;
+  CUtensorMap o;             // fp32 output, 32-column boxes of 128 rows (see out_tma)
 };
 
 cudaError_t launch_attention(const AttnMaps& maps, const AttnParams& p,
