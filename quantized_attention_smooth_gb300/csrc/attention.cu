@@ -241,6 +241,116 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
   const uint32_t tbase = *tmem_slot;
   const int wg = warp >> 2;
 
+  // Epilogue of query tile t by one warpgroup (thread r holds row r; the
+  // thread with r == 0 issues the tensor stores and counts them in stores):
+  // out = O * s_v / (448 l), the caller's D channels only.  Tensor stores
+  // where their clipping is exact (dense outputs end at Lq; full tiles of a
+  // packed sequence), from staging chunks of 128 rows x 32 fp32 in the
+  // 128-byte swizzle layout, held in Q_t and P~_t, which the tensor cores no
+  // longer read; per-row stores otherwise.  False if a bounded wait ran out.
+  auto epilogue = [&](int t, int r, uint32_t lane_off, int& stores) -> bool {
+    const int64_t qtile = qt0 + t;
+    if (qtile * kBlockM >= qlim) return true;              // not this CTA's tile
+    const int D = static_cast<int>(g.D);
+    const int64_t seg_off = g.varlen ? qstart * p.out_tok_stride : s * p.out_seg_stride;
+    const int64_t qi = qtile * kBlockM + r;
+    float* orow = p.out + seg_off + h * p.out_head_stride + qi * p.out_tok_stride;
+    const bool valid = qi < len_q;
+    if (n_t[t] == 0) {            // no visible key (empty key sequence): zeros
+      if (valid)
+        for (int c = 0; c < D; ++c) orow[c] = 0.0f;
+      return true;
+    }
+    // l_ready completes once, when the softmax has finished the tile; by then
+    // it has waited for every PV but the last, so o_done's parity names the
+    // last PV exactly, even for a warpgroup that has not followed its phases
+    if (!wait_all(&l_ready[t], 0, abort_flag, p.status, p.timeout_ns) ||
+        !wait_all(&o_done[t], (n_t[t] - 1) & 1, abort_flag, p.status, p.timeout_ns))
+      return false;
+    tc_fence_after();
+    const float l448 = l_s[t * kBlockM + r];
+    const float inv = l448 > 0.0f ? __fdiv_rn(1.0f, l448) : 0.0f;
+    const uint32_t to = tbase + lane_off + 256 + t * DP;
+    if (p.out_tma != 0 && (!g.varlen || (qtile + 1) * kBlockM <= len_q)) {
+      constexpr int kBufs = DP == 128 ? 3 : 2;
+      uint8_t* const q_t = smem + L::kQOff + t * L::kQBytes;
+      uint8_t* const p_t = smem + L::kPOff + t * L::kPBytes;
+      for (int cc = 0; cc < DP / 32 && 32 * cc < D; ++cc) {
+        uint8_t* buf = cc % kBufs == kBufs - 1 ? p_t : q_t + (cc % kBufs) * 16384;
+        if (cc >= kBufs) {        // the store of chunk cc - kBufs must have read it
+          if (r == 0) {
+            bulk_wait_read<kBufs - 1>();
+            mbar_arrive(&epi_free[t]);
+          }
+          if (!wait_all(&epi_free[t], (cc - kBufs) & 1, abort_flag, p.status, p.timeout_ns))
+            return false;
+        }
+        uint4* row = reinterpret_cast<uint4*>(buf + r * 128);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {     // 16 columns at a time
+          uint32_t o[16];
+          tmem_ld16(to + 32 * cc + 16 * half, o);
+          tmem_ld_wait();
+          reg_fence(o);
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int c = 32 * cc + 16 * half + 4 * k4;
+            uint4 v;
+            v.x = __float_as_uint(__uint_as_float(o[4 * k4]) * sv_cache[c] * inv);
+            v.y = __float_as_uint(__uint_as_float(o[4 * k4 + 1]) * sv_cache[c + 1] * inv);
+            v.z = __float_as_uint(__uint_as_float(o[4 * k4 + 2]) * sv_cache[c + 2] * inv);
+            v.w = __float_as_uint(__uint_as_float(o[4 * k4 + 3]) * sv_cache[c + 3] * inv);
+            row[(4 * half + k4) ^ (r & 7)] = v;
+          }
+        }
+        fence_proxy_async_smem();
+        // every row of the chunk is staged (all threads wait, so none can
+        // arrive twice in one phase)
+        mbar_arrive(&epi_full[t]);
+        if (!wait_all(&epi_full[t], cc & 1, abort_flag, p.status, p.timeout_ns)) return false;
+        if (r == 0) {
+          const int32_t row0 = static_cast<int32_t>(qtile * kBlockM);
+          if (p.out_tma == 3)
+            tma_store_3d(&tm_o, buf, 32 * cc, static_cast<int32_t>(h),
+                         static_cast<int32_t>(qstart) + row0);
+          else if (p.out_tma == 1)
+            tma_store_4d(&tm_o, buf, 32 * cc, row0, static_cast<int32_t>(h),
+                         static_cast<int32_t>(s));
+          else
+            tma_store_4d(&tm_o, buf, 32 * cc, static_cast<int32_t>(h), row0,
+                         static_cast<int32_t>(s));
+          bulk_commit();
+          ++stores;
+        }
+      }
+      return true;
+    }
+    const bool vec = (D % 4 == 0) && ((reinterpret_cast<uintptr_t>(orow) & 15) == 0);
+#pragma unroll 1
+    for (int cc = 0; cc < DP / 16; ++cc) {
+      uint32_t o[16];
+      tmem_ld16(to + 16 * cc, o);
+      tmem_ld_wait();
+      reg_fence(o);
+      if (!valid) continue;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int c = 16 * cc + i;
+        if (vec && (i & 3) == 0 && c < D) {
+          float4 v4;
+          v4.x = __uint_as_float(o[i]) * sv_cache[c] * inv;
+          v4.y = __uint_as_float(o[i + 1]) * sv_cache[c + 1] * inv;
+          v4.z = __uint_as_float(o[i + 2]) * sv_cache[c + 2] * inv;
+          v4.w = __uint_as_float(o[i + 3]) * sv_cache[c + 3] * inv;
+          *reinterpret_cast<float4*>(orow + c) = v4;
+        } else if (!vec && c < D) {
+          orow[c] = __uint_as_float(o[i]) * sv_cache[c] * inv;
+        }
+      }
+    }
+    return true;
+  };
+
   if (wg == 3) {
     regs_decrease<kMiscRegs>();
     if (warp == 12 && lane == 0) {
@@ -347,8 +457,15 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
         mbar_wait(&drain[t], 0, nullptr, p.status, p.timeout_ns);
       }
     }
+    // tile 1's epilogue, alongside tile 0's on the correction warps (lanes
+    // without a role wait here for their lane 0 instead of spinning)
+    __syncwarp();
+    const int r3 = threadIdx.x - 3 * kBlockM;
+    int stores = 0;
+    epilogue(1, r3, static_cast<uint32_t>((warp & 3) * 32) << 16, stores);
+    if (r3 == 0 && stores > 0) bulk_wait_all();
   } else if (wg == 2) {
-    // ================================================ correction + epilogue
+    // ================================================ correction + tile 0's epilogue
     regs_decrease<kCorrRegs>();
     const int r = threadIdx.x - 256;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -403,117 +520,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
         mbar_arrive(&pv_ready[t]);
       }
     }
-    // epilogue: out = O * s_v / (448 l), the caller's D channels only
-    const int D = static_cast<int>(g.D);
     int stores = 0;                 // tensor stores issued (thread r == 0)
-    const int64_t seg_off = g.varlen ? qstart * p.out_tok_stride : s * p.out_seg_stride;
-    for (int t = 0; ok && t < 2; ++t) {
-      if ((qt0 + t) * kBlockM >= qlim) continue;
-      const int64_t qi = (qt0 + t) * kBlockM + r;
-      float* orow = p.out + seg_off + h * p.out_head_stride + qi * p.out_tok_stride;
-      if (n_t[t] == 0) {          // no visible key (empty key sequence): zeros
-        if (qi < len_q)
-          for (int c = 0; c < D; ++c) orow[c] = 0.0f;
-        continue;
-      }
-      ok = wait_all(&o_done[t], (n_t[t] - 1) & 1, abort_flag, p.status, p.timeout_ns) &&
-           wait_all(&l_ready[t], 0, abort_flag, p.status, p.timeout_ns);
-      if (!ok) break;
-      tc_fence_after();
-      const float l448 = l_s[t * kBlockM + r];
-      const float inv = l448 > 0.0f ? __fdiv_rn(1.0f, l448) : 0.0f;
-      const bool valid = qi < len_q;
-      const int64_t qtile = qt0 + t;
-      if (p.out_tma != 0 && (!g.varlen || (qtile + 1) * kBlockM <= len_q)) {
-        // tensor stores where their clipping is exact (dense outputs end at
-        // Lq; full tiles of a packed sequence), from staging chunks of 128
-        // rows x 32 fp32 in the 128-byte swizzle layout, held in Q_t and
-        // P~_t, which the tensor cores no longer read
-        constexpr int kBufs = DP == 128 ? 3 : 2;
-        uint8_t* const q_t = smem + L::kQOff + t * L::kQBytes;
-        uint8_t* const p_t = smem + L::kPOff + t * L::kPBytes;
-        const uint32_t to = tbase + lane_off + 256 + t * DP;
-        for (int cc = 0; ok && cc < DP / 32 && 32 * cc < D; ++cc) {
-          uint8_t* buf = cc % kBufs == kBufs - 1 ? p_t : q_t + (cc % kBufs) * 16384;
-          if (cc >= kBufs) {      // the store of chunk cc - kBufs must have read it
-            if (r == 0) {
-              bulk_wait_read<kBufs - 1>();
-              mbar_arrive(&epi_free[t]);
-            }
-            ok = wait_all(&epi_free[t], (cc - kBufs) & 1, abort_flag, p.status, p.timeout_ns);
-            if (!ok) break;
-          }
-          uint4* row = reinterpret_cast<uint4*>(buf + r * 128);
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {   // 16 columns at a time
-            uint32_t o[16];
-            tmem_ld16(to + 32 * cc + 16 * half, o);
-            tmem_ld_wait();
-            reg_fence(o);
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-              const int c = 32 * cc + 16 * half + 4 * k4;
-              uint4 v;
-              v.x = __float_as_uint(__uint_as_float(o[4 * k4]) * sv_cache[c] * inv);
-              v.y = __float_as_uint(__uint_as_float(o[4 * k4 + 1]) * sv_cache[c + 1] * inv);
-              v.z = __float_as_uint(__uint_as_float(o[4 * k4 + 2]) * sv_cache[c + 2] * inv);
-              v.w = __float_as_uint(__uint_as_float(o[4 * k4 + 3]) * sv_cache[c + 3] * inv);
-              row[(4 * half + k4) ^ (r & 7)] = v;
-            }
-          }
-          fence_proxy_async_smem();
-          // every row of the chunk is staged (all threads wait, so none can
-          // arrive twice in one phase)
-          mbar_arrive(&epi_full[t]);
-          ok = wait_all(&epi_full[t], cc & 1, abort_flag, p.status, p.timeout_ns);
-          if (!ok) break;
-          if (r == 0) {
-            const int32_t row0 = static_cast<int32_t>(qtile * kBlockM);
-            if (p.out_tma == 3)
-              tma_store_3d(&tm_o, buf, 32 * cc, static_cast<int32_t>(h),
-                           static_cast<int32_t>(qstart) + row0);
-            else if (p.out_tma == 1)
-              tma_store_4d(&tm_o, buf, 32 * cc, row0, static_cast<int32_t>(h),
-                           static_cast<int32_t>(s));
-            else
-              tma_store_4d(&tm_o, buf, 32 * cc, static_cast<int32_t>(h), row0,
-                           static_cast<int32_t>(s));
-            bulk_commit();
-            ++stores;
-          }
-        }
-        continue;
-      }
-      const bool vec = (D % 4 == 0) && ((reinterpret_cast<uintptr_t>(orow) & 15) == 0);
-#pragma unroll 1
-      for (int cc = 0; cc < DP / 32; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(tbase + lane_off + 256 + t * DP + 32 * cc, o);
-        tmem_ld_wait();
-        reg_fence(o);
-        if (!valid) continue;
-        if (vec) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const int c = 32 * cc + i;
-            if (c < D) {
-              float4 v4;
-              v4.x = __uint_as_float(o[i]) * sv_cache[c] * inv;
-              v4.y = __uint_as_float(o[i + 1]) * sv_cache[c + 1] * inv;
-              v4.z = __uint_as_float(o[i + 2]) * sv_cache[c + 2] * inv;
-              v4.w = __uint_as_float(o[i + 3]) * sv_cache[c + 3] * inv;
-              *reinterpret_cast<float4*>(orow + c) = v4;
-            }
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int c = 32 * cc + i;
-            if (c < D) orow[c] = __uint_as_float(o[i]) * sv_cache[c] * inv;
-          }
-        }
-      }
-    }
+    if (ok) ok = epilogue(0, r, lane_off, stores);
     // the tensor stores must be complete before the CTA ends
     if (r == 0 && stores > 0) bulk_wait_all();
   } else {
