@@ -71,8 +71,9 @@ struct Layout {
   static constexpr int kPOff = kVOff + kVStages * kVBytes;
   static constexpr int kBarOff = kPOff + 2 * kPBytes;
   // q_full, k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], then per tile:
-  // s_full, s_free, alpha_ready[2], pv_ready, o_done, l_ready, drain, epi_full, epi_free
-  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 * 10;
+  // s_full, s_free, alpha_ready[2], pv_ready, o_done, l_ready, drain, epi_full, epi_free;
+  // sv_ready
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 * 10 + 1;
   static constexpr int kAlphaOff = (kBarOff + kNumBars * 8 + 15) / 16 * 16;
   static constexpr int kLOff = kAlphaOff + 4 * kBlockM * 4;
   static constexpr int kSvOff = kLOff + 2 * kBlockM * 4;
@@ -195,24 +196,61 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
   // buffer has been read by its tensor store
   uint64_t* epi_full = drain + 2;             // [2]
   uint64_t* epi_free = epi_full + 2;          // [2]
+  uint64_t* sv_ready = epi_free + 2;          // the V scales are in shared memory
   float* alpha_s = reinterpret_cast<float*>(smem + L::kAlphaOff);   // [2][2][128]
   float* l_s = reinterpret_cast<float*>(smem + L::kLOff);           // [2][128]
   float* sv_cache = reinterpret_cast<float*>(smem + L::kSvOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
 
-  if (threadIdx.x == 0) {
-    *abort_flag = 0;
+  // The producers set up their own rings and issue the copies that need no
+  // free slot (Q, the first K and V tiles) at once, so those loads overlap
+  // the rest of the set-up.
+  const uint32_t active = n_t[1] > 0 ? 2u : 1u;   // query tiles reading K/V
+  int k_last = -1, v_last = -1;                    // last tile each producer issued
+  if (warp == 12 && lane == 0) {
     mbar_init(q_full, 1);
-    const uint32_t active = n_t[1] > 0 ? 2u : 1u;   // query tiles reading K/V
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], active);
     }
+    mbar_fence_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    if (n_max > 0) mbar_expect_tx(q_full, (n_t[1] > 0 ? 2 : 1) * L::kQBytes);
+    for (int t = 0; t < 2; ++t) {
+      if (n_t[t] == 0) continue;
+      for (int a = 0; a < DP / 64; ++a)
+        tma_load_2d(smem + L::kQOff + t * L::kQBytes + a * kAtomBytes, &tm_q, a * 64,
+                    static_cast<int32_t>(q_row0 + t * kBlockM), q_full);
+    }
+    for (int j = 0; j < n_max && j < kKStages; ++j) {
+      if (j == p.skip_kv_tile) continue;   // failure injection (tests only)
+      mbar_expect_tx(&k_full[j], L::kKBytes);
+      for (int a = 0; a < DP / 64; ++a)
+        tma_load_2d(smem + L::kKOff + j * L::kKBytes + a * kAtomBytes, &tm_k, a * 64,
+                    static_cast<int32_t>(k_row0 + j * kBlockN), &k_full[j]);
+      k_last = j;
+    }
+  }
+  if (warp == 14 && lane == 0) {
     for (int i = 0; i < kVStages; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], active);
     }
+    mbar_fence_init();
+    tma_prefetch_desc(&tm_v);
+    for (int j = 0; j < n_max && j < kVStages; ++j) {
+      mbar_expect_tx(&v_full[j], L::kVBytes);
+      tma_load_2d(smem + L::kVOff + j * L::kVBytes, &tm_v,
+                  static_cast<int32_t>(v_col0 + j * kBlockN), static_cast<int32_t>(v_row0),
+                  &v_full[j]);
+      v_last = j;
+    }
+  }
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(sv_ready, DP);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
       mbar_init(&s_free[t], kBlockM);
@@ -228,13 +266,6 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
     mbar_fence_init();
   }
   if (warp == 13) tmem_alloc(tmem_slot, kTmemCols);
-  if (threadIdx.x >= 256 && threadIdx.x < 256 + DP)
-    sv_cache[threadIdx.x - 256] = p.s_v[(s * g.Hkv + hk) * DP + (threadIdx.x - 256)];
-  if (warp == 12 && lane == 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -267,6 +298,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (!wait_all(&l_ready[t], 0, abort_flag, p.status, p.timeout_ns) ||
         !wait_all(&o_done[t], (n_t[t] - 1) & 1, abort_flag, p.status, p.timeout_ns))
       return false;
+    if (!wait_all(sv_ready, 0, abort_flag, p.status, p.timeout_ns)) return false;
     tc_fence_after();
     const float l448 = l_s[t * kBlockM + r];
     const float inv = l448 > 0.0f ? __fdiv_rn(1.0f, l448) : 0.0f;
@@ -354,16 +386,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
   if (wg == 3) {
     regs_decrease<kMiscRegs>();
     if (warp == 12 && lane == 0) {
-      // ============================================== TMA producer: Q and K
-      if (n_max > 0) mbar_expect_tx(q_full, (n_t[1] > 0 ? 2 : 1) * L::kQBytes);
-      for (int t = 0; t < 2; ++t) {
-        if (n_t[t] == 0) continue;
-        for (int a = 0; a < DP / 64; ++a)
-          tma_load_2d(smem + L::kQOff + t * L::kQBytes + a * kAtomBytes, &tm_q, a * 64,
-                      static_cast<int32_t>(q_row0 + t * kBlockM), q_full);
-      }
-      int last = -1;
-      for (int j = 0; j < n_max; ++j) {
+      // ============================================== TMA producer: K (Q and
+      // the first kKStages tiles went out during set-up)
+      int last = k_last;
+      for (int j = kKStages; j < n_max; ++j) {
         const int st = j % kKStages;
         if (j >= kKStages &&
             !mbar_wait(&k_empty[st], ((j / kKStages) - 1) & 1, abort_flag, p.status,
@@ -384,9 +410,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
           mbar_wait(&k_full[j % kKStages], (j / kKStages) & 1, nullptr, p.status,
                     p.timeout_ns);
     } else if (warp == 14 && lane == 0) {
-      // ============================================== TMA producer: V
-      int last = -1;
-      for (int j = 0; j < n_max; ++j) {
+      // ============================================== TMA producer: V (the
+      // first kVStages tiles went out during set-up)
+      int last = v_last;
+      for (int j = kVStages; j < n_max; ++j) {
         const int st = j % kVStages;
         if (j >= kVStages &&
             !mbar_wait(&v_empty[st], ((j / kVStages) - 1) & 1, abort_flag, p.status,
@@ -469,6 +496,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
     regs_decrease<kCorrRegs>();
     const int r = threadIdx.x - 256;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    if (r < DP) {             // the V scales for the epilogue, off the set-up path
+      sv_cache[r] = p.s_v[(s * g.Hkv + hk) * DP + r];
+      mbar_arrive(sv_ready);
+    }
     bool ok = true;
     for (int j = 0; ok && j < n_max; ++j) {
       for (int t = 0; t < 2; ++t) {
