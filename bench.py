@@ -37,7 +37,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per attention-kernel launch on the default
 # workload, from the ncu capture summarised in
 # profiles/attn_kernel_b2_h24_l4096_d128.md (None for other workloads).
-ATTN_NCU_DRAM_BYTES = {"b2_h24_l4096_d128": 126.747136e6 + 58.950656e6}
+ATTN_NCU_DRAM_BYTES = {"b2_h24_l4096_d128": 126.746624e6 + 60.900096e6}
 
 
 def load_peaks():
