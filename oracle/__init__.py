@@ -71,6 +71,13 @@ def lib():
                                             I, ctypes.c_double, I64, I64, I64,
                                             I64, P, I]
             L.oracle_attn_exact.restype = I
+            L.oracle_fp16_encode.argtypes = [ctypes.c_float]
+            L.oracle_fp16_encode.restype = ctypes.c_uint16
+            L.oracle_v16.argtypes = [P, I, I64, I64, I64, P]
+            L.oracle_v16.restype = I
+            L.oracle_attn_pv16.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64,
+                                           I, ctypes.c_float, I64, I64, I64, I64, P, I]
+            L.oracle_attn_pv16.restype = I
             _lib = L
     return _lib
 
@@ -149,6 +156,44 @@ def attn(pro: dict, causal: bool, sm_scale: float, heads=None, rows=None,
         _ptr(out), nthreads)
     if rc:
         raise ValueError(f"oracle_attn failed ({rc})")
+    return out
+
+
+def fp16_encode(x) -> np.ndarray:
+    """fp32 -> IEEE binary16 bits, round to nearest even (scalar loop: tests)."""
+    x = np.asarray(x, dtype=np.float32)
+    L = lib()
+    flat = [L.oracle_fp16_encode(float(v)) for v in x.ravel()]
+    return np.array(flat, dtype=np.uint16).reshape(x.shape)
+
+
+def v16(v, dtype: int) -> np.ndarray:
+    """V of one segment ([Hkv,Lk,D] input bits) rounded to fp16, padded to Dp:
+    [Hkv,Lk,Dp] binary16 bits (the FP16-PV variant's V operand)."""
+    v = np.ascontiguousarray(v, dtype=np.uint16)
+    Hkv, Lk, D = v.shape
+    out = np.zeros((Hkv, Lk, padded_dim(D)), dtype=np.uint16)
+    rc = lib().oracle_v16(_ptr(v), dtype, Hkv, Lk, D, _ptr(out))
+    if rc:
+        raise ValueError(f"oracle_v16 failed ({rc})")
+    return out
+
+
+def attn_pv16(pro: dict, v16_bits: np.ndarray, causal: bool, sm_scale: float, heads=None,
+              rows=None, nthreads: int = 0) -> np.ndarray:
+    """FP16-PV variant from the prologue's Q/K operands and fp16 V; [Hq,Lq,D]
+    fp32 (rows outside ``heads``/``rows`` stay NaN)."""
+    Hq, Lq, D = pro["Hq"], pro["Lq"], pro["D"]
+    h0, h1 = heads if heads is not None else (0, Hq)
+    r0, r1 = rows if rows is not None else (0, Lq)
+    v16_bits = np.ascontiguousarray(v16_bits, dtype=np.uint16)
+    out = np.full((Hq, Lq, D), np.nan, dtype=np.float32)
+    rc = lib().oracle_attn_pv16(
+        _ptr(pro["q8"]), _ptr(pro["s_q"]), _ptr(pro["k8"]), _ptr(pro["s_k"]),
+        _ptr(v16_bits), Hq, pro["Hkv"], Lq, pro["Lk"], D, int(bool(causal)),
+        float(np.float32(sm_scale)), h0, h1, r0, r1, _ptr(out), nthreads)
+    if rc:
+        raise ValueError(f"oracle_attn_pv16 failed ({rc})")
     return out
 
 

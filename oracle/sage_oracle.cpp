@@ -112,6 +112,32 @@ uint8_t e4m3_encode(float x) {
   return sign | static_cast<uint8_t>(code);
 }
 
+// ------------------------------------------------------------------ fp16
+// IEEE binary16: sign, 5 exponent bits (bias 15), 10 mantissa bits; largest
+// finite 65504, subnormals m * 2^-24.  Round to nearest, ties to even;
+// magnitudes from 65520 (the tie above 65504) round to infinity.
+uint16_t fp16_encode(float x) {
+  const uint16_t sign = std::signbit(x) ? 0x8000 : 0;
+  if (std::isnan(x)) return 0x7E00;
+  const double a = std::fabs(static_cast<double>(x));
+  if (a >= 65520.0) return sign | 0x7C00;
+  if (a == 0.0) return sign;
+  int E;
+  std::frexp(a, &E);                       // a = f * 2^E, f in [0.5, 1)
+  const int e = std::max(E - 1, -14);      // binade exponent, subnormals below 2^-14
+  const double ulp = std::ldexp(1.0, e - 10);
+  const double r = std::nearbyint(a / ulp);   // exact quotient, ties to even
+  const double v = r * ulp;
+  if (v >= 65520.0) return sign | 0x7C00;
+  if (v < std::ldexp(1.0, -14))            // subnormal: m * 2^-24
+    return sign | static_cast<uint16_t>(std::ldexp(v, 24));
+  int Ev;
+  const double f = std::frexp(v, &Ev);     // v = f * 2^Ev
+  const int biased = Ev - 1 + 15;
+  const uint16_t mant = static_cast<uint16_t>((f * 2.0 - 1.0) * 1024.0);
+  return sign | static_cast<uint16_t>(biased << 10) | mant;
+}
+
 // ------------------------------------------------------------ quantisers
 int8_t int8_code(float x, float inv) {
   float r = std::nearbyint(x * inv);
@@ -177,6 +203,7 @@ extern "C" {
 int oracle_padded_dim(int64_t D) { return static_cast<int>(padded_dim(D)); }
 
 uint8_t oracle_e4m3_encode(float x) { return e4m3_encode(x); }
+uint16_t oracle_fp16_encode(float x) { return fp16_encode(x); }
 float oracle_e4m3_value(uint8_t code) { return e4m3_value(code); }
 
 void oracle_e4m3_encode_array(const float* x, uint8_t* out, int64_t n) {
@@ -350,6 +377,83 @@ int oracle_attn(const int8_t* q8, const float* s_q, const int8_t* k8,
     float* o = &out[(h * Lq + i) * D];
     for (int64_t d = 0; d < D; ++d)
       o[d] = l > 0.0f ? (O[d] * s_v[hk * Dp + d]) / (kFp8Max * l) : 0.0f;
+  });
+  return 0;
+}
+
+// V for the FP16-PV variant ([OV] API list: "INT8 QK^T, FP16 PV"): each
+// input value rounded to fp16 (exact for fp16 inputs), channels padded to Dp
+// with zeros.  v16 is [Hkv][Lk][Dp] binary16 bits.
+int oracle_v16(const uint16_t* v, int dtype, int64_t Hkv, int64_t Lk, int64_t D,
+               uint16_t* v16) {
+  if (D < 1 || D > 128) return 2;
+  const int64_t Dp = padded_dim(D);
+  for (int64_t h = 0; h < Hkv; ++h)
+    for (int64_t t = 0; t < Lk; ++t)
+      for (int64_t c = 0; c < Dp; ++c)
+        v16[(h * Lk + t) * Dp + c] =
+            c < D ? fp16_encode(decode_in(v[(h * Lk + t) * D + c], dtype)) : 0;
+  return 0;
+}
+
+// FP16-PV variant of the quantised attention: the same INT8 QK^T, dequant,
+// masking and online softmax as oracle_attn, then P~ = fp16(P) (no 448
+// scaling), O accumulates P~ * V16 in fp32 per 128-key tile, and the output
+// is O / l for the first D channels (a row with no visible key outputs zeros).
+int oracle_attn_pv16(const int8_t* q8, const float* s_q, const int8_t* k8,
+                     const float* s_k, const uint16_t* v16, int64_t Hq, int64_t Hkv,
+                     int64_t Lq, int64_t Lk, int64_t D, int causal, float sm_scale,
+                     int64_t h0, int64_t h1, int64_t r0, int64_t r1, float* out,
+                     int nthreads) {
+  if (D < 1 || D > 128 || Hq % Hkv) return 2;
+  const int64_t Dp = padded_dim(D);
+  const int64_t group = Hq / Hkv;
+  const int64_t nkb = (Lk + kKeyBlock - 1) / kKeyBlock;
+  const float scale_log2 = sm_scale * kLog2e;
+  const int64_t nrows = r1 - r0;
+  parallel_for((h1 - h0) * nrows, nthreads, [&](int64_t it) {
+    const int64_t h = h0 + it / nrows;
+    const int64_t i = r0 + it % nrows;
+    const int64_t hk = h / group;
+    const int8_t* qi = &q8[(h * Lq + i) * Dp];
+    const float sq = s_q[h * Lq + i];
+    float m = -INFINITY, l = 0.0f;
+    std::vector<float> O(Dp, 0.0f), x(kKeyBlock), acc(Dp), pt(kKeyBlock);
+    for (int64_t b = 0; b < nkb; ++b) {
+      const int64_t j0 = b * kKeyBlock, j1 = std::min(Lk, j0 + kKeyBlock);
+      const float c = (sq * s_k[hk * nkb + b]) * scale_log2;
+      float mt = -INFINITY;
+      bool visible = false;
+      for (int64_t j = j0; j < j1; ++j) {
+        if (causal && j > i) { x[j - j0] = -INFINITY; continue; }
+        const int8_t* kj = &k8[(hk * Lk + j) * Dp];
+        int32_t S = 0;
+        for (int64_t d = 0; d < Dp; ++d)
+          S += static_cast<int32_t>(qi[d]) * static_cast<int32_t>(kj[d]);
+        x[j - j0] = static_cast<float>(S) * c;
+        mt = std::max(mt, x[j - j0]);
+        visible = true;
+      }
+      if (!visible) continue;
+      const float m_new = std::max(m, mt);
+      const float alpha = std::exp2(m - m_new);
+      float psum = 0.0f;
+      for (int64_t j = j0; j < j1; ++j) {
+        const float p = std::exp2(x[j - j0] - m_new);
+        psum += p;
+        pt[j - j0] = decode_f16(fp16_encode(p));
+      }
+      l = l * alpha + psum;
+      for (int64_t d = 0; d < Dp; ++d) acc[d] = 0.0f;
+      for (int64_t j = j0; j < j1; ++j) {
+        const uint16_t* vj = &v16[(hk * Lk + j) * Dp];
+        for (int64_t d = 0; d < Dp; ++d) acc[d] += pt[j - j0] * decode_f16(vj[d]);
+      }
+      for (int64_t d = 0; d < Dp; ++d) O[d] = O[d] * alpha + acc[d];
+      m = m_new;
+    }
+    float* o = &out[(h * Lq + i) * D];
+    for (int64_t d = 0; d < D; ++d) o[d] = l > 0.0f ? O[d] / l : 0.0f;
   });
   return 0;
 }

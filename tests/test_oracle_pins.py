@@ -399,3 +399,111 @@ def test_large_magnitude_causal_inputs_stay_finite(orc):
     p = orc.prologue(q, k, v, wl.BF16)
     out = orc.attn(p, True, 0.125)
     assert np.all(np.isfinite(out))
+
+
+# ------------------------------------------------- FP16-PV variant (NEXT-3)
+def test_fp16_encode_matches_ieee_library(orc):
+    """fp32 -> binary16, ties to even, overflow at 65520: bit-equal to numpy's
+    IEEE conversion over normals, subnormals, exact ties and overflow."""
+    rng = np.random.default_rng(61)
+    mags = np.exp2(rng.uniform(-30.0, 17.0, 20000)).astype(np.float32)
+    x = np.where(rng.random(20000) < 0.5, -mags, mags).astype(np.float32)
+    # exact ties halfway between consecutive fp16 values (normal and subnormal)
+    h = rng.integers(1, 0x7BFF, 2000).astype(np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).view(np.float16).astype(np.float64)
+    ties = ((lo + hi) / 2).astype(np.float32)
+    edge = np.array([0.0, -0.0, 65504.0, 65519.996, 65520.0, 1e6, 2.0 ** -24, 2.0 ** -25,
+                     3 * 2.0 ** -26, 2.0 ** -14, np.float32(2.0 ** -14) * np.float32(0.999)],
+                    dtype=np.float32)
+    for arr in (x, ties, edge):
+        np.testing.assert_array_equal(orc.fp16_encode(arr), arr.astype(np.float16).view(np.uint16))
+
+
+def _pv16_case(orc, q, k, v, dtype, causal, scale):
+    p = orc.prologue(q, k, v, dtype)
+    v16 = orc.v16(v, dtype)
+    return p, v16, orc.attn_pv16(p, v16, causal, scale)
+
+
+def test_pv16_single_key_returns_fp16_v(orc):
+    """Lk = 1: P = 1 exactly (fp16 1.0), l = 1, so the output is fp16(v) exactly."""
+    rng = np.random.default_rng(62)
+    q = _rand_bits(rng, (2, 5, 64), wl.BF16)
+    k = _rand_bits(rng, (2, 1, 64), wl.BF16)
+    v = _rand_bits(rng, (2, 1, 64), wl.BF16, scale=3.0)
+    _, v16, got = _pv16_case(orc, q, k, v, wl.BF16, False, 0.125)
+    ref = v16[:, 0, :].view(np.float16).astype(np.float32)
+    for h in range(2):
+        np.testing.assert_array_equal(got[h], np.broadcast_to(ref[h], (5, 64)))
+
+
+def test_pv16_uniform_scores_average_fp16_v(orc):
+    """Zero queries: every score is 0, P = 1 for every key, output = token mean
+    of fp16(v) (up to fp32 summation rounding)."""
+    rng = np.random.default_rng(63)
+    L, D = 300, 80
+    q = np.zeros((1, 6, D), dtype=np.uint16)
+    k = _rand_bits(rng, (1, L, D), wl.F16)
+    v = _rand_bits(rng, (1, L, D), wl.F16)
+    _, v16, got = _pv16_case(orc, q, k, v, wl.F16, False, 0.1)
+    ref = v16[0, :, :D].view(np.float16).astype(np.float64).mean(axis=0)
+    np.testing.assert_allclose(got[0], np.broadcast_to(ref, (6, D)), rtol=1e-5, atol=1e-6)
+
+
+def test_pv16_causal_first_row_sees_first_key_only(orc):
+    rng = np.random.default_rng(64)
+    q, k, v = (_rand_bits(rng, (2, 200, 64), wl.F16) for _ in range(3))
+    _, v16, got = _pv16_case(orc, q, k, v, wl.F16, True, 0.125)
+    np.testing.assert_array_equal(got[:, 0, :], v16[:, 0, :].view(np.float16).astype(np.float32))
+
+
+@pytest.mark.parametrize("causal,Hq,Hkv,Lq,Lk,D,dtype", [
+    (False, 2, 2, 200, 700, 64, wl.F16),
+    (True, 4, 2, 300, 300, 128, wl.BF16),
+    (False, 4, 1, 130, 513, 40, wl.F16),
+    (True, 2, 2, 512, 1024, 128, wl.F16),
+])
+def test_pv16_accuracy_matches_the_pages_table(orc, causal, Hq, Hkv, Lq, Lk, D, dtype):
+    """The SageAttention 2.2.0 sm_120a wheel page's accuracy table on N(0,1)
+    inputs against float64 attention: the FP16-PV backend has rel_l2 0.0092 to
+    0.0112 and cosine >= 0.99994, the FP8-PV backend rel_l2 0.0345 to 0.0381,
+    i.e. about 3.7x more error.  The oracle lands in those ranges."""
+    rng = np.random.default_rng(71 + D + Lk)
+    q = _rand_bits(rng, (Hq, Lq, D), dtype)
+    k = _rand_bits(rng, (Hkv, Lk, D), dtype)
+    v = _rand_bits(rng, (Hkv, Lk, D), dtype)
+    scale = 1.0 / math.sqrt(D)
+    p, v16, got16 = _pv16_case(orc, q, k, v, dtype, causal, scale)
+    got8 = orc.attn(p, causal, scale)
+    ref = orc.attn_exact(q, k, v, dtype, causal, scale)
+    r16, r8 = _rel_l2(got16, ref), _rel_l2(got8, ref)
+    assert 0.008 <= r16 <= 0.0118, r16
+    assert 0.030 <= r8 <= 0.040, r8
+    assert r8 / r16 >= 2.5, (r8, r16)
+    assert _cos(got16, ref) >= 0.99993, _cos(got16, ref)
+    assert np.all(np.isfinite(got16))
+
+
+def test_pv16_rounds_p_to_fp16_brute_force(orc):
+    """One key tile restated in numpy from the prologue's codes: P = exp2(x - m)
+    in fp32, rounded to fp16, O = sum fp16(P) v16, out = O / sum P.  The
+    unrounded-P formula differs by far more than the tolerance, so the test
+    would catch a dropped rounding."""
+    rng = np.random.default_rng(65)
+    Lk, D = 100, 64
+    q = _rand_bits(rng, (1, 4, D), wl.F16, scale=2.0)
+    k = _rand_bits(rng, (1, Lk, D), wl.F16, scale=2.0)
+    v = _rand_bits(rng, (1, Lk, D), wl.F16, scale=4.0)
+    scale = 0.125
+    p, v16, got = _pv16_case(orc, q, k, v, wl.F16, False, scale)
+    S = p["q8"][0].astype(np.int64) @ p["k8"][0].astype(np.int64).T          # [4, Lk]
+    c = (p["s_q"][0][:, None] * p["s_k"][0][0]).astype(np.float32) * np.float32(scale * math.log2(math.e))
+    x = S.astype(np.float32) * c.astype(np.float32)
+    P = np.exp2((x - x.max(axis=1, keepdims=True)).astype(np.float32)).astype(np.float32)
+    V = v16[0, :, :D].view(np.float16).astype(np.float64)
+    l = P.astype(np.float64).sum(axis=1, keepdims=True)
+    ref = (P.astype(np.float16).astype(np.float64) @ V) / l
+    unrounded = (P.astype(np.float64) @ V) / l
+    np.testing.assert_allclose(got[0], ref, rtol=2e-5, atol=2e-6)
+    assert np.max(np.abs(unrounded - ref)) > 20 * 2e-6
