@@ -152,14 +152,20 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int):
     stream = torch.cuda.current_stream()
     scale = wl.default_sm_scale(w)
 
+    pv16 = args.variant == "pv16"
+
     def fwd():
         if w.varlen:
             sage.attn_fwd_varlen(d["q"], d["k"], d["v"], out, d["cu_q"], d["cu_k"],
                                  max(w.seqlens_q), max(w.seqlens_k), w.causal, scale, ws=ws)
+        elif pv16:
+            sage.attn_fwd_pv16(d["q"], d["k"], d["v"], out, w.layout, w.causal, scale, ws=ws)
         else:
             sage.attn_fwd(d["q"], d["k"], d["v"], out, w.layout, w.causal, scale, ws=ws)
 
     def prologue():
+        if pv16:
+            return sage.quant_prologue_pv16(d["q"], d["k"], d["v"], w.layout, ws=ws)
         if w.varlen:
             return sage.quant_prologue_varlen(d["q"], d["k"], d["v"], d["cu_q"], d["cu_k"],
                                               max(w.seqlens_q), max(w.seqlens_k), ws=ws)
@@ -355,6 +361,8 @@ def main():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="sage", choices=["sage", "reference"])
+    ap.add_argument("--variant", default="fp8", choices=["fp8", "pv16"],
+                    help="fp8: INT8 QK^T + FP8 PV (default); pv16: INT8 QK^T + FP16 PV")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--ref-rows", type=int, default=512)
     ap.add_argument("--cpu-rows", type=int, default=4096)
@@ -378,7 +386,9 @@ def main():
     # attention kernel roofline: QK^T on the 16-bit tensor pipe (exact int8
     # emulation) and PV on the FP8 pipe (2x rate) => ceiling 4/3 x bf16 peak
     bf16 = peaks["bf16_tflops"]
-    mix_peak = bf16 * 4.0 / 3.0
+    pv16 = args.variant == "pv16"
+    # the FP16-PV variant runs both products on the 16-bit pipe
+    mix_peak = bf16 if pv16 else bf16 * 4.0 / 3.0
     fp8_peak = bf16 * 2.0
     fig = job_figures(r, world, args.steps)
     # the kernel's algorithmic work: padded head dimension, masked tiles of a
@@ -393,14 +403,17 @@ def main():
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": r["total_ms"] / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "int8+e4m3 (fp32 softmax/accumulate)", "data": "synthetic",
-        "config": config_of(w),
+        "dtype": ("int8+fp16 (fp32 softmax/accumulate)" if pv16 else
+                  "int8+e4m3 (fp32 softmax/accumulate)"), "data": "synthetic",
+        "config": dict(config_of(w), variant=args.variant),
         "roofline": {"bound": "tensor", "achieved": att_tflops, "peak": mix_peak,
                      "unit": "TFLOP/s", "frac": att_tflops / mix_peak,
-                     "traffic": ATTN_NCU_DRAM_BYTES.get(w.name),
+                     "traffic": None if pv16 else ATTN_NCU_DRAM_BYTES.get(w.name),
                      "kernel": "attn_kernel (fused QK^T/softmax/PV)",
-                     "peak_note": f"4/3 x {src} bf16 burst {bf16} (QK^T at the 16-bit "
-                                  "rate, PV at the FP8 rate)",
+                     "peak_note": (f"{src} bf16 burst {bf16} (QK^T and the fp16 PV at the "
+                                   "16-bit rate)" if pv16 else
+                                   f"4/3 x {src} bf16 burst {bf16} (QK^T at the 16-bit "
+                                   "rate, PV at the FP8 rate)"),
                      "fp8_peak": fp8_peak, "frac_of_fp8_peak": att_tflops / fp8_peak},
         "ops_per_step": {"literal": r["ops"], "padded_d": r["ops_padded"],
                          "causal_effective": r["ops_effective"],

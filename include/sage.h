@@ -14,8 +14,10 @@
  *   [RM] SageAttention README translation, usage section (q, k, v fp16/bf16,
  *        tensor_layout "HND" (B,H,L,D) or "NHD" (B,L,H,D), is_causal).
  *   [RD] SageAttention-RDNA4 releases, v0.4.0 (hand-written prologue, key
- *        mean summed in fp64, 64-bit offsets) and v0.3.0 (a refusal carries
- *        its reason).
+ *        mean summed in fp64, 64-bit offsets) and v0.3.0 (fused q/k/v views;
+ *        a refusal carries its reason).
+ *   [WH] SageAttention 2.2.0 sm_120a wheel page, accuracy section (the
+ *        backends' errors against float64 attention).
  *
  * Conventions shared by every call:
  *  - All tensor pointers are DEVICE pointers of the current CUDA device and
@@ -24,7 +26,8 @@
  *  - Arguments are validated on the host before anything is enqueued; a bad
  *    argument returns an error and launches nothing.  The reason is kept in
  *    a thread-local string returned by sage_last_error().
- *  - Inputs q, k, v are fp16 or bf16, densely packed (no strided views).
+ *  - Inputs q, k, v are fp16 or bf16, densely packed (the *_strided calls
+ *    also take views with their own strides).
  *    Dense calls take HND (B,H,L,D) or NHD (B,L,H,D); varlen calls take
  *    packed (T,H,D) with int32 cumulative sequence offsets.
  *  - The output is fp32 in the same layout as q, with the caller's D
@@ -99,6 +102,7 @@ typedef struct {
   float* k_mean;
   void* stats;                      /* per-channel accumulators          */
   uint32_t* status;                 /* device status word (workspace+0)  */
+  int32_t v_fp16;                   /* 1: v8 holds fp16 V (FP16-PV), no s_v */
 } sage_quantized;
 
 /* Workspace bytes for a dense call (HND or NHD).  Returns 0 for invalid
@@ -154,6 +158,19 @@ SAGE_API sage_status sage_quant_prologue_strided(
     const int64_t* kv_strides, void* ws, size_t ws_bytes, sage_quantized* qt,
     sage_stream_t stream);
 
+/* FP16-PV prologue ([OV] API list, sageattn_qk_int8_pv_fp16_cuda: INT8
+ * QK^T, FP16 PV; [WH] accuracy table: the most accurate backend).  As
+ * sage_quant_prologue, except that V is kept in fp16 instead of e4m3: each
+ * value rounded to nearest even (exact for fp16 inputs), no per-channel
+ * scale, stored channel-major like the e4m3 V (2 bytes per element; the
+ * workspace of sage_workspace_bytes has room for it).  Sets qt->v_fp16 = 1,
+ * which makes sage_attn_quantized run the FP16-PV kernel.  Dense inputs. */
+SAGE_API sage_status sage_quant_prologue_pv16(const void* q, const void* k, const void* v,
+                                     int dtype, int layout, int64_t B, int64_t Hq,
+                                     int64_t Hkv, int64_t Lq, int64_t Lk, int64_t D,
+                                     void* ws, size_t ws_bytes, sage_quantized* qt,
+                                     sage_stream_t stream);
+
 /* Fused attention on quantised operands ([SD] kernel table: INT8 QK^T,
  * FP8 PV with an fp32 accumulator; [OV] Core features): per 128x128 tile,
  * exact integer S = q8 k8^T on the tensor cores, logits S*s_q*s_k*sm_scale
@@ -161,6 +178,9 @@ SAGE_API sage_status sage_quant_prologue_strided(
  * 448*P, O += P~ V~ accumulated in fp32 tensor memory, and
  * out = O * s_v / (448 * l) in fp32.  `layout` is the dense output layout
  * (ignored for varlen, which writes packed (total_q,Hq,D)). */
+/* (With qt->v_fp16 set, the FP16-PV kernel runs instead: the same INT8
+ * QK^T and online softmax, P~ = fp16(P) without the 448 scaling, O += P~ V16
+ * in fp32 tensor memory, out = O / l.) */
 SAGE_API sage_status sage_attn_quantized(const sage_quantized* qt, float* out,
                                 int layout, int is_causal, float sm_scale,
                                 sage_stream_t stream);
@@ -171,6 +191,14 @@ SAGE_API sage_status sage_attn_fwd(const void* q, const void* k, const void* v,
                           int64_t Lq, int64_t Lk, int64_t D, int layout,
                           int is_causal, float sm_scale, int dtype, void* ws,
                           size_t ws_bytes, sage_stream_t stream);
+
+/* Prologue + FP16-PV attention in one call (dense; see
+ * sage_quant_prologue_pv16). */
+SAGE_API sage_status sage_attn_fwd_pv16(const void* q, const void* k, const void* v,
+                               float* out, int64_t B, int64_t Hq, int64_t Hkv,
+                               int64_t Lq, int64_t Lk, int64_t D, int layout,
+                               int is_causal, float sm_scale, int dtype, void* ws,
+                               size_t ws_bytes, sage_stream_t stream);
 
 /* Prologue + attention in one call on strided views (see
  * sage_quant_prologue_strided); out is dense fp32 in `layout`. */

@@ -87,7 +87,7 @@ WsLayout ws_layout(const SegGeo& g) {
   w.s_k = o; o = align256(o + (k_rows / 128) * 4);
   w.q16 = o; o = align256(o + q_rows * g.Dp * 2);
   w.k16 = o; o = align256(o + k_rows * g.Dp * 2);
-  w.v8 = o; o = align256(o + v_rows * g.v_cols);
+  w.v8 = o; o = align256(o + v_rows * g.v_cols * 2);   // e4m3, or fp16 (FP16-PV)
   w.total = o;
   return w;
 }
@@ -244,8 +244,11 @@ sage_status make_maps(const sage_quantized* qt, AttnMaps* maps) {
                  qt->Dp * 2, 64, 128) ||
       !encode_2d(&maps->k, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qt->k16, qt->Dp, qt->k_rows,
                  qt->Dp * 2, 64, 128) ||
-      !encode_2d(&maps->v, CU_TENSOR_MAP_DATA_TYPE_UINT8, qt->v8, qt->v_cols, qt->v_rows,
-                 qt->v_cols, 128, static_cast<uint32_t>(qt->Dp)))
+      !(qt->v_fp16
+            ? encode_2d(&maps->v, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qt->v8, qt->v_cols,
+                        qt->v_rows, qt->v_cols * 2, 64, static_cast<uint32_t>(qt->Dp))
+            : encode_2d(&maps->v, CU_TENSOR_MAP_DATA_TYPE_UINT8, qt->v8, qt->v_cols,
+                        qt->v_rows, qt->v_cols, 128, static_cast<uint32_t>(qt->Dp))))
     return fail(SAGE_ERR_CUDA, "cuTensorMapEncodeTiled failed or unavailable");
   return SAGE_OK;
 }
@@ -283,7 +286,7 @@ void fill_quantized(const SegGeo& g, const WsLayout& w, uint8_t* ws, sage_quanti
 // Shared tail of both prologue entry points (arguments already validated).
 sage_status run_prologue(const SegGeo& g, const void* q, const void* k, const void* v,
                          void* ws, size_t ws_bytes, sage_quantized* qt,
-                         cudaStream_t st) {
+                         cudaStream_t st, bool v16 = false) {
   const WsLayout w = ws_layout(g);
   if (ws == nullptr || !aligned(ws, 256))
     return fail(SAGE_ERR_WORKSPACE, "workspace must be a 256-byte aligned device pointer");
@@ -297,6 +300,7 @@ sage_status run_prologue(const SegGeo& g, const void* q, const void* k, const vo
   if (s != SAGE_OK) return s;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   fill_quantized(g, w, wsb, qt);
+  qt->v_fp16 = v16 ? 1 : 0;
   cudaError_t e = cudaMemsetAsync(wsb, 0, w.zero_end, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
   PrologueBuffers b{};
@@ -322,6 +326,7 @@ sage_status run_prologue(const SegGeo& g, const void* q, const void* k, const vo
                    g.q_seg_stride % 8 == 0 && g.q_head_stride % 8 == 0 &&
                    g.q_tok_stride % 8 == 0 && g.k_seg_stride % 8 == 0 &&
                    g.k_head_stride % 8 == 0 && g.k_tok_stride % 8 == 0;
+  b.v16 = v16 ? 1 : 0;
   e = launch_prologue(g, b, vec, st);
   if (e != cudaSuccess) return cuda_fail(e, "prologue launch");
   return ok();
@@ -393,6 +398,7 @@ sage_status launch_attn(const sage_quantized* qt, float* out, int layout, int is
                      CU_TENSOR_MAP_SWIZZLE_128B))
       p.out_tma = kind;
   }
+  p.v16 = qt->v_fp16;
   p.skip_kv_tile = g_skip_kv_tile.load();
   p.timeout_ns = wait_timeout_ns();
   p.status = qt->status;
@@ -443,6 +449,26 @@ sage_status sage_quant_prologue(const void* q, const void* k, const void* v, int
     return fail(SAGE_ERR_INVALID_ARG, "the prologue needs B, Lq and Lk > 0");
   return run_prologue(dense_geo(B, Hq, Hkv, Lq, Lk, D, dtype, layout), q, k, v, ws,
                       ws_bytes, qt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sage_status sage_quant_prologue_pv16(const void* q, const void* k, const void* v, int dtype,
+                                     int layout, int64_t B, int64_t Hq, int64_t Hkv,
+                                     int64_t Lq, int64_t Lk, int64_t D, void* ws,
+                                     size_t ws_bytes, sage_quantized* qt,
+                                     sage_stream_t stream) {
+  if (qt == nullptr) return fail(SAGE_ERR_INVALID_ARG, "qt must not be null");
+  sage_status s = SAGE_OK;
+  if (layout != SAGE_HND && layout != SAGE_NHD)
+    return fail(SAGE_ERR_INVALID_ARG, "layout %d is neither SAGE_HND nor SAGE_NHD", layout);
+  if (B < 0 || Lq < 0 || Lk < 0)
+    return fail(SAGE_ERR_INVALID_ARG, "negative size (B=%lld Lq=%lld Lk=%lld)",
+                (long long)B, (long long)Lq, (long long)Lk);
+  if (!check_dims(Hq, Hkv, D, &s)) return s;
+  if ((s = check_common(q, k, v, dtype)) != SAGE_OK) return s;
+  if (B == 0 || Lq == 0 || Lk == 0)
+    return fail(SAGE_ERR_INVALID_ARG, "the prologue needs B, Lq and Lk > 0");
+  return run_prologue(dense_geo(B, Hq, Hkv, Lq, Lk, D, dtype, layout), q, k, v, ws,
+                      ws_bytes, qt, reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 sage_status sage_quant_prologue_varlen(const void* q, const void* k, const void* v,
@@ -531,6 +557,36 @@ sage_status sage_attn_fwd(const void* q, const void* k, const void* v, float* ou
   sage_quantized qt;
   s = run_prologue(dense_geo(B, Hq, Hkv, Lq, Lk, D, dtype, layout), q, k, v, ws, ws_bytes,
                    &qt, st);
+  if (s != SAGE_OK) return s;
+  if (qt.nseg > 65535 || qt.Hq > 65535)
+    return fail(SAGE_ERR_UNSUPPORTED, "more than 65535 segments or heads");
+  return launch_attn(&qt, out, layout, is_causal, sm_scale, st);
+}
+
+sage_status sage_attn_fwd_pv16(const void* q, const void* k, const void* v, float* out,
+                               int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk,
+                               int64_t D, int layout, int is_causal, float sm_scale,
+                               int dtype, void* ws, size_t ws_bytes, sage_stream_t stream) {
+  sage_status s = SAGE_OK;
+  if (layout != SAGE_HND && layout != SAGE_NHD)
+    return fail(SAGE_ERR_INVALID_ARG, "layout %d is neither SAGE_HND nor SAGE_NHD", layout);
+  if (B < 0 || Lq < 0 || Lk < 0)
+    return fail(SAGE_ERR_INVALID_ARG, "negative size (B=%lld Lq=%lld Lk=%lld)",
+                (long long)B, (long long)Lq, (long long)Lk);
+  if (!check_dims(Hq, Hkv, D, &s)) return s;
+  if (B == 0 || Lq == 0) return ok();                 // nothing to compute
+  if ((s = check_common(q, Lk == 0 ? q : k, Lk == 0 ? q : v, dtype)) != SAGE_OK) return s;
+  if (out == nullptr || !aligned(out, 4))
+    return fail(SAGE_ERR_INVALID_ARG, "out must be a 4-byte aligned device pointer");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (Lk == 0) {                                      // empty softmax: zeros
+    if ((s = check_device()) != SAGE_OK) return s;
+    cudaError_t e = cudaMemsetAsync(out, 0, out_elems_dense(B, Hq, Lq, D) * 4, st);
+    return e == cudaSuccess ? ok() : cuda_fail(e, "cudaMemsetAsync");
+  }
+  sage_quantized qt;
+  s = run_prologue(dense_geo(B, Hq, Hkv, Lq, Lk, D, dtype, layout), q, k, v, ws, ws_bytes,
+                   &qt, st, true);
   if (s != SAGE_OK) return s;
   if (qt.nseg > 65535 || qt.Hq > 65535)
     return fail(SAGE_ERR_UNSUPPORTED, "more than 65535 segments or heads");

@@ -40,6 +40,8 @@
 // an abort flag, all roles drain their in-flight copies and MMAs, and the CTA
 // frees its TMEM and exits.
 
+#include <cuda_fp16.h>
+
 #include "sage_device.cuh"
 #include "sage_geom.h"
 #include "sage_kernels.h"
@@ -48,7 +50,6 @@ namespace sage {
 namespace {
 
 constexpr int kKStages = 2;   // K ring (released after the second QK^T)
-constexpr int kVStages = 3;   // V ring (released after the second PV)
 constexpr int kThreads = 512;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kAtomBytes = 128 * 128;   // 128 rows x 128 bytes (swizzle atom column)
@@ -59,17 +60,21 @@ constexpr int kSoftmaxRegs = 192;
 constexpr int kCorrRegs = 80;
 constexpr int kMiscRegs = 48;
 
-template <int DP>
+// Shared memory of one CTA.  kV16: the FP16-PV variant (fp16 P~ and V, one
+// query tile per CTA so that its larger operands fit).
+template <int DP, bool kV16 = false>
 struct Layout {
+  static constexpr int kTiles = kV16 ? 1 : 2;          // query tiles per CTA
+  static constexpr int kVStages = kV16 ? 2 : 3;        // V ring (released after a PV)
   static constexpr int kQBytes = kBlockM * DP * 2;     // one query tile
   static constexpr int kKBytes = kBlockN * DP * 2;
-  static constexpr int kVBytes = DP * kBlockN;
-  static constexpr int kPBytes = kBlockM * kBlockN;    // e4m3 P~ of one query tile
+  static constexpr int kVBytes = DP * kBlockN * (kV16 ? 2 : 1);
+  static constexpr int kPBytes = kBlockM * kBlockN * (kV16 ? 2 : 1);   // P~ of one tile
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + 2 * kQBytes;
+  static constexpr int kKOff = kQOff + kTiles * kQBytes;
   static constexpr int kVOff = kKOff + kKStages * kKBytes;
   static constexpr int kPOff = kVOff + kVStages * kVBytes;
-  static constexpr int kBarOff = kPOff + 2 * kPBytes;
+  static constexpr int kBarOff = kPOff + kTiles * kPBytes;
   // q_full, k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], then per tile:
   // s_full, s_free, alpha_ready[2], pv_ready, o_done, l_ready, drain, epi_full, epi_free;
   // sv_ready
@@ -106,6 +111,22 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_lo, uint32_
                  (accumulate || kk > 0) ? 1u : 0u);
 }
 
+// FP16-PV: O (128xDP fp32 in TMEM) (+)= P~ (128x128 fp16, smem, two 64-key
+// swizzle atoms) . V16 tile^T (DP rows x 128 keys fp16, two 64-key atoms),
+// K dimension 128 keys in steps of 16.
+template <int DP>
+__device__ __forceinline__ void issue_pv16(uint32_t o_tmem, uint32_t p_lo, uint32_t v_lo,
+                                           bool accumulate) {
+  constexpr uint32_t idesc = make_idesc(kFmtF16, kFmtF16, kBlockM, DP);
+#pragma unroll
+  for (int kk = 0; kk < kBlockN / 16; ++kk) {
+    const uint32_t p_off = ((kk / 4) * kAtomBytes + (kk % 4) * 32) >> 4;
+    const uint32_t v_off = ((kk / 4) * (DP * 128) + (kk % 4) * 32) >> 4;
+    mma_f16_ss_lo(o_tmem, p_lo + p_off, v_lo + v_off, idesc,
+                  (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity,
                                          volatile int* abort_flag, uint32_t* status,
                                          uint64_t timeout_ns) {
@@ -113,13 +134,14 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity,
   return __all_sync(kFull, ok);
 }
 
-template <int DP>
+template <int DP, bool kV16>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_kernel(const __grid_constant__ CUtensorMap tm_q,
             const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v,
             const __grid_constant__ CUtensorMap tm_o, const AttnParams p) {
-  using L = Layout<DP>;
+  using L = Layout<DP, kV16>;
+  constexpr int kVStages = L::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const SegGeo& g = p.g;
@@ -203,6 +225,20 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
 
+  // V tile j (channel-major: DP rows x 128 keys) into a ring stage: one box of
+  // e4m3, or two 64-key boxes of fp16 (one 128-byte swizzle atom each)
+  auto load_v = [&](uint8_t* dst, int j, uint64_t* bar) {
+    if constexpr (kV16) {
+      for (int a = 0; a < 2; ++a)
+        tma_load_2d(dst + a * (DP * 128), &tm_v,
+                    static_cast<int32_t>(v_col0 + j * kBlockN + 64 * a),
+                    static_cast<int32_t>(v_row0), bar);
+    } else {
+      tma_load_2d(dst, &tm_v, static_cast<int32_t>(v_col0 + j * kBlockN),
+                  static_cast<int32_t>(v_row0), bar);
+    }
+  };
+
   // The producers set up their own rings and issue the copies that need no
   // free slot (Q, the first K and V tiles) at once, so those loads overlap
   // the rest of the set-up.
@@ -242,9 +278,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
     tma_prefetch_desc(&tm_v);
     for (int j = 0; j < n_max && j < kVStages; ++j) {
       mbar_expect_tx(&v_full[j], L::kVBytes);
-      tma_load_2d(smem + L::kVOff + j * L::kVBytes, &tm_v,
-                  static_cast<int32_t>(v_col0 + j * kBlockN), static_cast<int32_t>(v_row0),
-                  &v_full[j]);
+      load_v(smem + L::kVOff + j * L::kVBytes, j, &v_full[j]);
       v_last = j;
     }
   }
@@ -304,11 +338,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
     const float inv = l448 > 0.0f ? __fdiv_rn(1.0f, l448) : 0.0f;
     const uint32_t to = tbase + lane_off + 256 + t * DP;
     if (p.out_tma != 0 && (!g.varlen || (qtile + 1) * kBlockM <= len_q)) {
-      constexpr int kBufs = DP == 128 ? 3 : 2;
+      // 16 KB staging buffers: the pieces of Q_t, then those of P~_t
+      constexpr int kQBufs = L::kQBytes / 16384, kBufs = kQBufs + L::kPBytes / 16384;
       uint8_t* const q_t = smem + L::kQOff + t * L::kQBytes;
       uint8_t* const p_t = smem + L::kPOff + t * L::kPBytes;
       for (int cc = 0; cc < DP / 32 && 32 * cc < D; ++cc) {
-        uint8_t* buf = cc % kBufs == kBufs - 1 ? p_t : q_t + (cc % kBufs) * 16384;
+        const int bi = cc % kBufs;
+        uint8_t* buf = bi < kQBufs ? q_t + bi * 16384 : p_t + (bi - kQBufs) * 16384;
         if (cc >= kBufs) {        // the store of chunk cc - kBufs must have read it
           if (r == 0) {
             bulk_wait_read<kBufs - 1>();
@@ -420,9 +456,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                        p.timeout_ns))
           break;
         mbar_expect_tx(&v_full[st], L::kVBytes);
-        tma_load_2d(smem + L::kVOff + st * L::kVBytes, &tm_v,
-                    static_cast<int32_t>(v_col0 + j * kBlockN),
-                    static_cast<int32_t>(v_row0), &v_full[st]);
+        load_v(smem + L::kVOff + st * L::kVBytes, j, &v_full[st]);
         last = j;
       }
       for (int j = max(0, last - kVStages + 1); j <= last; ++j)
@@ -464,7 +498,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
              mbar_wait(&pv_ready[t], j & 1, abort_flag, p.status, p.timeout_ns);
         if (!ok) break;
         tc_fence_after();
-        issue_pv<DP>(to, pa, va0 + sv * (L::kVBytes >> 4), j > 0);
+        if constexpr (kV16) issue_pv16<DP>(to, pa, va0 + sv * (L::kVBytes >> 4), j > 0);
+        else issue_pv<DP>(to, pa, va0 + sv * (L::kVBytes >> 4), j > 0);
         tc_commit(&o_done[t]);
         tc_commit(&v_empty[sv]);
       }
@@ -497,7 +532,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int r = threadIdx.x - 256;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     if (r < DP) {             // the V scales for the epilogue, off the set-up path
-      sv_cache[r] = p.s_v[(s * g.Hkv + hk) * DP + r];
+      sv_cache[r] = kV16 ? 1.0f : p.s_v[(s * g.Hkv + hk) * DP + r];
       mbar_arrive(sv_ready);
     }
     bool ok = true;
@@ -618,13 +653,14 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
       alpha_s[(2 * t + (j & 1)) * kBlockM + r] = alpha;
       mbar_arrive(&alpha_ready[2 * t + (j & 1)]);        // correction may rescale O now
 
-      // 448 P = 2^(S c - m' + log2 448), quantised to e4m3
-      const float bias = kLog2_448 - m_new;
+      // 448 P = 2^(S c - m' + log2 448), quantised to e4m3; the FP16-PV
+      // variant takes P = 2^(S c - m') itself, rounded to fp16
+      const float bias = kV16 ? -m_new : kLog2_448 - m_new;
       // packed fp32 pairs: the fused multiply-add rounds like fmaf, and the
       // two packed sums keep the four chains (element i goes to chain i % 4)
       const float2 c2 = make_float2(c, c), b2 = make_float2(bias, bias);
       float2 a01 = make_float2(0.0f, 0.0f), a23 = make_float2(0.0f, 0.0f);
-      uint32_t w[32];
+      uint32_t w[kV16 ? 64 : 32];
 #pragma unroll
       for (int q4 = 0; q4 < 32; ++q4) {
         const int i = 4 * q4;
@@ -637,7 +673,14 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
         const float2 p23 = make_float2(fast_exp2(x23.x), fast_exp2(x23.y));
         a01 = __fadd2_rn(a01, p01);
         a23 = __fadd2_rn(a23, p23);
-        w[q4] = pack_e4m3x2(p01.x, p01.y) | (pack_e4m3x2(p23.x, p23.y) << 16);
+        if constexpr (kV16) {
+          const __half2 h01 = __floats2half2_rn(p01.x, p01.y);
+          const __half2 h23 = __floats2half2_rn(p23.x, p23.y);
+          w[2 * q4] = *reinterpret_cast<const uint32_t*>(&h01);
+          w[2 * q4 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
+        } else {
+          w[q4] = pack_e4m3x2(p01.x, p01.y) | (pack_e4m3x2(p23.x, p23.y) << 16);
+        }
       }
       const float a0 = a01.x, a1 = a01.y, a2 = a23.x, a3 = a23.y;
       // the P~ buffer is free once PV(j-1) has read it
@@ -645,9 +688,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
         ok = wait_all(&o_done[t], (j - 1) & 1, abort_flag, p.status, p.timeout_ns);
         if (!ok) break;
       }
+      // 16-byte chunks of the row, swizzled by row % 8 within each 64-key
+      // (fp16) or 128-key (e4m3) atom
 #pragma unroll
-      for (int c16 = 0; c16 < 8; ++c16)
-        *reinterpret_cast<uint4*>(prow + ((c16 ^ rsw) << 4)) =
+      for (int c16 = 0; c16 < (kV16 ? 16 : 8); ++c16)
+        *reinterpret_cast<uint4*>(prow + (c16 / 8) * kAtomBytes + (((c16 % 8) ^ rsw) << 4)) =
             make_uint4(w[4 * c16], w[4 * c16 + 1], w[4 * c16 + 2], w[4 * c16 + 3]);
       fence_proxy_async_smem();
       l448 = l448 * alpha + ((a0 + a1) + (a2 + a3));
@@ -747,13 +792,14 @@ __global__ void debug_e4m3_kernel(const float* in, uint8_t* out, int64_t n) {
     out[i] = static_cast<uint8_t>(pack_e4m3x2(in[i], 0.0f) & 0xFFu);
 }
 
-template <int DP>
+template <int DP, bool kV16>
 cudaError_t launch_attention_t(const AttnMaps& maps, const AttnParams& p,
                                cudaStream_t st) {
+  using L = Layout<DP, kV16>;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(
-        attn_kernel<DP>, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<DP>::kAlloc);
+        attn_kernel<DP, kV16>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -763,7 +809,14 @@ cudaError_t launch_attention_t(const AttnMaps& maps, const AttnParams& p,
             static_cast<unsigned>(p.g.nseg));
   AttnParams prm = p;
   prm.flat_pairs = -1;
-  if (!p.g.varlen && !p.causal) {
+  if (kV16) {
+    // one query tile per CTA (dense problems only): the 1D grid of single
+    // tiles, in (segment, head, tile) order
+    const int64_t pairs = static_cast<int64_t>(grid.x) * grid.y * grid.z;
+    if (p.g.varlen || 2 * pairs >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+    prm.flat_pairs = 0;
+    grid = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+  } else if (!p.g.varlen && !p.causal) {
     // Uniform pairs run in waves of one CTA per SM.  When the last wave is
     // at most half full, its pairs run as single tiles instead (launched
     // last), which shortens that wave to one tile's time.
@@ -775,8 +828,8 @@ cudaError_t launch_attention_t(const AttnMaps& maps, const AttnParams& p,
       int n = 0, per = 0;
       e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
       if (e != cudaSuccess) return e;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, attn_kernel<DP>, kThreads,
-                                                        Layout<DP>::kAlloc);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, attn_kernel<DP, kV16>, kThreads,
+                                                        L::kAlloc);
       if (e != cudaSuccess) return e;
       sms[dev] = n * (per > 0 ? per : 1);
     }
@@ -788,8 +841,8 @@ cudaError_t launch_attention_t(const AttnMaps& maps, const AttnParams& p,
       grid = dim3(static_cast<unsigned>(pairs + tail), 1, 1);
     }
   }
-  attn_kernel<DP><<<grid, kThreads, Layout<DP>::kAlloc, st>>>(maps.q, maps.k, maps.v, maps.o,
-                                                               prm);
+  attn_kernel<DP, kV16><<<grid, kThreads, L::kAlloc, st>>>(maps.q, maps.k, maps.v, maps.o,
+                                                            prm);
   note_launch();
   return cudaGetLastError();
 }
@@ -815,8 +868,11 @@ cudaError_t launch_debug_qk_t(const AttnMaps& maps, const AttnParams& p,
 
 cudaError_t launch_attention(const AttnMaps& maps, const AttnParams& p,
                              cudaStream_t st) {
-  return p.g.Dp == 64 ? launch_attention_t<64>(maps, p, st)
-                      : launch_attention_t<128>(maps, p, st);
+  if (p.v16)
+    return p.g.Dp == 64 ? launch_attention_t<64, true>(maps, p, st)
+                        : launch_attention_t<128, true>(maps, p, st);
+  return p.g.Dp == 64 ? launch_attention_t<64, false>(maps, p, st)
+                      : launch_attention_t<128, false>(maps, p, st);
 }
 
 cudaError_t launch_debug_qk(const AttnMaps& maps, const AttnParams& p,

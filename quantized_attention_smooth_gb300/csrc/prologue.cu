@@ -125,6 +125,7 @@ struct ProParams {
   uint64_t timeout_ns;
   int32_t q_hnd, k_hnd;       // 1: tiles are (head, token) planes; 0: token-major
   float one;                  // 1.0, opaque to the compiler (see code2)
+  int32_t v16;                // V written as fp16 (FP16-PV variant) instead of e4m3
   Plan plan;
 };
 
@@ -715,6 +716,66 @@ __device__ __forceinline__ void v_tile(const ProParams& p, int nvalid, const Til
   }
 }
 
+// V for the FP16-PV variant: the same transposition without scaling, to
+// fp16 (bf16 inputs rounded to nearest even).  A channel row of the tile is
+// 64 words of two tokens; word w of channel c sits at c * 64 + (w ^ 8 * (c /
+// 8 % 8)), keeping every 16-byte group whole.
+// out: v16 at (channel 0 of the unit, first token of the tile).
+template <bool kTma, bool kBf16, int DP>
+__device__ __forceinline__ void v_tile16(const ProParams& p, int nvalid,
+                                         const TileRows<kTma, DP>& rows, uint16_t* out,
+                                         uint32_t* vt) {
+  constexpr int G = DP / 8, RG = kConsumers / G, NTW = (kBlockN / 4) / RG;
+  const int lc = threadIdx.x % G, r = threadIdx.x / G, c0 = lc * 8;
+  const bool full = nvalid == kBlockN;
+  TileRows<kTma, DP> rv = rows;
+  if constexpr (kTma) rv.at = rows.at + 3 * r * DP * 2;          // row r -> row 4r
+  else rv.row0 = rows.row0 + static_cast<int64_t>(3 * r) * rows.tok_stride;
+  uint4 raw[NTW][4];
+#pragma unroll
+  for (int a = 0; a < NTW; ++a) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int t = 4 * (r + a * RG) + e;
+      raw[a][e] = (full || t < nvalid) ? rv.template get<1>(e + 4 * RG * a)
+                                       : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  csync();                                      // every row read: the stage is free
+  const int swz = ((c0 >> 3) & 7) << 3;         // the same for the 8 channels of c0
+#pragma unroll
+  for (int a = 0; a < NTW; ++a) {
+    const int q = r + a * RG;                   // tokens 4q .. 4q + 3
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {               // channels c0 + 2j, c0 + 2j + 1
+      uint32_t h[4];                            // fp16 pair (channel 2j low, 2j + 1 high)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if constexpr (kBf16) {
+          const float2 x = cvt2<true>(word(raw[a][e], j));
+          const __half2 hv = __floats2half2_rn(x.x, x.y);
+          memcpy(&h[e], &hv, 4);
+        } else {
+          h[e] = word(raw[a][e], j);
+        }
+      }
+      uint2* lo = reinterpret_cast<uint2*>(vt + (c0 + 2 * j) * 64 + ((2 * q) ^ swz));
+      uint2* hi = reinterpret_cast<uint2*>(vt + (c0 + 2 * j + 1) * 64 + ((2 * q) ^ swz));
+      *lo = make_uint2(__byte_perm(h[0], h[1], 0x5410), __byte_perm(h[2], h[3], 0x5410));
+      *hi = make_uint2(__byte_perm(h[0], h[1], 0x7632), __byte_perm(h[2], h[3], 0x7632));
+    }
+  }
+  csync();
+  constexpr int kChunks = DP * (kBlockN * 2 / 16);   // 16-byte pieces
+  const int64_t vcols = p.g.v_cols;
+#pragma unroll
+  for (int ci = threadIdx.x; ci < kChunks; ci += kConsumers) {
+    const int c = ci / (kBlockN * 2 / 16), w4 = 4 * (ci % (kBlockN * 2 / 16));
+    const uint4 val = *reinterpret_cast<const uint4*>(&vt[c * 64 + (w4 ^ (((c >> 3) & 7) << 3))]);
+    *reinterpret_cast<uint4*>(out + c * vcols + 2 * w4) = val;
+  }
+}
+
 // ---------------------------------------------------------- statistics
 // A unit's K mean of one channel from its exact sum (fp16: int64 fixed point
 // at 2^-24; bf16: fp64): the fp64 quotient by the key count, rounded to fp32.
@@ -807,8 +868,13 @@ __device__ __forceinline__ void consume(const ProParams& p, const Slot& it, int 
     csync();
     const int64_t vrow0 = (g.varlen ? 0 : s * g.Hkv * DP) + h * DP;
     const int64_t vcol0 = (g.varlen ? ws_seg_base(1, s, start, 0, 0) : 0) + t0;
-    v_tile<kTma, kBf16, DP>(p, it.nvalid, rows, sm.coef, p.v8 + vrow0 * g.v_cols + vcol0,
-                            reinterpret_cast<uint32_t*>(sm.tile[stage]));
+    if (p.v16)
+      v_tile16<kTma, kBf16, DP>(p, it.nvalid, rows,
+                                reinterpret_cast<uint16_t*>(p.v8) + vrow0 * g.v_cols + vcol0,
+                                reinterpret_cast<uint32_t*>(sm.tile[stage]));
+    else
+      v_tile<kTma, kBf16, DP>(p, it.nvalid, rows, sm.coef, p.v8 + vrow0 * g.v_cols + vcol0,
+                              reinterpret_cast<uint32_t*>(sm.tile[stage]));
   } else {
     // final item (statistics only): the unit's K mean and V scales, read from
     // L2 (the group's barrier, acquired by the producer, orders them)
@@ -1370,6 +1436,7 @@ cudaError_t launch_prologue(const SegGeo& g, const PrologueBuffers& b,
   prm.cnt_a = b.sync; prm.cnt_b = b.sync + kMaxGroups; prm.gbar = b.sync + 2 * kMaxGroups;
   prm.cnt_q = b.sync + 3 * kMaxGroups;
   prm.status = b.status; prm.timeout_ns = b.timeout_ns;
+  prm.v16 = b.v16;
   prm.one = 1.0f;
   return launch_any(prm, vec, true, st);
 }

@@ -24,7 +24,7 @@ EXPORTS = (
     "sage_attn_fwd_varlen", "sage_debug_qk_int32", "sage_debug_e4m3",
     "sage_debug_set_fault", "sage_device_status", "sage_last_error",
     "sage_kv_stats_noalloc", "sage_launch_count", "sage_quant_prologue_strided",
-    "sage_attn_fwd_strided",
+    "sage_attn_fwd_strided", "sage_quant_prologue_pv16", "sage_attn_fwd_pv16",
 )
 
 
@@ -50,7 +50,7 @@ class Quantized(ctypes.Structure):
         ("q16", ctypes.c_void_p), ("k16", ctypes.c_void_p), ("v8", ctypes.c_void_p),
         ("s_q", ctypes.c_void_p), ("s_k", ctypes.c_void_p), ("s_v", ctypes.c_void_p),
         ("k_mean", ctypes.c_void_p), ("stats", ctypes.c_void_p),
-        ("status", ctypes.c_void_p),
+        ("status", ctypes.c_void_p), ("v_fp16", ctypes.c_int32),
     ]
 
 
@@ -72,6 +72,10 @@ def _load():
                                          QP, P], I),
         "sage_attn_fwd_strided": ([P, P, P, P, I64, I64, I64, I64, I64, I64, P, P, I, I, F, I,
                                    P, SZ, P], I),
+        "sage_quant_prologue_pv16": ([P, P, P, I, I, I64, I64, I64, I64, I64, I64, P, SZ, QP,
+                                      P], I),
+        "sage_attn_fwd_pv16": ([P, P, P, P, I64, I64, I64, I64, I64, I64, I, I, F, I, P, SZ, P],
+                               I),
         "sage_attn_quantized": ([QP, P, I, I, F, P], I),
         "sage_attn_fwd": ([P, P, P, P, I64, I64, I64, I64, I64, I64, I, I, F, I, P, SZ, P], I),
         "sage_attn_fwd_varlen": ([P, P, P, P, P, P, I64, I64, I64, I, I, I64, I64, I64, I, F,
@@ -176,6 +180,21 @@ def quant_prologue(q, k, v, layout="HND", ws=None, stream=None) -> Quantized:
     return qt
 
 
+def quant_prologue_pv16(q, k, v, layout="HND", ws=None, stream=None) -> Quantized:
+    """Prologue of the FP16-PV variant: INT8 Q/K as usual, V kept in fp16."""
+    lay = _layout_code(layout)
+    B, Hq, Hkv, Lq, Lk, D = _dims(q, k, lay)
+    if ws is None:
+        ws = alloc_workspace(workspace_bytes(B, Hq, Hkv, Lq, Lk, D), q.device)
+    qt = Quantized()
+    rc = _lib.sage_quant_prologue_pv16(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), lay, B, Hq,
+                                       Hkv, Lq, Lk, D, _ptr(ws), ws.numel(), ctypes.byref(qt),
+                                       _stream(stream))
+    _check(rc, "sage_quant_prologue_pv16")
+    qt._ws = ws
+    return qt
+
+
 def quant_prologue_varlen(q, k, v, cu_q, cu_k, max_q, max_k, ws=None, stream=None):
     total_q, Hq, D = q.shape
     total_k, Hkv, _ = k.shape
@@ -212,6 +231,20 @@ def attn_fwd(q, k, v, out, layout="HND", is_causal=False, sm_scale=None, ws=None
                             lay, int(bool(is_causal)), float(sm_scale or 0.0),
                             _dtype_code(q), _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "sage_attn_fwd")
+    return out
+
+
+def attn_fwd_pv16(q, k, v, out, layout="HND", is_causal=False, sm_scale=None, ws=None,
+                 stream=None):
+    """Prologue + FP16-PV attention (dense)."""
+    lay = _layout_code(layout)
+    B, Hq, Hkv, Lq, Lk, D = _dims(q, k, lay)
+    if ws is None:
+        ws = alloc_workspace(workspace_bytes(B, Hq, Hkv, Lq, Lk, D), q.device)
+    rc = _lib.sage_attn_fwd_pv16(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, Lq, Lk, D,
+                                 lay, int(bool(is_causal)), float(sm_scale or 0.0),
+                                 _dtype_code(q), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "sage_attn_fwd_pv16")
     return out
 
 
@@ -294,6 +327,13 @@ def sageattn(q, k, v, tensor_layout="HND", is_causal=False, sm_scale=None):
     if q.is_contiguous() and k.is_contiguous() and v.is_contiguous():
         return attn_fwd(q, k, v, out, tensor_layout, is_causal, sm_scale)
     return attn_fwd_strided(q, k, v, out, tensor_layout, is_causal, sm_scale)
+
+
+def sageattn_qk_int8_pv_fp16(q, k, v, tensor_layout="HND", is_causal=False, sm_scale=None):
+    """The more accurate variant: INT8 QK^T, fp16 P and V (dense inputs)."""
+    import torch
+    out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    return attn_fwd_pv16(q, k, v, out, tensor_layout, is_causal, sm_scale)
 
 
 def debug_qk_int32(qt: Quantized, seg, hq, qtile, ktile, out=None, stream=None):
