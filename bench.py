@@ -53,17 +53,18 @@ def workload_ops(w: wl.Workload, dim=None) -> float:
     return w.ops(dim=dim)
 
 
-def prologue_bytes(w: wl.Workload) -> float:
+def prologue_bytes(w: wl.Workload, v_bytes: int = 1) -> float:
     """Algorithmic HBM bytes of the prologue: read q, k, v (2 B each); write
-    the fp16 code copies of Q and K (2 B each) and the e4m3 V (1 B) per padded
-    element; the second pass over K and V is an L2 re-read and counts 0."""
+    the fp16 code copies of Q and K (2 B each) and V (e4m3: 1 B, or fp16 for
+    the FP16-PV variant: 2 B) per padded element; the second pass over K and
+    V is an L2 re-read and counts 0."""
     Dp = 64 if w.D <= 64 else 128
     nq = nk = 0
     for lq, lk in w.seg_lengths():
         nq += lq
         nk += lk
     read = 2 * w.D * (nq * w.Hq + 2 * nk * w.Hkv)
-    write = Dp * (2 * nq * w.Hq + 3 * nk * w.Hkv)
+    write = Dp * (2 * nq * w.Hq + (2 + v_bytes) * nk * w.Hkv)
     scales = 4 * (nq * w.Hq + nk * w.Hkv // 128 + 2 * w.Hkv * Dp * w.nseg)
     return float(read + write + scales)
 
@@ -395,7 +396,7 @@ def main():
     # causal problem not counted (the kernel skips them)
     att_tflops = fig["attention_tflops_padded_effective"]
     tops = fig["value"]
-    pro_gbs = prologue_bytes(w) / (r["pro_ms"] * 1e-3) / 1e9
+    pro_gbs = prologue_bytes(w, 2 if pv16 else 1) / (r["pro_ms"] * 1e-3) / 1e9
     inp = wl.make_inputs(w)
     cpu_ops, cpu_s, cores = oracle_sample(w, inp, args.cpu_rows)
     line = {
