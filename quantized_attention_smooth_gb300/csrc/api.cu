@@ -77,7 +77,7 @@ WsLayout ws_layout(const SegGeo& g) {
   w.status = o; o += 256;
   w.ksum = o; o = align256(o + nstat * 8);
   w.vmax = o; o = align256(o + nstat * 4);
-  w.sync = o; o = align256(o + 4 * 64 * 4);
+  w.sync = o; o = align256(o + 8 * 64 * 4);   // two launches' list counters
   // means and scales start at zero: a segment without keys keeps them so
   w.k_mean = o; o = align256(o + nstat * 4);
   w.s_v = o; o = align256(o + nstat * 4);

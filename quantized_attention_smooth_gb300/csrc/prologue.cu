@@ -26,16 +26,17 @@
 //             next to the tile and turned into multipliers there),
 //             transposed to channel-major;
 //   final     (statistics-only calls) the unit's K mean and V scales.
-// The units are cut into groups of about 12 MB of K and V, and each group
+// The units are cut into groups of about 100 MB of K and V, and each group
 // has two lists: A (its stats tiles) and B (its K and V tiles, or its final
 // items, which need the group's statistics).  A items never wait.  Once a
 // CTA's consumers are done with every A item of group g it has taken, its
 // helper warp arrives at the group's barrier (a counter, one release per
 // CTA and group); B items of the group are taken only after every CTA has
 // arrived, so they find the group's sums complete and their K and V, read
-// by the A list with an evict-last hint, still in L2.  The A list runs a
-// few groups ahead of the B list (about 48 MB of K and V held in L2), which
-// hides the barriers.  The Q tiles depend on nothing: they form one more
+// by the A list with an evict-last hint, still in L2.  Few large groups
+// measured faster than many small ones (fewer barrier rounds; the Q list
+// fills the waits).  Inputs whose K and V exceed 5/4 of L2 are re-read from
+// HBM anyway and take two launches instead (launch_prologue).  The Q tiles depend on nothing: they form one more
 // list, taken only when neither of the others has an item ready, so they
 // fill the barrier waits and the end.  Nothing waits inside a list, and
 // every wait is bounded (timeout -> status bit).  Every 128-token
@@ -67,8 +68,8 @@ constexpr int kThreads = kConsumers + 64;
 constexpr int kStages = 3;
 constexpr int kQueue = 8;                    // finished stats tiles awaiting the helper
 constexpr int kMaxGroups = 64;               // counters per list in the workspace
-constexpr int64_t kGroupBytes = 12ll << 20;  // K and V bytes of a group (target)
-constexpr int64_t kL2Hold = 48ll << 20;      // K and V bytes held in L2 between reads
+constexpr int64_t kGroupBytes = 100ll << 20; // K and V bytes of a group (target)
+constexpr int64_t kL2Hold = 128ll << 20;     // K and V bytes held in L2 between reads
 constexpr int kTileBytes = 128 * 128 * 2;    // 128 rows of up to 128 16-bit values
 constexpr uint32_t kSleepNs = 20000;         // suspend hint of barrier waits
 // fp32 2^23 + 2^22 + 0x6600: adding it rounds to an integer n (ties to even)
@@ -99,6 +100,16 @@ struct Plan {
   int32_t n_kv;       // K and V items per unit (K and V tiles alternate)
   int32_t n_b;        // B items per unit: n_kv, or 1 (final) without quantisation
   int32_t nqt;        // 128-token tiles per query head
+  int32_t open;       // the statistics are final already (no A list, no barriers)
+  int32_t q_first;    // Q items before A items
+};
+
+// What a launch does (see make_plan).
+enum PlanMode : int {
+  kPlanAll = 0,       // statistics, Q, then K and V once a group's statistics are final
+  kPlanStats = 1,     // statistics and the final items only
+  kPlanStatsQ = 2,    // Q first, then statistics and the final items
+  kPlanKV = 3,        // K and V from final statistics
 };
 
 struct ProParams {
@@ -1006,8 +1017,9 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
   uint32_t upar = 0;       // bit s: parity of the uses of stage s so far
   uint32_t tma = 0;        // bit s: stage s was last filled by a tensor copy
   bool ok = true;
-  int ga = 0, gb = 0;      // group of the A list / B list being taken
-  bool b_open = false;     // group gb's statistics are final
+  int ga = P.n_stats > 0 ? 0 : P.groups;   // group of the A list being taken
+  int gb = 0;              // group of the B list being taken
+  bool b_open = P.open != 0;   // group gb's statistics are final
   uint32_t poll = 0;       // group gb's barrier count, read on the previous turn
   bool polled = false;
   int a_idx = 0, b_idx = 0, q_idx = 0;  // claims taken ahead (lane 0), valid when *_pend
@@ -1049,8 +1061,24 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
         break;
       }
       ++gb;
-      b_open = false;
+      b_open = P.open != 0;
     }
+    // the Q list: a lambda, taken before or after the A list
+    auto take_q = [&]() {
+      if (it.kind < 0 && q_left) {
+        if (!q_pend && lane == 0) q_idx = static_cast<int>(atomicAdd(p.cnt_q, 1u));
+        const int idx = __shfl_sync(0xFFFFFFFFu, q_idx, 0);
+        q_pend = false;
+        if (idx < P.units * P.n_q) {
+          decode_q(P, idx, &it.kind, &it.unit, &it.sub);
+          if (lane == 0) q_idx = static_cast<int>(atomicAdd(p.cnt_q, 1u));
+          q_pend = true;
+        } else {
+          q_left = false;
+        }
+      }
+    };
+    if (P.q_first) take_q();
     if (it.kind < 0 && ga < P.groups && ga <= gb + P.lead) {
       if (!a_pend && lane == 0) a_idx = static_cast<int>(atomicAdd(p.cnt_a + ga, 1u));
       const int idx = __shfl_sync(0xFFFFFFFFu, a_idx, 0);
@@ -1068,18 +1096,7 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
         ++ga;
       }
     }
-    if (it.kind < 0 && q_left) {
-      if (!q_pend && lane == 0) q_idx = static_cast<int>(atomicAdd(p.cnt_q, 1u));
-      const int idx = __shfl_sync(0xFFFFFFFFu, q_idx, 0);
-      q_pend = false;
-      if (idx < P.units * P.n_q) {
-        decode_q(P, idx, &it.kind, &it.unit, &it.sub);
-        if (lane == 0) q_idx = static_cast<int>(atomicAdd(p.cnt_q, 1u));
-        q_pend = true;
-      } else {
-        q_left = false;
-      }
-    }
+    if (!P.q_first) take_q();
     if (it.kind < 0) {
       if (ga >= P.groups && gb >= P.groups && !q_left) {
         it.kind = kEnd;
@@ -1269,21 +1286,23 @@ prologue_kernel(const __grid_constant__ ProParams p) {
 
 constexpr size_t kSmemBytes = sizeof(PSmem) + 1024;   // + alignment slack
 
-// Work of a call: n_q = n_kv = 0 gives statistics only.
-bool make_plan(const SegGeo& g, bool with_quant, Plan* out) {
+// Work of a launch (PlanMode): without K/V items the B list holds one final
+// item per unit; without statistics (kPlanKV) the B list is open at once.
+bool make_plan(const SegGeo& g, int mode, Plan* out) {
   Plan P{};
   const int64_t maxk = g.varlen ? g.max_k : g.Lk;
   const int64_t maxq = g.varlen ? g.max_q : g.Lq;
   const int64_t nkb = (maxk + kBlockN - 1) / kBlockN;
   const int64_t units = g.nseg * g.Hkv;
-  const int64_t n_stats = nkb > 0 ? 2 * nkb : 1;
+  const bool stats = mode != kPlanKV;
+  const int64_t n_stats = stats ? (nkb > 0 ? 2 * nkb : 1) : 0;
   const int64_t nqt = (maxq + kBlockM - 1) / kBlockM;
-  const int64_t n_q = with_quant ? (g.Hq / g.Hkv) * nqt : 0;
-  const int64_t n_kv = with_quant ? 2 * nkb : 0;
+  const int64_t n_q = (mode == kPlanAll || mode == kPlanStatsQ) ? (g.Hq / g.Hkv) * nqt : 0;
+  const int64_t n_kv = (mode == kPlanAll || mode == kPlanKV) ? 2 * nkb : 0;
   const int64_t per = n_stats + n_q + (n_kv > 0 ? n_kv : 1);
   if (units * per >= (int64_t(1) << 31)) return false;
   int64_t group = units, lead = 1;
-  if (n_kv > 0) {
+  if (n_kv > 0 && stats) {
     // a group's K and V are read by its A list and again (from L2) by its B
     // list, which runs up to `lead` groups behind: lead + 1 groups must fit
     const int64_t unit_bytes = 4 * maxk * g.D;
@@ -1305,6 +1324,8 @@ bool make_plan(const SegGeo& g, bool with_quant, Plan* out) {
   P.n_kv = static_cast<int32_t>(n_kv);
   P.n_b = static_cast<int32_t>(n_kv > 0 ? n_kv : 1);
   P.nqt = static_cast<int32_t>(nqt);
+  P.open = stats ? 0 : 1;
+  P.q_first = mode == kPlanStatsQ ? 1 : 0;
   *out = P;
   return true;
 }
@@ -1351,7 +1372,7 @@ bool view_map(CUtensorMap* map, const uint16_t* base, int64_t D, int64_t Dp, int
 }
 
 template <bool kTma, bool kBf16, int DP>
-cudaError_t launch_t(ProParams& prm, bool with_quant, cudaStream_t st) {
+cudaError_t launch_t(ProParams& prm, int mode, cudaStream_t st) {
   static int per_sm[64] = {};                  // resident CTAs per SM, per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1371,7 +1392,7 @@ cudaError_t launch_t(ProParams& prm, bool with_quant, cudaStream_t st) {
   int sms = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  if (!make_plan(prm.g, with_quant, &prm.plan)) return cudaErrorInvalidValue;
+  if (!make_plan(prm.g, mode, &prm.plan)) return cudaErrorInvalidValue;
   if (prm.plan.groups <= 0) return cudaSuccess;
   // every CTA is resident at once (the group barriers count them all): a
   // cooperative launch of exactly the resident CTAs
@@ -1384,7 +1405,7 @@ cudaError_t launch_t(ProParams& prm, bool with_quant, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_any(ProParams& prm, bool vec, bool with_quant, cudaStream_t st) {
+cudaError_t launch_any(ProParams& prm, bool vec, int mode, cudaStream_t st) {
   const SegGeo& g = prm.g;
   const bool bf16 = g.dtype == 1;
   const bool d64 = g.Dp == 64;
@@ -1411,15 +1432,15 @@ cudaError_t launch_any(ProParams& prm, bool vec, bool with_quant, cudaStream_t s
                       !input_map(&prm.mv, prm.v, g.D, g.Dp, g.Hkv, g.Lk, ntk, prm.k_hnd)))
         return cudaErrorInvalidValue;
     }
-    if (bf16) return d64 ? launch_t<true, true, 64>(prm, with_quant, st)
-                         : launch_t<true, true, 128>(prm, with_quant, st);
-    return d64 ? launch_t<true, false, 64>(prm, with_quant, st)
-               : launch_t<true, false, 128>(prm, with_quant, st);
+    if (bf16) return d64 ? launch_t<true, true, 64>(prm, mode, st)
+                         : launch_t<true, true, 128>(prm, mode, st);
+    return d64 ? launch_t<true, false, 64>(prm, mode, st)
+               : launch_t<true, false, 128>(prm, mode, st);
   }
-  if (bf16) return d64 ? launch_t<false, true, 64>(prm, with_quant, st)
-                       : launch_t<false, true, 128>(prm, with_quant, st);
-  return d64 ? launch_t<false, false, 64>(prm, with_quant, st)
-             : launch_t<false, false, 128>(prm, with_quant, st);
+  if (bf16) return d64 ? launch_t<false, true, 64>(prm, mode, st)
+                       : launch_t<false, true, 128>(prm, mode, st);
+  return d64 ? launch_t<false, false, 64>(prm, mode, st)
+             : launch_t<false, false, 128>(prm, mode, st);
 }
 
 }  // namespace
@@ -1438,7 +1459,33 @@ cudaError_t launch_prologue(const SegGeo& g, const PrologueBuffers& b,
   prm.status = b.status; prm.timeout_ns = b.timeout_ns;
   prm.v16 = b.v16;
   prm.one = 1.0f;
-  return launch_any(prm, vec, true, st);
+  // One launch keeps a few groups of K and V in L2 between their two reads
+  // (the A list runs ahead of the B list).  When the K and V inputs exceed
+  // 5/4 of L2 (measured crossover: 134 MB one launch faster, 188 MB two
+  // launches), two launches stream better: the Q tiles, the K and V
+  // statistics and the final items; then the K and V tiles from the final
+  // statistics (counters of their own).
+  const int64_t ntk = g.varlen ? g.total_k : g.nseg * g.Lk;
+  const int64_t kv_bytes = 2 * ntk * g.Hkv * g.D * 2;
+  static int64_t l2_bytes[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (l2_bytes[dev] == 0) {
+    int l2 = 0;
+    e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+    if (e != cudaSuccess) return e;
+    l2_bytes[dev] = l2 > 0 ? l2 : 1;
+  }
+  if (4 * kv_bytes <= 5 * l2_bytes[dev]) return launch_any(prm, vec, kPlanAll, st);
+  e = launch_any(prm, vec, kPlanStatsQ, st);
+  if (e != cudaSuccess) return e;
+  if ((g.varlen ? g.max_k : g.Lk) <= 0) return cudaSuccess;    // no keys to quantise
+  ProParams kv = prm;
+  kv.cnt_a = b.sync + 4 * kMaxGroups; kv.cnt_b = b.sync + 5 * kMaxGroups;
+  kv.gbar = b.sync + 6 * kMaxGroups; kv.cnt_q = b.sync + 7 * kMaxGroups;
+  return launch_any(kv, vec, kPlanKV, st);
 }
 
 // ------------------------------------------- statistics without allocation
@@ -1497,7 +1544,7 @@ cudaError_t launch_kv_stats_static(const SegGeo& g, const uint16_t* k,
   prm.v_inv = reinterpret_cast<float*>(base + kStaticHeader + kStaticStatEntries * 12);
   prm.timeout_ns = timeout_ns;
   prm.one = 1.0f;
-  return launch_any(prm, vec, false, st);
+  return launch_any(prm, vec, kPlanStats, st);
 }
 
 }  // namespace sage

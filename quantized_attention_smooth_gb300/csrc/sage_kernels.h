@@ -33,7 +33,8 @@ struct PrologueBuffers {
   float* v_inv;
   void* ksum;        // int64 (fp16 inputs) or double (bf16), [nseg][Hkv][Dp]
   uint32_t* vmax;    // float bits, [nseg][Hkv][Dp]
-  unsigned int* sync;         // 4 x 64 counters (A lists, B lists, group barriers, Q list), zeroed
+  unsigned int* sync;         // 2 x 4 x 64 counters (A lists, B lists, group barriers, Q list
+                              // of each of the prologue's two launches), zeroed
   uint32_t* status;
   uint64_t timeout_ns;        // bound of every wait
   int32_t v16;                // write V as fp16 (FP16-PV variant) instead of e4m3
