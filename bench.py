@@ -38,6 +38,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # workload, from the ncu capture summarised in
 # profiles/attn_kernel_b2_h24_l4096_d128.md (None for other workloads).
 ATTN_NCU_DRAM_BYTES = {"b2_h24_l4096_d128": 126.746624e6 + 60.900096e6}
+# the same for the FP16-PV variant's attention kernel (fp16 V and P~)
+ATTN16_NCU_DRAM_BYTES = {"b2_h24_l4096_d128": 151.875584e6 + 69.889792e6}
 
 
 def load_peaks():
@@ -409,7 +411,8 @@ def main():
         "config": dict(config_of(w), variant=args.variant),
         "roofline": {"bound": "tensor", "achieved": att_tflops, "peak": mix_peak,
                      "unit": "TFLOP/s", "frac": att_tflops / mix_peak,
-                     "traffic": None if pv16 else ATTN_NCU_DRAM_BYTES.get(w.name),
+                     "traffic": (ATTN16_NCU_DRAM_BYTES if pv16 else
+                                 ATTN_NCU_DRAM_BYTES).get(w.name),
                      "kernel": "attn_kernel (fused QK^T/softmax/PV)",
                      "peak_note": (f"{src} bf16 burst {bf16} (QK^T and the fp16 PV at the "
                                    "16-bit rate)" if pv16 else
