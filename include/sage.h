@@ -235,6 +235,13 @@ SAGE_API sage_status sage_debug_e4m3(const float* in, uint8_t* out, int64_t n,
  * bounded wait runs out after `timeout_ns` (0: default of one second). */
 SAGE_API void sage_debug_set_fault(int skip_kv_tile, uint64_t timeout_ns);
 
+/* Test hook: the prologue entry points run as one launch (1), as two
+ * launches (2: Q tiles and K/V statistics, then K/V tiles), or choose by
+ * size (0, the default: two launches when the K and V inputs exceed 5/4 of
+ * the device's L2).  Other values mean 0.  The results are identical either
+ * way; the hook lets tests cover both plans at any size. */
+SAGE_API void sage_debug_set_prologue_launches(int launches);
+
 /* Reads (synchronising `stream`) the device status word of workspace ws:
  * SAGE_OK, SAGE_ERR_DEVICE_TIMEOUT, SAGE_ERR_INVALID_ARG, or
  * SAGE_ERR_UNSUPPORTED for an internal inconsistency the prologue caught

@@ -30,6 +30,7 @@ namespace {
 
 thread_local std::string g_last_error;
 std::atomic<int> g_skip_kv_tile{-1};
+std::atomic<int> g_prologue_launches{0};
 std::atomic<unsigned long long> g_timeout_ns{0};
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;   // 1 s
 
@@ -327,6 +328,7 @@ sage_status run_prologue(const SegGeo& g, const void* q, const void* k, const vo
                    g.q_tok_stride % 8 == 0 && g.k_seg_stride % 8 == 0 &&
                    g.k_head_stride % 8 == 0 && g.k_tok_stride % 8 == 0;
   b.v16 = v16 ? 1 : 0;
+  b.launches = g_prologue_launches.load();
   e = launch_prologue(g, b, vec, st);
   if (e != cudaSuccess) return cuda_fail(e, "prologue launch");
   return ok();
@@ -693,6 +695,10 @@ sage_status sage_debug_e4m3(const float* in, uint8_t* out, int64_t n, sage_strea
 void sage_debug_set_fault(int skip_kv_tile, uint64_t timeout_ns) {
   g_skip_kv_tile.store(skip_kv_tile);
   g_timeout_ns.store(timeout_ns);
+}
+
+void sage_debug_set_prologue_launches(int launches) {
+  g_prologue_launches.store(launches == 1 || launches == 2 ? launches : 0);
 }
 
 sage_status sage_device_status(const void* ws, sage_stream_t stream) {

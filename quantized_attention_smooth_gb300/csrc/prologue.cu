@@ -1478,7 +1478,8 @@ cudaError_t launch_prologue(const SegGeo& g, const PrologueBuffers& b,
     if (e != cudaSuccess) return e;
     l2_bytes[dev] = l2 > 0 ? l2 : 1;
   }
-  if (4 * kv_bytes <= 5 * l2_bytes[dev]) return launch_any(prm, vec, kPlanAll, st);
+  const bool two = b.launches == 2 || (b.launches == 0 && 4 * kv_bytes > 5 * l2_bytes[dev]);
+  if (!two) return launch_any(prm, vec, kPlanAll, st);
   e = launch_any(prm, vec, kPlanStatsQ, st);
   if (e != cudaSuccess) return e;
   if ((g.varlen ? g.max_k : g.Lk) <= 0) return cudaSuccess;    // no keys to quantise

@@ -33,6 +33,7 @@ struct PrologueBuffers {
   float* v_inv;
   void* ksum;        // int64 (fp16 inputs) or double (bf16), [nseg][Hkv][Dp]
   uint32_t* vmax;    // float bits, [nseg][Hkv][Dp]
+  int32_t launches;           // 0: one or two launches by size; 1 or 2: that many (tests)
   unsigned int* sync;         // 2 x 4 x 64 counters (A lists, B lists, group barriers, Q list
                               // of each of the prologue's two launches), zeroed
   uint32_t* status;

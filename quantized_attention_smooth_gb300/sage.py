@@ -22,7 +22,8 @@ EXPORTS = (
     "sage_workspace_bytes", "sage_workspace_bytes_varlen", "sage_quant_prologue",
     "sage_quant_prologue_varlen", "sage_attn_quantized", "sage_attn_fwd",
     "sage_attn_fwd_varlen", "sage_debug_qk_int32", "sage_debug_e4m3",
-    "sage_debug_set_fault", "sage_device_status", "sage_last_error",
+    "sage_debug_set_fault", "sage_debug_set_prologue_launches", "sage_device_status",
+    "sage_last_error",
     "sage_kv_stats_noalloc", "sage_launch_count", "sage_quant_prologue_strided",
     "sage_attn_fwd_strided", "sage_quant_prologue_pv16", "sage_attn_fwd_pv16",
 )
@@ -83,6 +84,7 @@ def _load():
         "sage_debug_qk_int32": ([QP, I64, I64, I64, I64, P, P], I),
         "sage_debug_e4m3": ([P, P, I64, P], I),
         "sage_debug_set_fault": ([I, ctypes.c_uint64], None),
+        "sage_debug_set_prologue_launches": ([I], None),
         "sage_device_status": ([P, P], I),
         "sage_last_error": ([], ctypes.c_char_p),
         "sage_kv_stats_noalloc": ([P, P, I, I, I64, I64, I64, I64, P, P, P], I),
@@ -372,6 +374,11 @@ def kv_stats_noalloc(k, v, layout, k_mean, s_v, stream=None):
 
 def set_fault(skip_kv_tile: int = -1, timeout_ns: int = 0):
     _lib.sage_debug_set_fault(int(skip_kv_tile), int(timeout_ns))
+
+
+def set_prologue_launches(launches: int = 0):
+    """Test hook: 1 or 2 prologue launches, 0 to choose by size."""
+    _lib.sage_debug_set_prologue_launches(int(launches))
 
 
 def device_status(ws, stream=None) -> int:

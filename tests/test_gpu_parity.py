@@ -315,3 +315,67 @@ def test_inconsistent_cu_seqlens_reported(sage):
     ws = sage.alloc_workspace(sage.workspace_bytes_varlen(2, 300, 300, 2, 2, 64))
     sage.attn_fwd_varlen(q, q, q, out, cu, cu, 200, 200, ws=ws)
     assert sage.device_status(ws) == sage.ERR_INVALID_ARG
+
+
+# ------------------------------------------------- the prologue's two-launch plan
+# Inputs whose K and V exceed 5/4 of L2 take two prologue launches (Q tiles
+# and K/V statistics, then K/V tiles).  A test hook forces either plan, so the
+# small shapes check the two-launch plan bit-exactly against the oracle and
+# the bench shape checks that both plans write identical workspaces.
+TWO_LAUNCH = ["d1", "d128_ragged", "d80", "causal_lq_gt_lk", "gqa_nhd", "varlen_small",
+              "varlen_empty_keys"]
+
+
+@pytest.fixture
+def two_launches(sage):
+    sage.set_prologue_launches(2)
+    yield
+    sage.set_prologue_launches(0)
+
+
+@pytest.mark.parametrize("name", TWO_LAUNCH)
+def test_two_launch_prologue_bit_exact(sage, orc, two_launches, name):
+    w = next(x for x in SMALL if x.name == name)
+    inp = wl.make_inputs(w)
+    d = H.device_inputs(w, inp)
+    before = sage.launch_count()
+    _, ws = _check_prologue(sage, orc, w, inp, d)
+    assert sage.launch_count() - before == (2 if max(wl_lk(w)) > 0 else 1)
+    out = H.run_attention(sage, w, d).cpu().numpy()
+    samples = [(s, (0, w.Hq), (0, lq)) for s, (lq, lk) in enumerate(w.seg_lengths()) if lq > 0]
+    worst, cmin = _check_rows(orc, w, inp, out, samples, ws.oracle)
+    assert worst <= H.ATOL_ORACLE, worst
+    assert cmin >= H.COS_EXACT, cmin
+
+
+def wl_lk(w):
+    return [lk for lq, lk in w.seg_lengths()]
+
+
+def _workspace_fields(sage, qt):
+    nstat = qt.nseg * qt.Hkv * qt.Dp
+    shapes = {"q16": (torch.int16, (qt.q_rows, qt.Dp)), "k16": (torch.int16, (qt.k_rows, qt.Dp)),
+              "v8": (torch.uint8, (qt.v_rows, qt.v_cols)), "s_q": (torch.float32, (qt.q_rows,)),
+              "s_k": (torch.float32, (qt.k_rows // 128,)), "s_v": (torch.float32, (nstat,)),
+              "k_mean": (torch.float32, (nstat,))}
+    return {f: sage.ws_view(qt, f, dt, sh).clone() for f, (dt, sh) in shapes.items()}
+
+
+def test_prologue_plans_agree_at_bench_size(sage):
+    w = wl.WORKLOADS["b2_h24_l4096_d128"]
+    inp = wl.make_inputs(w)
+    d = H.device_inputs(w, inp)
+    got = []
+    for n in (1, 2):
+        sage.set_prologue_launches(n)
+        try:
+            before = sage.launch_count()
+            qt = H.run_prologue(sage, w, d)
+            torch.cuda.synchronize()
+            assert sage.launch_count() - before == n
+            assert sage.device_status(qt._ws) == sage.OK
+            got.append(_workspace_fields(sage, qt))
+        finally:
+            sage.set_prologue_launches(0)
+    for f in got[0]:
+        assert torch.equal(got[0][f], got[1][f]), f
