@@ -39,7 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # profiles/attn_kernel_b2_h24_l4096_d128.md (None for other workloads).
 ATTN_NCU_DRAM_BYTES = {"b2_h24_l4096_d128": 126.746624e6 + 60.900096e6}
 # the same for the FP16-PV variant's attention kernel (fp16 V and P~)
-ATTN16_NCU_DRAM_BYTES = {"b2_h24_l4096_d128": 151.875584e6 + 69.889792e6}
+ATTN16_NCU_DRAM_BYTES = {"b2_h24_l4096_d128": 152.014336e6 + 63.817216e6}
 
 
 def load_peaks():

@@ -60,25 +60,26 @@ constexpr int kSoftmaxRegs = 192;
 constexpr int kCorrRegs = 80;
 constexpr int kMiscRegs = 48;
 
-// Shared memory of one CTA.  kV16: the FP16-PV variant (fp16 P~ and V, one
-// query tile per CTA so that its larger operands fit).
+// Shared memory of one CTA.  kV16: the FP16-PV variant (fp16 P~ and V; its
+// larger operands leave room for one K and one V stage only).
 template <int DP, bool kV16 = false>
 struct Layout {
-  static constexpr int kTiles = kV16 ? 1 : 2;          // query tiles per CTA
-  static constexpr int kVStages = kV16 ? 2 : 3;        // V ring (released after a PV)
+  static constexpr int kTiles = 2;                     // query tiles per CTA
+  static constexpr int kKSt = kV16 ? 1 : kKStages;     // K ring
+  static constexpr int kVStages = kV16 ? 1 : 3;        // V ring (released after a PV)
   static constexpr int kQBytes = kBlockM * DP * 2;     // one query tile
   static constexpr int kKBytes = kBlockN * DP * 2;
   static constexpr int kVBytes = DP * kBlockN * (kV16 ? 2 : 1);
   static constexpr int kPBytes = kBlockM * kBlockN * (kV16 ? 2 : 1);   // P~ of one tile
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kTiles * kQBytes;
-  static constexpr int kVOff = kKOff + kKStages * kKBytes;
+  static constexpr int kVOff = kKOff + kKSt * kKBytes;
   static constexpr int kPOff = kVOff + kVStages * kVBytes;
   static constexpr int kBarOff = kPOff + kTiles * kPBytes;
   // q_full, k_full[SK], k_empty[SK], v_full[SV], v_empty[SV], then per tile:
   // s_full, s_free, alpha_ready[2], pv_ready, o_done, l_ready, drain, epi_full, epi_free;
   // sv_ready
-  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 * 10 + 1;
+  static constexpr int kNumBars = 1 + 2 * kKSt + 2 * kVStages + 2 * 10 + 1;
   static constexpr int kAlphaOff = (kBarOff + kNumBars * 8 + 15) / 16 * 16;
   static constexpr int kLOff = kAlphaOff + 4 * kBlockM * 4;
   static constexpr int kSvOff = kLOff + 2 * kBlockM * 4;
@@ -141,6 +142,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
             const __grid_constant__ CUtensorMap tm_v,
             const __grid_constant__ CUtensorMap tm_o, const AttnParams p) {
   using L = Layout<DP, kV16>;
+  constexpr int kKStages = L::kKSt;
   constexpr int kVStages = L::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -809,14 +811,8 @@ cudaError_t launch_attention_t(const AttnMaps& maps, const AttnParams& p,
             static_cast<unsigned>(p.g.nseg));
   AttnParams prm = p;
   prm.flat_pairs = -1;
-  if (kV16) {
-    // one query tile per CTA (dense problems only): the 1D grid of single
-    // tiles, in (segment, head, tile) order
-    const int64_t pairs = static_cast<int64_t>(grid.x) * grid.y * grid.z;
-    if (p.g.varlen || 2 * pairs >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
-    prm.flat_pairs = 0;
-    grid = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
-  } else if (!p.g.varlen && !p.causal) {
+  if (kV16 && p.g.varlen) return cudaErrorInvalidValue;    // dense problems only
+  if (!p.g.varlen && !p.causal) {
     // Uniform pairs run in waves of one CTA per SM.  When the last wave is
     // at most half full, its pairs run as single tiles instead (launched
     // last), which shortens that wave to one tile's time.

@@ -64,7 +64,7 @@ struct AttnParams {
   float scale_log2;          // sm_scale * log2(e)
   int32_t causal;
   int32_t skip_kv_tile;      // failure-injection hook, -1 = off
-  int32_t v16;               // FP16-PV variant: V and P~ in fp16, one query tile per CTA
+  int32_t v16;               // FP16-PV variant: V and P~ in fp16, single-stage K and V rings
   int32_t out_tma;           // output map: 0 none (per-row stores), 1 dense HND,
                              // 2 dense NHD, 3 packed (varlen)
   int32_t flat_pairs;        // >= 0: 1D grid of this many pairs, then single tiles;
