@@ -291,9 +291,10 @@ def job_figures(r: dict, world: int, steps: int) -> dict:
 
 
 # ---------------------------------------------------------- CPU oracle arm
-def oracle_sample(w: wl.Workload, inp: dict, rows: int, heads: int = 1):
-    """Times the oracle (prologue + attention) on `heads` query heads of segment 0
-    and its first `rows` query rows; returns (ops, seconds, threads)."""
+def oracle_sample(w: wl.Workload, inp: dict, rows: int, heads: int = 1, pv16: bool = False):
+    """Times the oracle (prologue + attention; the FP16-PV variant's when pv16)
+    on `heads` query heads of segment 0 and its first `rows` query rows;
+    returns (ops, seconds, threads)."""
     import oracle
     q, k, v = wl.segment(w, inp, 0)
     # query head 0 reads kv head 0 for every GQA grouping
@@ -304,7 +305,11 @@ def oracle_sample(w: wl.Workload, inp: dict, rows: int, heads: int = 1):
     rows = min(rows, lq)
     t0 = time.perf_counter()
     pro = oracle.prologue(qs, ks, vs, w.dtype)
-    oracle.attn(pro, w.causal, wl.default_sm_scale(w), rows=(0, rows))
+    if pv16:
+        oracle.attn_pv16(pro, oracle.v16(vs, w.dtype), w.causal, wl.default_sm_scale(w),
+                         rows=(0, rows))
+    else:
+        oracle.attn(pro, w.causal, wl.default_sm_scale(w), rows=(0, rows))
     dt = time.perf_counter() - t0
     if w.causal:
         # the sample's unmasked work, restated in the metric's literal count
@@ -324,11 +329,12 @@ def reference_arm(args, w: wl.Workload, rank: int, world: int):
     oracle.build()
     inp = wl.make_inputs(w)
     rows = args.ref_rows
+    pv16 = args.variant == "pv16"
     for _ in range(args.warmup):
-        oracle_sample(w, inp, min(rows, 128))
+        oracle_sample(w, inp, min(rows, 128), pv16=pv16)
     tot_ops, tot_s = 0.0, 0.0
     for _ in range(args.steps):
-        ops, dt, cores = oracle_sample(w, inp, rows)
+        ops, dt, cores = oracle_sample(w, inp, rows, pv16=pv16)
         tot_ops += ops
         tot_s += dt
     tops = tot_ops / tot_s / 1e12
@@ -338,8 +344,9 @@ def reference_arm(args, w: wl.Workload, rank: int, world: int):
         "impl": "reference", "metric": METRIC, "value": tops, "unit": "TOPS",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": tot_s / args.steps * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int8+e4m3 (fp32 softmax)",
-        "data": "synthetic", "config": config_of(w),
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8+fp16 (fp32 softmax)" if pv16 else "int8+e4m3 (fp32 softmax)",
+        "data": "synthetic", "config": dict(config_of(w), variant=args.variant),
         "cpu_baseline": {"value": tops, "unit": "TOPS", "cores": os.cpu_count(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": tops, "unit": "TOPS", "h2d_bytes_per_step": 0,
@@ -400,7 +407,7 @@ def main():
     tops = fig["value"]
     pro_gbs = prologue_bytes(w, 2 if pv16 else 1) / (r["pro_ms"] * 1e-3) / 1e9
     inp = wl.make_inputs(w)
-    cpu_ops, cpu_s, cores = oracle_sample(w, inp, args.cpu_rows)
+    cpu_ops, cpu_s, cores = oracle_sample(w, inp, args.cpu_rows, pv16=pv16)
     line = {
         "metric": METRIC, "value": tops, "unit": "TOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,

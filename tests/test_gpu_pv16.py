@@ -107,3 +107,14 @@ def test_pv16_small_shapes(sage, orc, w):
 def test_pv16_bench_shape_sampled_rows(sage, orc):
     w = wl.WORKLOADS["b2_h24_l4096_d128"]
     _check(sage, orc, w, rows_of=lambda lq: (lq - 200, lq))
+
+
+def test_pv16_two_launch_prologue(sage, orc):
+    """The prologue's two-launch plan (forced) writes the same fp16 V and
+    Q/K operands, bit-exactly, and the outputs keep the tolerance."""
+    sage.set_prologue_launches(2)
+    try:
+        _check(sage, orc, _w("pv16_two_launch", Lq=300, Lk=333, D=128, seed=507,
+                             dtype=wl.BF16))
+    finally:
+        sage.set_prologue_launches(0)

@@ -118,3 +118,12 @@ def test_strided_views_bit_exact_and_outputs(sage, orc, c):
     again = sage.sageattn(q, k, v, lay, w.causal, scale)
     torch.cuda.synchronize()
     assert torch.equal(again, out)
+
+
+def test_strided_views_two_launch_prologue(sage, orc):
+    """Strided views through the prologue's two-launch plan (forced)."""
+    sage.set_prologue_launches(2)
+    try:
+        test_strided_views_bit_exact_and_outputs(sage, orc, CASES[2])
+    finally:
+        sage.set_prologue_launches(0)
