@@ -2,13 +2,15 @@
 
 Each test ties one step of the oracle to a closed form, an invariant, a
 brute-force search, a library routine (math.fsum, torch SDPA in float64) or
-the accuracy the pages report for the FP8-PV path (cosine >= 0.99926 against
-float64 attention on the SageAttention 2.2.0 sm_120a wheel page, accuracy
-table).  They are chosen so that a plausible slip in the oracle (a dropped
+the accuracy the pages report for the FP8-PV and FP16-PV paths (the
+SageAttention 2.2.0 sm_120a wheel page's accuracy table against float64
+attention, stored with its citation in tests/golden/accuracy_table.json).  They are chosen so that a plausible slip in the oracle (a dropped
 rescale, a wrong block index, a transposed operand, a wrong mean axis, a
 wrong rounding tie) fails at least one of them.
 """
+import json
 import math
+from pathlib import Path
 
 import numpy as np
 import pytest
@@ -17,6 +19,10 @@ import torch
 from quantized_attention_smooth_gb300 import workloads as wl
 
 pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+# The pages' accuracy table (tests/golden/accuracy_table.json names the page).
+ACCURACY = json.loads((Path(__file__).parent / "golden" / "accuracy_table.json")
+                      .read_text())["backends"]
 
 
 # ------------------------------------------------------------------ e4m3
@@ -259,8 +265,11 @@ def test_quantized_attention_accuracy(orc, causal, Hq, Hkv, Lq, Lk, D, dtype):
     np.testing.assert_allclose(ref, ref_t, atol=1e-10)
     c = _cos(got, ref)
     r = _rel_l2(got, ref)
-    assert c >= 0.9992, c
-    assert r <= 0.05, r
+    t8 = ACCURACY["qk_int8_pv_fp8"]
+    # heterogeneous scales and a K offset: the table's cosine less 1e-4, and
+    # up to 1.3x its worst relative error
+    assert c >= t8["cos_min"] - 1e-4, c
+    assert r <= 1.3 * t8["rel_l2"][1], r
     assert np.all(np.isfinite(got))
 
 
@@ -478,10 +487,13 @@ def test_pv16_accuracy_matches_the_pages_table(orc, causal, Hq, Hkv, Lq, Lk, D, 
     got8 = orc.attn(p, causal, scale)
     ref = orc.attn_exact(q, k, v, dtype, causal, scale)
     r16, r8 = _rel_l2(got16, ref), _rel_l2(got8, ref)
-    assert 0.008 <= r16 <= 0.0118, r16
-    assert 0.030 <= r8 <= 0.040, r8
+    t16, t8 = ACCURACY["qk_int8_pv_fp16"], ACCURACY["qk_int8_pv_fp8"]
+    # the table's ranges, widened 15 % below and 5 % above for other inputs
+    assert 0.85 * t16["rel_l2"][0] <= r16 <= 1.05 * t16["rel_l2"][1], r16
+    assert 0.85 * t8["rel_l2"][0] <= r8 <= 1.05 * t8["rel_l2"][1], r8
+    # FP8 PV carries several times the FP16 PV error (the table: about 3.4x)
     assert r8 / r16 >= 2.5, (r8, r16)
-    assert _cos(got16, ref) >= 0.99993, _cos(got16, ref)
+    assert _cos(got16, ref) >= t16["cos_min"] - 1e-5, _cos(got16, ref)
     assert np.all(np.isfinite(got16))
 
 
