@@ -415,6 +415,63 @@ int64_t out_elems_dense(int64_t B, int64_t Hq, int64_t Lq, int64_t D) {
 
 }  // namespace
 
+namespace {
+
+// Dense prologue entry points (e4m3 V, or fp16 V for the FP16-PV variant).
+sage_status dense_prologue(const void* q, const void* k, const void* v, int dtype, int layout,
+                           int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk,
+                           int64_t D, void* ws, size_t ws_bytes, sage_quantized* qt,
+                           sage_stream_t stream, bool v16) {
+  if (qt == nullptr) return fail(SAGE_ERR_INVALID_ARG, "qt must not be null");
+  sage_status s = SAGE_OK;
+  if (layout != SAGE_HND && layout != SAGE_NHD)
+    return fail(SAGE_ERR_INVALID_ARG, "layout %d is neither SAGE_HND nor SAGE_NHD", layout);
+  if (B < 0 || Lq < 0 || Lk < 0)
+    return fail(SAGE_ERR_INVALID_ARG, "negative size (B=%lld Lq=%lld Lk=%lld)",
+                (long long)B, (long long)Lq, (long long)Lk);
+  if (!check_dims(Hq, Hkv, D, &s)) return s;
+  if ((s = check_common(q, k, v, dtype)) != SAGE_OK) return s;
+  if (B == 0 || Lq == 0 || Lk == 0)
+    return fail(SAGE_ERR_INVALID_ARG, "the prologue needs B, Lq and Lk > 0");
+  return run_prologue(dense_geo(B, Hq, Hkv, Lq, Lk, D, dtype, layout), q, k, v, ws,
+                      ws_bytes, qt, reinterpret_cast<cudaStream_t>(stream), v16);
+}
+
+// Dense one-call entry points: prologue and attention, or zeros for an empty
+// key set.
+sage_status dense_fwd(const void* q, const void* k, const void* v, float* out, int64_t B,
+                      int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk, int64_t D, int layout,
+                      int is_causal, float sm_scale, int dtype, void* ws, size_t ws_bytes,
+                      sage_stream_t stream, bool v16) {
+  sage_status s = SAGE_OK;
+  if (layout != SAGE_HND && layout != SAGE_NHD)
+    return fail(SAGE_ERR_INVALID_ARG, "layout %d is neither SAGE_HND nor SAGE_NHD", layout);
+  if (B < 0 || Lq < 0 || Lk < 0)
+    return fail(SAGE_ERR_INVALID_ARG, "negative size (B=%lld Lq=%lld Lk=%lld)",
+                (long long)B, (long long)Lq, (long long)Lk);
+  if (!check_dims(Hq, Hkv, D, &s)) return s;
+  if (B == 0 || Lq == 0) return ok();                 // nothing to compute
+  // an empty key tensor may legitimately have null data pointers
+  if ((s = check_common(q, Lk == 0 ? q : k, Lk == 0 ? q : v, dtype)) != SAGE_OK) return s;
+  if (out == nullptr || !aligned(out, 4))
+    return fail(SAGE_ERR_INVALID_ARG, "out must be a 4-byte aligned device pointer");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (Lk == 0) {                                      // empty softmax: zeros
+    if ((s = check_device()) != SAGE_OK) return s;
+    cudaError_t e = cudaMemsetAsync(out, 0, out_elems_dense(B, Hq, Lq, D) * 4, st);
+    return e == cudaSuccess ? ok() : cuda_fail(e, "cudaMemsetAsync");
+  }
+  sage_quantized qt;
+  s = run_prologue(dense_geo(B, Hq, Hkv, Lq, Lk, D, dtype, layout), q, k, v, ws, ws_bytes,
+                   &qt, st, v16);
+  if (s != SAGE_OK) return s;
+  if (qt.nseg > 65535 || qt.Hq > 65535)
+    return fail(SAGE_ERR_UNSUPPORTED, "more than 65535 segments or heads");
+  return launch_attn(&qt, out, layout, is_causal, sm_scale, st);
+}
+
+}  // namespace
+
 extern "C" {
 
 size_t sage_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk,
@@ -438,19 +495,8 @@ sage_status sage_quant_prologue(const void* q, const void* k, const void* v, int
                                 int64_t Lq, int64_t Lk, int64_t D, void* ws,
                                 size_t ws_bytes, sage_quantized* qt,
                                 sage_stream_t stream) {
-  if (qt == nullptr) return fail(SAGE_ERR_INVALID_ARG, "qt must not be null");
-  sage_status s = SAGE_OK;
-  if (layout != SAGE_HND && layout != SAGE_NHD)
-    return fail(SAGE_ERR_INVALID_ARG, "layout %d is neither SAGE_HND nor SAGE_NHD", layout);
-  if (B < 0 || Lq < 0 || Lk < 0)
-    return fail(SAGE_ERR_INVALID_ARG, "negative size (B=%lld Lq=%lld Lk=%lld)",
-                (long long)B, (long long)Lq, (long long)Lk);
-  if (!check_dims(Hq, Hkv, D, &s)) return s;
-  if ((s = check_common(q, k, v, dtype)) != SAGE_OK) return s;
-  if (B == 0 || Lq == 0 || Lk == 0)
-    return fail(SAGE_ERR_INVALID_ARG, "the prologue needs B, Lq and Lk > 0");
-  return run_prologue(dense_geo(B, Hq, Hkv, Lq, Lk, D, dtype, layout), q, k, v, ws,
-                      ws_bytes, qt, reinterpret_cast<cudaStream_t>(stream));
+  return dense_prologue(q, k, v, dtype, layout, B, Hq, Hkv, Lq, Lk, D, ws, ws_bytes, qt,
+                        stream, false);
 }
 
 sage_status sage_quant_prologue_pv16(const void* q, const void* k, const void* v, int dtype,
@@ -458,19 +504,8 @@ sage_status sage_quant_prologue_pv16(const void* q, const void* k, const void* v
                                      int64_t Lq, int64_t Lk, int64_t D, void* ws,
                                      size_t ws_bytes, sage_quantized* qt,
                                      sage_stream_t stream) {
-  if (qt == nullptr) return fail(SAGE_ERR_INVALID_ARG, "qt must not be null");
-  sage_status s = SAGE_OK;
-  if (layout != SAGE_HND && layout != SAGE_NHD)
-    return fail(SAGE_ERR_INVALID_ARG, "layout %d is neither SAGE_HND nor SAGE_NHD", layout);
-  if (B < 0 || Lq < 0 || Lk < 0)
-    return fail(SAGE_ERR_INVALID_ARG, "negative size (B=%lld Lq=%lld Lk=%lld)",
-                (long long)B, (long long)Lq, (long long)Lk);
-  if (!check_dims(Hq, Hkv, D, &s)) return s;
-  if ((s = check_common(q, k, v, dtype)) != SAGE_OK) return s;
-  if (B == 0 || Lq == 0 || Lk == 0)
-    return fail(SAGE_ERR_INVALID_ARG, "the prologue needs B, Lq and Lk > 0");
-  return run_prologue(dense_geo(B, Hq, Hkv, Lq, Lk, D, dtype, layout), q, k, v, ws,
-                      ws_bytes, qt, reinterpret_cast<cudaStream_t>(stream), true);
+  return dense_prologue(q, k, v, dtype, layout, B, Hq, Hkv, Lq, Lk, D, ws, ws_bytes, qt,
+                        stream, true);
 }
 
 sage_status sage_quant_prologue_varlen(const void* q, const void* k, const void* v,
@@ -538,61 +573,16 @@ sage_status sage_attn_fwd(const void* q, const void* k, const void* v, float* ou
                           int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk,
                           int64_t D, int layout, int is_causal, float sm_scale, int dtype,
                           void* ws, size_t ws_bytes, sage_stream_t stream) {
-  sage_status s = SAGE_OK;
-  if (layout != SAGE_HND && layout != SAGE_NHD)
-    return fail(SAGE_ERR_INVALID_ARG, "layout %d is neither SAGE_HND nor SAGE_NHD", layout);
-  if (B < 0 || Lq < 0 || Lk < 0)
-    return fail(SAGE_ERR_INVALID_ARG, "negative size (B=%lld Lq=%lld Lk=%lld)",
-                (long long)B, (long long)Lq, (long long)Lk);
-  if (!check_dims(Hq, Hkv, D, &s)) return s;
-  if (B == 0 || Lq == 0) return ok();                 // nothing to compute
-  // an empty key tensor may legitimately have null data pointers
-  if ((s = check_common(q, Lk == 0 ? q : k, Lk == 0 ? q : v, dtype)) != SAGE_OK) return s;
-  if (out == nullptr || !aligned(out, 4))
-    return fail(SAGE_ERR_INVALID_ARG, "out must be a 4-byte aligned device pointer");
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (Lk == 0) {                                      // empty softmax: zeros
-    if ((s = check_device()) != SAGE_OK) return s;
-    cudaError_t e = cudaMemsetAsync(out, 0, out_elems_dense(B, Hq, Lq, D) * 4, st);
-    return e == cudaSuccess ? ok() : cuda_fail(e, "cudaMemsetAsync");
-  }
-  sage_quantized qt;
-  s = run_prologue(dense_geo(B, Hq, Hkv, Lq, Lk, D, dtype, layout), q, k, v, ws, ws_bytes,
-                   &qt, st);
-  if (s != SAGE_OK) return s;
-  if (qt.nseg > 65535 || qt.Hq > 65535)
-    return fail(SAGE_ERR_UNSUPPORTED, "more than 65535 segments or heads");
-  return launch_attn(&qt, out, layout, is_causal, sm_scale, st);
+  return dense_fwd(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, layout, is_causal, sm_scale, dtype,
+                   ws, ws_bytes, stream, false);
 }
 
 sage_status sage_attn_fwd_pv16(const void* q, const void* k, const void* v, float* out,
                                int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk,
                                int64_t D, int layout, int is_causal, float sm_scale,
                                int dtype, void* ws, size_t ws_bytes, sage_stream_t stream) {
-  sage_status s = SAGE_OK;
-  if (layout != SAGE_HND && layout != SAGE_NHD)
-    return fail(SAGE_ERR_INVALID_ARG, "layout %d is neither SAGE_HND nor SAGE_NHD", layout);
-  if (B < 0 || Lq < 0 || Lk < 0)
-    return fail(SAGE_ERR_INVALID_ARG, "negative size (B=%lld Lq=%lld Lk=%lld)",
-                (long long)B, (long long)Lq, (long long)Lk);
-  if (!check_dims(Hq, Hkv, D, &s)) return s;
-  if (B == 0 || Lq == 0) return ok();                 // nothing to compute
-  if ((s = check_common(q, Lk == 0 ? q : k, Lk == 0 ? q : v, dtype)) != SAGE_OK) return s;
-  if (out == nullptr || !aligned(out, 4))
-    return fail(SAGE_ERR_INVALID_ARG, "out must be a 4-byte aligned device pointer");
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (Lk == 0) {                                      // empty softmax: zeros
-    if ((s = check_device()) != SAGE_OK) return s;
-    cudaError_t e = cudaMemsetAsync(out, 0, out_elems_dense(B, Hq, Lq, D) * 4, st);
-    return e == cudaSuccess ? ok() : cuda_fail(e, "cudaMemsetAsync");
-  }
-  sage_quantized qt;
-  s = run_prologue(dense_geo(B, Hq, Hkv, Lq, Lk, D, dtype, layout), q, k, v, ws, ws_bytes,
-                   &qt, st, true);
-  if (s != SAGE_OK) return s;
-  if (qt.nseg > 65535 || qt.Hq > 65535)
-    return fail(SAGE_ERR_UNSUPPORTED, "more than 65535 segments or heads");
-  return launch_attn(&qt, out, layout, is_causal, sm_scale, st);
+  return dense_fwd(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, layout, is_causal, sm_scale, dtype,
+                   ws, ws_bytes, stream, true);
 }
 
 sage_status sage_attn_fwd_strided(const void* q, const void* k, const void* v, float* out,
