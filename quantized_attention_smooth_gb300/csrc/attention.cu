@@ -798,12 +798,17 @@ template <int DP, bool kV16>
 cudaError_t launch_attention_t(const AttnMaps& maps, const AttnParams& p,
                                cudaStream_t st) {
   using L = Layout<DP, kV16>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(
-        attn_kernel<DP, kV16>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (e != cudaSuccess) return e;
-    configured = true;
+  // the shared-memory limit is a per-device attribute of the kernel
+  static bool configured[64] = {};
+  int cdev = 0;
+  cudaError_t ce = cudaGetDevice(&cdev);
+  if (ce != cudaSuccess) return ce;
+  if (cdev < 0 || cdev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[cdev]) {
+    ce = cudaFuncSetAttribute(attn_kernel<DP, kV16>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (ce != cudaSuccess) return ce;
+    configured[cdev] = true;
   }
   const int64_t maxq = p.g.varlen ? p.g.max_q : p.g.Lq;
   const int64_t nqt = (maxq + kBlockM - 1) / kBlockM;      // query tiles, two per CTA
@@ -847,12 +852,16 @@ template <int DP>
 cudaError_t launch_debug_qk_t(const AttnMaps& maps, const AttnParams& p,
                               int64_t q_row0, int64_t k_row0, int32_t* out,
                               cudaStream_t st) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(
-        debug_qk_kernel<DP>, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<DP>::kAlloc);
+  static bool configured[64] = {};            // per-device kernel attribute
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(debug_qk_kernel<DP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Layout<DP>::kAlloc);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev] = true;
   }
   debug_qk_kernel<DP><<<1, 128, Layout<DP>::kAlloc, st>>>(maps.q, maps.k, q_row0, k_row0,
                                                           out, p.status, p.timeout_ns);
