@@ -137,6 +137,27 @@ def _dtype_code(t) -> int:
     raise TypeError(f"q/k/v must be float16 or bfloat16, got {t.dtype}")
 
 
+def _require_dense(where, q, k, v, out=None):
+    """The dense and packed entry points read q, k, v (and write out) as
+    contiguous arrays of one dtype on a CUDA device.  Anything else is
+    refused here, before any call: a view must go through the *_strided
+    calls, which take its strides."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda:
+            raise ValueError(f"{where}: {name} is not on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError(f"{where}: {name} is not contiguous; pass views to "
+                             f"quant_prologue_strided / attn_fwd_strided")
+        if t.dtype != q.dtype:
+            raise TypeError(f"{where}: {name} is {t.dtype}, q is {q.dtype}")
+    if out is not None:
+        import torch
+        if not out.is_cuda or not out.is_contiguous() or out.dtype != torch.float32:
+            raise ValueError(f"{where}: out must be a contiguous float32 CUDA tensor")
+        if tuple(out.shape) != tuple(q.shape):
+            raise ValueError(f"{where}: out has shape {tuple(out.shape)}, q {tuple(q.shape)}")
+
+
 def _layout_code(layout) -> int:
     if layout in (HND, "HND"):
         return HND
@@ -169,6 +190,7 @@ def alloc_workspace(nbytes: int, device="cuda"):
 
 
 def quant_prologue(q, k, v, layout="HND", ws=None, stream=None) -> Quantized:
+    _require_dense("quant_prologue", q, k, v)
     lay = _layout_code(layout)
     B, Hq, Hkv, Lq, Lk, D = _dims(q, k, lay)
     if ws is None:
@@ -184,6 +206,7 @@ def quant_prologue(q, k, v, layout="HND", ws=None, stream=None) -> Quantized:
 
 def quant_prologue_pv16(q, k, v, layout="HND", ws=None, stream=None) -> Quantized:
     """Prologue of the FP16-PV variant: INT8 Q/K as usual, V kept in fp16."""
+    _require_dense("quant_prologue_pv16", q, k, v)
     lay = _layout_code(layout)
     B, Hq, Hkv, Lq, Lk, D = _dims(q, k, lay)
     if ws is None:
@@ -198,6 +221,7 @@ def quant_prologue_pv16(q, k, v, layout="HND", ws=None, stream=None) -> Quantize
 
 
 def quant_prologue_varlen(q, k, v, cu_q, cu_k, max_q, max_k, ws=None, stream=None):
+    _require_dense("quant_prologue_varlen", q, k, v)
     total_q, Hq, D = q.shape
     total_k, Hkv, _ = k.shape
     nseq = cu_q.numel() - 1
@@ -225,6 +249,7 @@ def attn_quantized(qt: Quantized, out, layout="HND", is_causal=False, sm_scale=N
 
 def attn_fwd(q, k, v, out, layout="HND", is_causal=False, sm_scale=None, ws=None,
              stream=None):
+    _require_dense("attn_fwd", q, k, v, out)
     lay = _layout_code(layout)
     B, Hq, Hkv, Lq, Lk, D = _dims(q, k, lay)
     if ws is None:
@@ -239,6 +264,7 @@ def attn_fwd(q, k, v, out, layout="HND", is_causal=False, sm_scale=None, ws=None
 def attn_fwd_pv16(q, k, v, out, layout="HND", is_causal=False, sm_scale=None, ws=None,
                  stream=None):
     """Prologue + FP16-PV attention (dense)."""
+    _require_dense("attn_fwd_pv16", q, k, v, out)
     lay = _layout_code(layout)
     B, Hq, Hkv, Lq, Lk, D = _dims(q, k, lay)
     if ws is None:
@@ -252,6 +278,7 @@ def attn_fwd_pv16(q, k, v, out, layout="HND", is_causal=False, sm_scale=None, ws
 
 def attn_fwd_varlen(q, k, v, out, cu_q, cu_k, max_q, max_k, is_causal=False,
                     sm_scale=None, ws=None, stream=None):
+    _require_dense("attn_fwd_varlen", q, k, v, out)
     total_q, Hq, D = q.shape
     total_k, Hkv, _ = k.shape
     nseq = cu_q.numel() - 1

@@ -144,3 +144,18 @@ def test_view_strides_of_fused_projection_slices():
     assert sage.view_strides(t, "HND") == (H * L * 2 * D, L * 2 * D, 2 * D)
     with pytest.raises(ValueError, match="contiguous channels"):
         sage.view_strides(torch.empty(B, H, L, D, dtype=torch.float16).transpose(2, 3), "HND")
+
+
+def test_binding_refuses_tensors_it_would_misread():
+    """The dense wrappers refuse tensors they would read wrongly (host-side,
+    before any call): not on a CUDA device, and (on a GPU) not contiguous,
+    mixed dtypes or a wrong output."""
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 2, 128, 64, dtype=torch.float16)
+    out = torch.zeros(1, 2, 128, 64, dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA"):
+        sage.attn_fwd(q, q, q, out)
+    with pytest.raises(ValueError, match="CUDA"):
+        sage.quant_prologue(q, q, q)
+    with pytest.raises(ValueError, match="CUDA"):
+        sage.quant_prologue_pv16(q, q, q)

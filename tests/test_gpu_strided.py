@@ -127,3 +127,21 @@ def test_strided_views_two_launch_prologue(sage, orc):
         test_strided_views_bit_exact_and_outputs(sage, orc, CASES[2])
     finally:
         sage.set_prologue_launches(0)
+
+
+def test_dense_wrappers_refuse_views_and_mixed_dtypes(sage):
+    """A view passed to a dense wrapper would be read as if contiguous: the
+    binding refuses it (pointing at the strided calls), as it refuses mixed
+    q/k/v dtypes and an output of the wrong type or shape."""
+    fused = torch.zeros(1, 128, 3, 2, 64, dtype=torch.float16, device="cuda")
+    q, k, v = fused.unbind(2)
+    out = torch.zeros(q.shape, dtype=torch.float32, device="cuda")
+    with pytest.raises(ValueError, match="strided"):
+        sage.attn_fwd(q, k, v, out, "NHD")
+    with pytest.raises(ValueError, match="strided"):
+        sage.quant_prologue(q, k, v, "NHD")
+    qc, kc = q.contiguous(), k.contiguous()
+    with pytest.raises(TypeError):
+        sage.attn_fwd(qc, kc.to(torch.bfloat16), v.contiguous(), out, "NHD")
+    with pytest.raises(ValueError, match="out"):
+        sage.attn_fwd(qc, kc, v.contiguous(), out.half(), "NHD")
