@@ -200,6 +200,30 @@ SAGE_API sage_status sage_attn_fwd_pv16(const void* q, const void* k, const void
                                int is_causal, float sm_scale, int dtype, void* ws,
                                size_t ws_bytes, sage_stream_t stream);
 
+/* Host-buffer call: sage_attn_fwd on q, k, v and out in HOST memory (dense
+ * HND or NHD, same arguments and conventions), with the host<->device copies
+ * inside.  The problem is cut into chunks of (one batch entry, chunk_kv_heads
+ * kv heads with their query heads); 0 picks enough kv heads for one wave of
+ * query-tile pairs per chunk.  Chunk i+1's inputs are copied into device
+ * staging while chunk i is computed on `stream` and chunk i-1's output is
+ * copied back, on two copy streams the library creates once per device and
+ * keeps.  Attention never mixes heads or batch entries, so the output equals
+ * one sage_attn_fwd call's.
+ *   ws: device workspace of sage_workspace_bytes_host(...) bytes (the chunk
+ *       prologue's workspace and two staging slots).
+ *   Host buffers should be page-locked for the copies to overlap; the call
+ *   returns once everything is enqueued, and `stream` completes when every
+ *   output row is in `out`.  Calls on one device enqueue one at a time.
+ *   Lk = 0 is refused (use sage_attn_fwd); B = 0 or Lq = 0 does nothing. */
+SAGE_API size_t sage_workspace_bytes_host(int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq,
+                                          int64_t Lk, int64_t D, int64_t chunk_kv_heads);
+SAGE_API sage_status sage_attn_fwd_host(const void* q, const void* k, const void* v,
+                                        float* out, int64_t B, int64_t Hq, int64_t Hkv,
+                                        int64_t Lq, int64_t Lk, int64_t D, int layout,
+                                        int is_causal, float sm_scale, int dtype,
+                                        int64_t chunk_kv_heads, void* ws, size_t ws_bytes,
+                                        sage_stream_t stream);
+
 /* Prologue + attention in one call on strided views (see
  * sage_quant_prologue_strided); out is dense fp32 in `layout`. */
 SAGE_API sage_status sage_attn_fwd_strided(

@@ -11,6 +11,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "sage.h"
@@ -472,6 +473,110 @@ sage_status dense_fwd(const void* q, const void* k, const void* v, float* out, i
 
 }  // namespace
 
+
+// ------------------------------------------------ host-buffer pipeline
+// sage_attn_fwd_host cuts a dense problem into (batch, kv-head group) chunks
+// and pipelines them: the copy of chunk i+1 into device staging runs on one
+// stream while chunk i's prologue and attention run on the caller's stream
+// and chunk i-1's output is copied back on a third.  Two staging slots
+// alternate; events order every reuse.  Attention never mixes heads or
+// batches, so the result is the same as one sage_attn_fwd call.
+namespace {
+
+struct HostPlan {
+  int64_t chunk_kv;          // kv heads per chunk
+  int64_t group;             // query heads per kv head
+  size_t ws_bytes;           // prologue workspace of one chunk (offset 0)
+  size_t q_bytes, kv_bytes, out_bytes;   // one chunk's q, k (= v), out
+  size_t slot[2];            // offsets of the two staging slots
+  size_t total;
+};
+
+int sm_count_of_current_device() {
+  static int sms[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    sms[dev] = n;
+  }
+  return sms[dev];
+}
+
+// chunk_kv <= 0 picks enough kv heads for one wave of query-tile pairs per
+// chunk (one per SM), so that each chunk's attention still fills the GPU.
+HostPlan host_plan(int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk, int64_t D,
+                   int64_t chunk_kv) {
+  HostPlan P{};
+  P.group = Hq / Hkv;
+  if (chunk_kv <= 0) {
+    const int64_t pairs = P.group * (((Lq + 127) / 128 + 1) / 2);
+    const int64_t sms = sm_count_of_current_device() > 0 ? sm_count_of_current_device() : 152;
+    chunk_kv = pairs > 0 ? (sms + pairs - 1) / pairs : Hkv;
+  }
+  P.chunk_kv = chunk_kv < 1 ? 1 : (chunk_kv > Hkv ? Hkv : chunk_kv);
+  const int64_t hq = P.chunk_kv * P.group;
+  P.q_bytes = static_cast<size_t>(hq * Lq * D * 2);
+  P.kv_bytes = static_cast<size_t>(P.chunk_kv * Lk * D * 2);
+  P.out_bytes = static_cast<size_t>(hq * Lq * D * 4);
+  P.ws_bytes = align256(sage_workspace_bytes(1, hq, P.chunk_kv, Lq, Lk, D));
+  const size_t per_slot = align256(P.q_bytes) + 2 * align256(P.kv_bytes) + align256(P.out_bytes);
+  P.slot[0] = P.ws_bytes;
+  P.slot[1] = P.ws_bytes + per_slot;
+  P.total = P.ws_bytes + 2 * per_slot;
+  return P;
+}
+
+// Copy streams and events of the pipeline, created once per device and kept
+// for the process (like the kernels' attributes); calls on one device enqueue
+// one at a time.
+struct HostRuntime {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, loaded[2] = {}, computed[2] = {}, stored[2] = {};
+};
+
+HostRuntime g_host_rt[64];
+
+cudaError_t host_runtime_init(HostRuntime& rt) {
+  if (rt.ready) return cudaSuccess;
+  cudaError_t e = cudaStreamCreateWithFlags(&rt.in, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&rt.out, cudaStreamNonBlocking);
+  cudaEvent_t* evs[] = {&rt.start, &rt.loaded[0], &rt.loaded[1], &rt.computed[0],
+                        &rt.computed[1], &rt.stored[0], &rt.stored[1]};
+  for (cudaEvent_t* ev : evs)
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+  if (e == cudaSuccess) rt.ready = true;
+  return e;
+}
+
+// One chunk's rows of a dense tensor between host and device staging:
+// contiguous for HND, a pitched copy (Lq rows of the chunk's heads) for NHD.
+cudaError_t copy_chunk(void* dst, const void* src, bool to_device, bool hnd, int64_t b,
+                       int64_t h0, int64_t hn, int64_t H, int64_t L, int64_t D,
+                       size_t elem, cudaStream_t st) {
+  const cudaMemcpyKind kind = to_device ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToHost;
+  if (hnd) {
+    const size_t off = static_cast<size_t>((b * H + h0) * L * D) * elem;
+    const size_t n = static_cast<size_t>(hn * L * D) * elem;
+    return to_device
+               ? cudaMemcpyAsync(dst, static_cast<const char*>(src) + off, n, kind, st)
+               : cudaMemcpyAsync(static_cast<char*>(dst) + off, src, n, kind, st);
+  }
+  const size_t host_pitch = static_cast<size_t>(H * D) * elem;
+  const size_t dev_pitch = static_cast<size_t>(hn * D) * elem;
+  const size_t off = static_cast<size_t>((b * L * H + h0) * D) * elem;
+  return to_device
+             ? cudaMemcpy2DAsync(dst, dev_pitch, static_cast<const char*>(src) + off, host_pitch,
+                                 dev_pitch, static_cast<size_t>(L), kind, st)
+             : cudaMemcpy2DAsync(static_cast<char*>(dst) + off, host_pitch, src, dev_pitch,
+                                 dev_pitch, static_cast<size_t>(L), kind, st);
+}
+
+}  // namespace
+
 extern "C" {
 
 size_t sage_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk,
@@ -735,6 +840,92 @@ sage_status sage_kv_stats_noalloc(const void* k, const void* v, int dtype, int l
                                          reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "static-scratch statistics");
   return ok();
+}
+
+size_t sage_workspace_bytes_host(int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk,
+                                 int64_t D, int64_t chunk_kv_heads) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lk <= 0 || D < 1 || D > 128 ||
+      Hq % Hkv != 0)
+    return 0;
+  return host_plan(Hq, Hkv, Lq, Lk, D, chunk_kv_heads).total;
+}
+
+sage_status sage_attn_fwd_host(const void* q, const void* k, const void* v, float* out,
+                               int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk,
+                               int64_t D, int layout, int is_causal, float sm_scale,
+                               int dtype, int64_t chunk_kv_heads, void* ws, size_t ws_bytes,
+                               sage_stream_t stream) {
+  sage_status s = SAGE_OK;
+  if (layout != SAGE_HND && layout != SAGE_NHD)
+    return fail(SAGE_ERR_INVALID_ARG, "layout %d is neither SAGE_HND nor SAGE_NHD", layout);
+  if (B < 0 || Lq < 0 || Lk < 0)
+    return fail(SAGE_ERR_INVALID_ARG, "negative size (B=%lld Lq=%lld Lk=%lld)",
+                (long long)B, (long long)Lq, (long long)Lk);
+  if (!check_dims(Hq, Hkv, D, &s)) return s;
+  if (dtype != SAGE_F16 && dtype != SAGE_BF16)
+    return fail(SAGE_ERR_INVALID_ARG, "dtype %d is neither SAGE_F16 nor SAGE_BF16", dtype);
+  if (B == 0 || Lq == 0) return ok();                 // nothing to compute
+  if (Lk == 0)
+    return fail(SAGE_ERR_INVALID_ARG, "the host-buffer call needs Lk > 0");
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr)
+    return fail(SAGE_ERR_INVALID_ARG, "null host buffer");
+  if ((s = check_device()) != SAGE_OK) return s;
+  const HostPlan P = host_plan(Hq, Hkv, Lq, Lk, D, chunk_kv_heads);
+  if (ws == nullptr || !aligned(ws, 256))
+    return fail(SAGE_ERR_WORKSPACE, "workspace must be a 256-byte aligned device pointer");
+  if (ws_bytes < P.total)
+    return fail(SAGE_ERR_WORKSPACE, "workspace has %zu bytes, the host-buffer call needs %zu",
+                ws_bytes, P.total);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(SAGE_ERR_UNSUPPORTED, "device index %d", dev);
+  HostRuntime& rt = g_host_rt[dev];
+  std::lock_guard<std::mutex> lock(rt.mu);
+  if ((e = host_runtime_init(rt)) != cudaSuccess) return cuda_fail(e, "pipeline streams");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  const bool hnd = layout == SAGE_HND;
+  // the staging and the workspace may still be in use by the caller's
+  // earlier work on its stream
+  e = cudaEventRecord(rt.start, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(rt.in, rt.start, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "pipeline start");
+  int64_t i = 0;
+  for (int64_t b = 0; b < B; ++b) {
+    for (int64_t g0 = 0; g0 < Hkv; g0 += P.chunk_kv, ++i) {
+      const int64_t gn = Hkv - g0 < P.chunk_kv ? Hkv - g0 : P.chunk_kv;
+      const int64_t h0 = g0 * P.group, hn = gn * P.group;
+      const int sl = static_cast<int>(i & 1);
+      uint8_t* dq = base + P.slot[sl];
+      uint8_t* dk = dq + align256(P.q_bytes);
+      uint8_t* dv = dk + align256(P.kv_bytes);
+      float* dout = reinterpret_cast<float*>(dv + align256(P.kv_bytes));
+      // inputs: after the slot's previous chunk has been computed
+      e = cudaStreamWaitEvent(rt.in, rt.computed[sl], 0);
+      if (e == cudaSuccess) e = copy_chunk(dq, q, true, hnd, b, h0, hn, Hq, Lq, D, 2, rt.in);
+      if (e == cudaSuccess) e = copy_chunk(dk, k, true, hnd, b, g0, gn, Hkv, Lk, D, 2, rt.in);
+      if (e == cudaSuccess) e = copy_chunk(dv, v, true, hnd, b, g0, gn, Hkv, Lk, D, 2, rt.in);
+      if (e == cudaSuccess) e = cudaEventRecord(rt.loaded[sl], rt.in);
+      // compute: after the inputs landed and the slot's previous output left
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(st, rt.loaded[sl], 0);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(st, rt.stored[sl], 0);
+      if (e != cudaSuccess) return cuda_fail(e, "pipeline copy-in");
+      s = dense_fwd(dq, dk, dv, dout, 1, hn, gn, Lq, Lk, D, layout, is_causal, sm_scale,
+                    dtype, base, P.ws_bytes, stream, false);
+      if (s != SAGE_OK) return s;
+      e = cudaEventRecord(rt.computed[sl], st);
+      // output: after the chunk was computed
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(rt.out, rt.computed[sl], 0);
+      if (e == cudaSuccess) e = copy_chunk(out, dout, false, hnd, b, h0, hn, Hq, Lq, D, 4, rt.out);
+      if (e == cudaSuccess) e = cudaEventRecord(rt.stored[sl], rt.out);
+      if (e != cudaSuccess) return cuda_fail(e, "pipeline copy-out");
+    }
+  }
+  // the caller's stream completes once every output is in host memory
+  e = cudaStreamWaitEvent(st, rt.stored[0], 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, rt.stored[1], 0);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "pipeline end");
 }
 
 const char* sage_last_error(void) { return g_last_error.c_str(); }

@@ -26,6 +26,7 @@ EXPORTS = (
     "sage_last_error",
     "sage_kv_stats_noalloc", "sage_launch_count", "sage_quant_prologue_strided",
     "sage_attn_fwd_strided", "sage_quant_prologue_pv16", "sage_attn_fwd_pv16",
+    "sage_workspace_bytes_host", "sage_attn_fwd_host",
 )
 
 
@@ -65,6 +66,9 @@ def _load():
     QP = ctypes.POINTER(Quantized)
     sig = {
         "sage_workspace_bytes": ([I64] * 6, SZ),
+        "sage_workspace_bytes_host": ([I64] * 7, SZ),
+        "sage_attn_fwd_host": ([P, P, P, P, I64, I64, I64, I64, I64, I64, I, I, F, I, I64, P, SZ,
+                                P], I),
         "sage_workspace_bytes_varlen": ([I64] * 6, SZ),
         "sage_quant_prologue": ([P, P, P, I, I, I64, I64, I64, I64, I64, I64, P, SZ, QP, P], I),
         "sage_quant_prologue_varlen": ([P, P, P, I, P, P, I64, I64, I64, I, I, I64, I64, I64,
@@ -273,6 +277,36 @@ def attn_fwd_pv16(q, k, v, out, layout="HND", is_causal=False, sm_scale=None, ws
                                  lay, int(bool(is_causal)), float(sm_scale or 0.0),
                                  _dtype_code(q), _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "sage_attn_fwd_pv16")
+    return out
+
+
+def workspace_bytes_host(B, Hq, Hkv, Lq, Lk, D, chunk_kv_heads=0) -> int:
+    return int(_lib.sage_workspace_bytes_host(B, Hq, Hkv, Lq, Lk, D, int(chunk_kv_heads)))
+
+
+def attn_fwd_host(q, k, v, out, layout="HND", is_causal=False, sm_scale=None,
+                  chunk_kv_heads=0, ws=None, stream=None):
+    """Attention on host tensors (page-locked for overlap): the library copies
+    chunks in, computes them and copies the output back, pipelined.  `out`
+    is a host float32 tensor of q's shape; `stream` completes when it is
+    filled."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"attn_fwd_host: {name} must be a contiguous host tensor")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("attn_fwd_host: q, k and v must share one dtype")
+    if out.dtype != torch.float32 or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("attn_fwd_host: out must be float32 with q's shape")
+    lay = _layout_code(layout)
+    B, Hq, Hkv, Lq, Lk, D = _dims(q, k, lay)
+    if ws is None:
+        ws = alloc_workspace(workspace_bytes_host(B, Hq, Hkv, Lq, Lk, D, chunk_kv_heads))
+    rc = _lib.sage_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, Lq, Lk, D,
+                                 lay, int(bool(is_causal)), float(sm_scale or 0.0),
+                                 _dtype_code(q), int(chunk_kv_heads), _ptr(ws), ws.numel(),
+                                 _stream(stream))
+    _check(rc, "sage_attn_fwd_host")
     return out
 
 

@@ -159,3 +159,34 @@ def test_binding_refuses_tensors_it_would_misread():
         sage.quant_prologue(q, q, q)
     with pytest.raises(ValueError, match="CUDA"):
         sage.quant_prologue_pv16(q, q, q)
+
+
+def test_host_buffer_call_sizes_and_refusals():
+    """sage_workspace_bytes_host: the chunk prologue's workspace plus two
+    staging slots (q, k, v, out of one chunk); sage_attn_fwd_host refuses bad
+    arguments before touching a device."""
+    L = sage.lib
+    whole = L.sage_workspace_bytes(1, 4, 2, 256, 256, 64)
+    one = L.sage_workspace_bytes_host(3, 4, 2, 256, 256, 64, 1)
+    two = L.sage_workspace_bytes_host(3, 4, 2, 256, 256, 64, 2)
+    chunk1 = 2 * 256 * 64 * 2 + 2 * (1 * 256 * 64 * 2) + 2 * 256 * 64 * 4   # q, k, v, out
+    assert one >= 2 * chunk1
+    assert two > one >= whole // 2
+    assert L.sage_workspace_bytes_host(1, 3, 2, 256, 256, 64, 0) == 0       # Hq % Hkv
+    assert L.sage_workspace_bytes_host(1, 2, 2, 256, 256, 129, 0) == 0      # D > 128
+
+    def call(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, B=1, Hq=2, Hkv=2, Lq=128, Lk=128, D=64,
+                 layout=0, causal=0, scale=0.0, dtype=0, chunk=0, ws=FAKE, ws_bytes=1 << 30)
+        a.update(kw)
+        return L.sage_attn_fwd_host(a["q"], a["k"], a["v"], a["out"], a["B"], a["Hq"],
+                                    a["Hkv"], a["Lq"], a["Lk"], a["D"], a["layout"],
+                                    a["causal"], a["scale"], a["dtype"], a["chunk"], a["ws"],
+                                    a["ws_bytes"], None)
+    assert call(B=0) == sage.OK
+    assert call(Lq=0) == sage.OK
+    assert call(layout=5) == sage.ERR_INVALID_ARG
+    assert call(Lk=0) == sage.ERR_INVALID_ARG
+    assert call(q=None) == sage.ERR_INVALID_ARG
+    assert call(dtype=7) == sage.ERR_INVALID_ARG
+    assert call(Hq=3) == sage.ERR_INVALID_ARG

@@ -1,0 +1,65 @@
+"""The host-buffer call (sage_attn_fwd_host): q, k, v and out in page-locked
+host memory, chunked and pipelined by the library.  Attention never mixes
+heads or batch entries, so its output must equal sage_attn_fwd's bit for bit
+on the same inputs, whatever the chunking."""
+import numpy as np
+import pytest
+
+from quantized_attention_smooth_gb300 import workloads as wl
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def sage():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantized_attention_smooth_gb300 import sage as s
+    return s
+
+
+def _w(name, **kw):
+    base = dict(B=2, Hq=4, Hkv=2, Lq=300, Lk=333, D=128, dtype=wl.F16, layout=wl.HND,
+                causal=False, seed=900, k_offset_sigma=2.0)
+    base.update(kw)
+    return wl.Workload(name, **base)
+
+
+CASES = [
+    (_w("hnd_chunk1"), 1),
+    (_w("hnd_auto"), 0),
+    (_w("nhd_bf16_gqa_causal", B=3, Hq=6, Hkv=3, Lq=256, Lk=256, layout=wl.NHD,
+        dtype=wl.BF16, causal=True, seed=901), 2),          # 2 does not divide 3
+    (_w("d40_ragged_nhd", B=1, Hq=2, Hkv=2, Lq=130, Lk=700, D=40, layout=wl.NHD, seed=902), 1),
+    (_w("hnd_causal_lq_lt_lk", B=2, Hq=2, Hkv=1, Lq=200, Lk=450, D=64, causal=True,
+        seed=903), 0),
+]
+
+
+def _host(x):
+    return x.cpu().pin_memory()
+
+
+def _compare(sage, w, chunk):
+    inp = wl.make_inputs(w)
+    d = H.device_inputs(w, inp)
+    lay = "HND" if w.layout == wl.HND else "NHD"
+    scale = wl.default_sm_scale(w)
+    ref = torch.empty(d["q"].shape, dtype=torch.float32, device="cuda")
+    sage.attn_fwd(d["q"], d["k"], d["v"], ref, lay, w.causal, scale)
+    hq, hk, hv = _host(d["q"]), _host(d["k"]), _host(d["v"])
+    out = torch.full(hq.shape, float("nan"), dtype=torch.float32).pin_memory()
+    sage.attn_fwd_host(hq, hk, hv, out, lay, w.causal, scale, chunk_kv_heads=chunk)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref.cpu())
+
+
+@pytest.mark.parametrize("w,chunk", CASES, ids=[w.name for w, _ in CASES])
+def test_host_call_equals_device_call(sage, w, chunk):
+    _compare(sage, w, chunk)
+
+
+def test_host_call_at_bench_size(sage):
+    _compare(sage, wl.WORKLOADS["b2_h24_l4096_d128"], 0)
