@@ -202,7 +202,10 @@ SAGE_API sage_status sage_attn_fwd_pv16(const void* q, const void* k, const void
 
 /* Host-buffer call: sage_attn_fwd on q, k, v and out in HOST memory (dense
  * HND or NHD, same arguments and conventions), with the host<->device copies
- * inside.  The problem is cut into chunks of (one batch entry, chunk_kv_heads
+ * inside.  The operation is sage_attn_fwd's (the prologue of
+ * sage_quant_prologue, then sage_attn_quantized; [SD] kernel table, [OV]
+ * Core features); the chunking and copy pipeline are this library's own and
+ * have no counterpart on the pages.  The problem is cut into chunks of (one batch entry, chunk_kv_heads
  * kv heads with their query heads); 0 picks enough kv heads for one wave of
  * query-tile pairs per chunk.  Chunk i+1's inputs are copied into device
  * staging while chunk i is computed on `stream` and chunk i-1's output is
