@@ -247,6 +247,8 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int):
         b.record(stream)
         e2e_ev.append((a, b))
     torch.cuda.synchronize()
+    # query head 0 of segment 0 of the last output, for the parity sample
+    out_rows = np.array(wl.out_segment(w, out_host.numpy(), 0, inp.get("cu_q"))[0][:args.cpu_rows])
     e2e_ev = e2e_ev[-n_e2e:]
     e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
     h2d = sum(host[k].numel() * host[k].element_size() for k in ("q", "k", "v"))
@@ -255,7 +257,7 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int):
     Dp = 64 if w.D <= 64 else 128
     r = dict(total_ms=total_ms, step_ms=step_ms, pro_ms=pro_ms, att_ms=att_ms,
              launches_per_step=launches_per_step, launches=launches,
-             e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, ops=workload_ops(w),
+             e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, ops=workload_ops(w), out_rows=out_rows,
              e2e_api=("sage_attn_fwd_host (chunks of kv heads, copies pipelined with compute)"
                       if host_call else "copies, then the one-call entry point, then a copy back"),
              ops_padded=workload_ops(w, Dp),
@@ -308,7 +310,7 @@ def job_figures(r: dict, world: int, steps: int) -> dict:
 def oracle_sample(w: wl.Workload, inp: dict, rows: int, heads: int = 1, pv16: bool = False):
     """Times the oracle (prologue + attention; the FP16-PV variant's when pv16)
     on `heads` query heads of segment 0 and its first `rows` query rows;
-    returns (ops, seconds, threads)."""
+    returns (ops, seconds, threads, output rows [rows, D] of query head 0)."""
     import oracle
     q, k, v = wl.segment(w, inp, 0)
     # query head 0 reads kv head 0 for every GQA grouping
@@ -320,10 +322,10 @@ def oracle_sample(w: wl.Workload, inp: dict, rows: int, heads: int = 1, pv16: bo
     t0 = time.perf_counter()
     pro = oracle.prologue(qs, ks, vs, w.dtype)
     if pv16:
-        oracle.attn_pv16(pro, oracle.v16(vs, w.dtype), w.causal, wl.default_sm_scale(w),
-                         rows=(0, rows))
+        ref = oracle.attn_pv16(pro, oracle.v16(vs, w.dtype), w.causal, wl.default_sm_scale(w),
+                               rows=(0, rows))
     else:
-        oracle.attn(pro, w.causal, wl.default_sm_scale(w), rows=(0, rows))
+        ref = oracle.attn(pro, w.causal, wl.default_sm_scale(w), rows=(0, rows))
     dt = time.perf_counter() - t0
     if w.causal:
         # the sample's unmasked work, restated in the metric's literal count
@@ -333,7 +335,7 @@ def oracle_sample(w: wl.Workload, inp: dict, rows: int, heads: int = 1, pv16: bo
     else:
         pairs = rows * lk
     ops = 4.0 * qs.shape[0] * pairs * w.D
-    return ops, dt, os.cpu_count()
+    return ops, dt, os.cpu_count(), ref[0, :rows]
 
 
 def reference_arm(args, w: wl.Workload, rank: int, world: int):
@@ -348,7 +350,7 @@ def reference_arm(args, w: wl.Workload, rank: int, world: int):
         oracle_sample(w, inp, min(rows, 128), pv16=pv16)
     tot_ops, tot_s = 0.0, 0.0
     for _ in range(args.steps):
-        ops, dt, cores = oracle_sample(w, inp, rows, pv16=pv16)
+        ops, dt, cores, _ = oracle_sample(w, inp, rows, pv16=pv16)
         tot_ops += ops
         tot_s += dt
     tops = tot_ops / tot_s / 1e12
@@ -421,7 +423,10 @@ def main():
     tops = fig["value"]
     pro_gbs = prologue_bytes(w, 2 if pv16 else 1) / (r["pro_ms"] * 1e-3) / 1e9
     inp = wl.make_inputs(w)
-    cpu_ops, cpu_s, cores = oracle_sample(w, inp, args.cpu_rows, pv16=pv16)
+    cpu_ops, cpu_s, cores, ref_rows = oracle_sample(w, inp, args.cpu_rows, pv16=pv16)
+    # the bench's own output on the oracle's sample (segment 0, query head 0)
+    got_rows = r["out_rows"][:ref_rows.shape[0]]
+    parity = float(np.max(np.abs(got_rows.astype(np.float64) - ref_rows)))
     line = {
         "metric": METRIC, "value": tops, "unit": "TOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -452,6 +457,9 @@ def main():
         "e2e": {"value": fig["e2e"], "unit": "TOPS",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                 "api": r["e2e_api"]},
+        "parity_sample": {"max_abs_vs_oracle": parity, "tolerance": 2e-3,
+                          "rows": f"segment 0, query head 0, rows [0,{ref_rows.shape[0]}) "
+                                  "of the last e2e output"},
         "gpu_launches": r["launches"],
         "launches_per_step": r["launches_per_step"],
         "clocks": r["clocks"],
