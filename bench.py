@@ -224,9 +224,9 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int):
     assert sage.device_status(ws) == sage.OK, sage.last_error()
 
     # ---- end to end: host buffers, copies inside the timed region.  Dense
-    # FP8 problems go through the library's host-buffer call, which pipelines
-    # chunk copies with compute; the others copy, compute, copy back.
-    host_call = not w.varlen and not pv16
+    # problems go through the library's host-buffer call, which pipelines
+    # chunk copies with compute; packed sequences copy, compute, copy back.
+    host_call = not w.varlen
     if host_call:
         ws_host = sage.alloc_workspace(sage.workspace_bytes_host(
             w.B, w.Hq, w.Hkv, w.Lq, w.Lk, w.D), dev)
@@ -238,7 +238,7 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int):
         a.record(stream)
         if host_call:
             sage.attn_fwd_host(host["q"], host["k"], host["v"], out_host, w.layout, w.causal,
-                               scale, ws=ws_host, stream=stream)
+                               scale, ws=ws_host, stream=stream, pv16=pv16)
         else:
             for k in ("q", "k", "v"):
                 d[k].copy_(host[k], non_blocking=True)
@@ -258,7 +258,8 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int):
     r = dict(total_ms=total_ms, step_ms=step_ms, pro_ms=pro_ms, att_ms=att_ms,
              launches_per_step=launches_per_step, launches=launches,
              e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, ops=workload_ops(w), out_rows=out_rows,
-             e2e_api=("sage_attn_fwd_host (chunks of kv heads, copies pipelined with compute)"
+             e2e_api=(("sage_attn_fwd_host_pv16" if pv16 else "sage_attn_fwd_host") +
+                      " (chunks of kv heads, copies pipelined with compute)"
                       if host_call else "copies, then the one-call entry point, then a copy back"),
              ops_padded=workload_ops(w, Dp),
              ops_effective=w.ops(causal_effective=True),

@@ -227,6 +227,15 @@ SAGE_API sage_status sage_attn_fwd_host(const void* q, const void* k, const void
                                         int64_t chunk_kv_heads, void* ws, size_t ws_bytes,
                                         sage_stream_t stream);
 
+/* The same host-buffer pipeline around the FP16-PV variant
+ * (sage_attn_fwd_pv16); same workspace size. */
+SAGE_API sage_status sage_attn_fwd_host_pv16(const void* q, const void* k, const void* v,
+                                             float* out, int64_t B, int64_t Hq, int64_t Hkv,
+                                             int64_t Lq, int64_t Lk, int64_t D, int layout,
+                                             int is_causal, float sm_scale, int dtype,
+                                             int64_t chunk_kv_heads, void* ws,
+                                             size_t ws_bytes, sage_stream_t stream);
+
 /* Prologue + attention in one call on strided views (see
  * sage_quant_prologue_strided); out is dense fp32 in `layout`. */
 SAGE_API sage_status sage_attn_fwd_strided(

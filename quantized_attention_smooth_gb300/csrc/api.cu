@@ -577,6 +577,88 @@ cudaError_t copy_chunk(void* dst, const void* src, bool to_device, bool hnd, int
 
 }  // namespace
 
+namespace {
+
+// The host-buffer pipeline (see sage_attn_fwd_host); v16 runs the FP16-PV kernels.
+sage_status host_fwd(const void* q, const void* k, const void* v, float* out, int64_t B,
+                     int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk, int64_t D, int layout,
+                     int is_causal, float sm_scale, int dtype, int64_t chunk_kv_heads,
+                     void* ws, size_t ws_bytes, sage_stream_t stream, bool v16) {
+  sage_status s = SAGE_OK;
+  if (layout != SAGE_HND && layout != SAGE_NHD)
+    return fail(SAGE_ERR_INVALID_ARG, "layout %d is neither SAGE_HND nor SAGE_NHD", layout);
+  if (B < 0 || Lq < 0 || Lk < 0)
+    return fail(SAGE_ERR_INVALID_ARG, "negative size (B=%lld Lq=%lld Lk=%lld)",
+                (long long)B, (long long)Lq, (long long)Lk);
+  if (!check_dims(Hq, Hkv, D, &s)) return s;
+  if (dtype != SAGE_F16 && dtype != SAGE_BF16)
+    return fail(SAGE_ERR_INVALID_ARG, "dtype %d is neither SAGE_F16 nor SAGE_BF16", dtype);
+  if (B == 0 || Lq == 0) return ok();                 // nothing to compute
+  if (Lk == 0)
+    return fail(SAGE_ERR_INVALID_ARG, "the host-buffer call needs Lk > 0");
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr)
+    return fail(SAGE_ERR_INVALID_ARG, "null host buffer");
+  if ((s = check_device()) != SAGE_OK) return s;
+  const HostPlan P = host_plan(Hq, Hkv, Lq, Lk, D, chunk_kv_heads);
+  if (ws == nullptr || !aligned(ws, 256))
+    return fail(SAGE_ERR_WORKSPACE, "workspace must be a 256-byte aligned device pointer");
+  if (ws_bytes < P.total)
+    return fail(SAGE_ERR_WORKSPACE, "workspace has %zu bytes, the host-buffer call needs %zu",
+                ws_bytes, P.total);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(SAGE_ERR_UNSUPPORTED, "device index %d", dev);
+  HostRuntime& rt = g_host_rt[dev];
+  std::lock_guard<std::mutex> lock(rt.mu);
+  if ((e = host_runtime_init(rt)) != cudaSuccess) return cuda_fail(e, "pipeline streams");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  const bool hnd = layout == SAGE_HND;
+  // the staging and the workspace may still be in use by the caller's
+  // earlier work on its stream
+  e = cudaEventRecord(rt.start, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(rt.in, rt.start, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "pipeline start");
+  int64_t i = 0;
+  for (int64_t b = 0; b < B; ++b) {
+    for (int64_t g0 = 0; g0 < Hkv; g0 += P.chunk_kv, ++i) {
+      const int64_t gn = Hkv - g0 < P.chunk_kv ? Hkv - g0 : P.chunk_kv;
+      const int64_t h0 = g0 * P.group, hn = gn * P.group;
+      const int sl = static_cast<int>(i & 1);
+      uint8_t* dq = base + P.slot[sl];
+      uint8_t* dk = dq + align256(P.q_bytes);
+      uint8_t* dv = dk + align256(P.kv_bytes);
+      float* dout = reinterpret_cast<float*>(dv + align256(P.kv_bytes));
+      // inputs: after the slot's previous chunk has been computed
+      e = cudaStreamWaitEvent(rt.in, rt.computed[sl], 0);
+      if (e == cudaSuccess) e = copy_chunk(dq, q, true, hnd, b, h0, hn, Hq, Lq, D, 2, rt.in);
+      if (e == cudaSuccess) e = copy_chunk(dk, k, true, hnd, b, g0, gn, Hkv, Lk, D, 2, rt.in);
+      if (e == cudaSuccess) e = copy_chunk(dv, v, true, hnd, b, g0, gn, Hkv, Lk, D, 2, rt.in);
+      if (e == cudaSuccess) e = cudaEventRecord(rt.loaded[sl], rt.in);
+      // compute: after the inputs landed and the slot's previous output left
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(st, rt.loaded[sl], 0);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(st, rt.stored[sl], 0);
+      if (e != cudaSuccess) return cuda_fail(e, "pipeline copy-in");
+      s = dense_fwd(dq, dk, dv, dout, 1, hn, gn, Lq, Lk, D, layout, is_causal, sm_scale,
+                    dtype, base, P.ws_bytes, stream, v16);
+      if (s != SAGE_OK) return s;
+      e = cudaEventRecord(rt.computed[sl], st);
+      // output: after the chunk was computed
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(rt.out, rt.computed[sl], 0);
+      if (e == cudaSuccess) e = copy_chunk(out, dout, false, hnd, b, h0, hn, Hq, Lq, D, 4, rt.out);
+      if (e == cudaSuccess) e = cudaEventRecord(rt.stored[sl], rt.out);
+      if (e != cudaSuccess) return cuda_fail(e, "pipeline copy-out");
+    }
+  }
+  // the caller's stream completes once every output is in host memory
+  e = cudaStreamWaitEvent(st, rt.stored[0], 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, rt.stored[1], 0);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "pipeline end");
+}
+
+}  // namespace
+
 extern "C" {
 
 size_t sage_workspace_bytes(int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk,
@@ -855,77 +937,17 @@ sage_status sage_attn_fwd_host(const void* q, const void* k, const void* v, floa
                                int64_t D, int layout, int is_causal, float sm_scale,
                                int dtype, int64_t chunk_kv_heads, void* ws, size_t ws_bytes,
                                sage_stream_t stream) {
-  sage_status s = SAGE_OK;
-  if (layout != SAGE_HND && layout != SAGE_NHD)
-    return fail(SAGE_ERR_INVALID_ARG, "layout %d is neither SAGE_HND nor SAGE_NHD", layout);
-  if (B < 0 || Lq < 0 || Lk < 0)
-    return fail(SAGE_ERR_INVALID_ARG, "negative size (B=%lld Lq=%lld Lk=%lld)",
-                (long long)B, (long long)Lq, (long long)Lk);
-  if (!check_dims(Hq, Hkv, D, &s)) return s;
-  if (dtype != SAGE_F16 && dtype != SAGE_BF16)
-    return fail(SAGE_ERR_INVALID_ARG, "dtype %d is neither SAGE_F16 nor SAGE_BF16", dtype);
-  if (B == 0 || Lq == 0) return ok();                 // nothing to compute
-  if (Lk == 0)
-    return fail(SAGE_ERR_INVALID_ARG, "the host-buffer call needs Lk > 0");
-  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr)
-    return fail(SAGE_ERR_INVALID_ARG, "null host buffer");
-  if ((s = check_device()) != SAGE_OK) return s;
-  const HostPlan P = host_plan(Hq, Hkv, Lq, Lk, D, chunk_kv_heads);
-  if (ws == nullptr || !aligned(ws, 256))
-    return fail(SAGE_ERR_WORKSPACE, "workspace must be a 256-byte aligned device pointer");
-  if (ws_bytes < P.total)
-    return fail(SAGE_ERR_WORKSPACE, "workspace has %zu bytes, the host-buffer call needs %zu",
-                ws_bytes, P.total);
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= 64) return fail(SAGE_ERR_UNSUPPORTED, "device index %d", dev);
-  HostRuntime& rt = g_host_rt[dev];
-  std::lock_guard<std::mutex> lock(rt.mu);
-  if ((e = host_runtime_init(rt)) != cudaSuccess) return cuda_fail(e, "pipeline streams");
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t* base = static_cast<uint8_t*>(ws);
-  const bool hnd = layout == SAGE_HND;
-  // the staging and the workspace may still be in use by the caller's
-  // earlier work on its stream
-  e = cudaEventRecord(rt.start, st);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(rt.in, rt.start, 0);
-  if (e != cudaSuccess) return cuda_fail(e, "pipeline start");
-  int64_t i = 0;
-  for (int64_t b = 0; b < B; ++b) {
-    for (int64_t g0 = 0; g0 < Hkv; g0 += P.chunk_kv, ++i) {
-      const int64_t gn = Hkv - g0 < P.chunk_kv ? Hkv - g0 : P.chunk_kv;
-      const int64_t h0 = g0 * P.group, hn = gn * P.group;
-      const int sl = static_cast<int>(i & 1);
-      uint8_t* dq = base + P.slot[sl];
-      uint8_t* dk = dq + align256(P.q_bytes);
-      uint8_t* dv = dk + align256(P.kv_bytes);
-      float* dout = reinterpret_cast<float*>(dv + align256(P.kv_bytes));
-      // inputs: after the slot's previous chunk has been computed
-      e = cudaStreamWaitEvent(rt.in, rt.computed[sl], 0);
-      if (e == cudaSuccess) e = copy_chunk(dq, q, true, hnd, b, h0, hn, Hq, Lq, D, 2, rt.in);
-      if (e == cudaSuccess) e = copy_chunk(dk, k, true, hnd, b, g0, gn, Hkv, Lk, D, 2, rt.in);
-      if (e == cudaSuccess) e = copy_chunk(dv, v, true, hnd, b, g0, gn, Hkv, Lk, D, 2, rt.in);
-      if (e == cudaSuccess) e = cudaEventRecord(rt.loaded[sl], rt.in);
-      // compute: after the inputs landed and the slot's previous output left
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(st, rt.loaded[sl], 0);
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(st, rt.stored[sl], 0);
-      if (e != cudaSuccess) return cuda_fail(e, "pipeline copy-in");
-      s = dense_fwd(dq, dk, dv, dout, 1, hn, gn, Lq, Lk, D, layout, is_causal, sm_scale,
-                    dtype, base, P.ws_bytes, stream, false);
-      if (s != SAGE_OK) return s;
-      e = cudaEventRecord(rt.computed[sl], st);
-      // output: after the chunk was computed
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(rt.out, rt.computed[sl], 0);
-      if (e == cudaSuccess) e = copy_chunk(out, dout, false, hnd, b, h0, hn, Hq, Lq, D, 4, rt.out);
-      if (e == cudaSuccess) e = cudaEventRecord(rt.stored[sl], rt.out);
-      if (e != cudaSuccess) return cuda_fail(e, "pipeline copy-out");
-    }
-  }
-  // the caller's stream completes once every output is in host memory
-  e = cudaStreamWaitEvent(st, rt.stored[0], 0);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, rt.stored[1], 0);
-  return e == cudaSuccess ? ok() : cuda_fail(e, "pipeline end");
+  return host_fwd(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, layout, is_causal, sm_scale, dtype,
+                  chunk_kv_heads, ws, ws_bytes, stream, false);
+}
+
+sage_status sage_attn_fwd_host_pv16(const void* q, const void* k, const void* v, float* out,
+                                    int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk,
+                                    int64_t D, int layout, int is_causal, float sm_scale,
+                                    int dtype, int64_t chunk_kv_heads, void* ws,
+                                    size_t ws_bytes, sage_stream_t stream) {
+  return host_fwd(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, layout, is_causal, sm_scale, dtype,
+                  chunk_kv_heads, ws, ws_bytes, stream, true);
 }
 
 const char* sage_last_error(void) { return g_last_error.c_str(); }

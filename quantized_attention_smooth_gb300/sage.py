@@ -26,7 +26,7 @@ EXPORTS = (
     "sage_last_error",
     "sage_kv_stats_noalloc", "sage_launch_count", "sage_quant_prologue_strided",
     "sage_attn_fwd_strided", "sage_quant_prologue_pv16", "sage_attn_fwd_pv16",
-    "sage_workspace_bytes_host", "sage_attn_fwd_host",
+    "sage_workspace_bytes_host", "sage_attn_fwd_host", "sage_attn_fwd_host_pv16",
 )
 
 
@@ -69,6 +69,8 @@ def _load():
         "sage_workspace_bytes_host": ([I64] * 7, SZ),
         "sage_attn_fwd_host": ([P, P, P, P, I64, I64, I64, I64, I64, I64, I, I, F, I, I64, P, SZ,
                                 P], I),
+        "sage_attn_fwd_host_pv16": ([P, P, P, P, I64, I64, I64, I64, I64, I64, I, I, F, I, I64, P,
+                                     SZ, P], I),
         "sage_workspace_bytes_varlen": ([I64] * 6, SZ),
         "sage_quant_prologue": ([P, P, P, I, I, I64, I64, I64, I64, I64, I64, P, SZ, QP, P], I),
         "sage_quant_prologue_varlen": ([P, P, P, I, P, P, I64, I64, I64, I, I, I64, I64, I64,
@@ -285,7 +287,7 @@ def workspace_bytes_host(B, Hq, Hkv, Lq, Lk, D, chunk_kv_heads=0) -> int:
 
 
 def attn_fwd_host(q, k, v, out, layout="HND", is_causal=False, sm_scale=None,
-                  chunk_kv_heads=0, ws=None, stream=None):
+                  chunk_kv_heads=0, ws=None, stream=None, pv16=False):
     """Attention on host tensors (page-locked for overlap): the library copies
     chunks in, computes them and copies the output back, pipelined.  `out`
     is a host float32 tensor of q's shape; `stream` completes when it is
@@ -302,11 +304,11 @@ def attn_fwd_host(q, k, v, out, layout="HND", is_causal=False, sm_scale=None,
     B, Hq, Hkv, Lq, Lk, D = _dims(q, k, lay)
     if ws is None:
         ws = alloc_workspace(workspace_bytes_host(B, Hq, Hkv, Lq, Lk, D, chunk_kv_heads))
-    rc = _lib.sage_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, Lq, Lk, D,
-                                 lay, int(bool(is_causal)), float(sm_scale or 0.0),
-                                 _dtype_code(q), int(chunk_kv_heads), _ptr(ws), ws.numel(),
-                                 _stream(stream))
-    _check(rc, "sage_attn_fwd_host")
+    fn = _lib.sage_attn_fwd_host_pv16 if pv16 else _lib.sage_attn_fwd_host
+    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, Lq, Lk, D, lay,
+            int(bool(is_causal)), float(sm_scale or 0.0), _dtype_code(q), int(chunk_kv_heads),
+            _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "sage_attn_fwd_host_pv16" if pv16 else "sage_attn_fwd_host")
     return out
 
 

@@ -63,3 +63,18 @@ def test_host_call_equals_device_call(sage, w, chunk):
 
 def test_host_call_at_bench_size(sage):
     _compare(sage, wl.WORKLOADS["b2_h24_l4096_d128"], 0)
+
+
+def test_host_call_pv16_equals_device_call(sage):
+    w = _w("pv16_nhd_bf16", B=2, Hq=4, Hkv=2, Lq=300, Lk=333, layout=wl.NHD, dtype=wl.BF16,
+           seed=904)
+    inp = wl.make_inputs(w)
+    d = H.device_inputs(w, inp)
+    scale = wl.default_sm_scale(w)
+    ref = torch.empty(d["q"].shape, dtype=torch.float32, device="cuda")
+    sage.attn_fwd_pv16(d["q"], d["k"], d["v"], ref, "NHD", w.causal, scale)
+    hq, hk, hv = _host(d["q"]), _host(d["k"]), _host(d["v"])
+    out = torch.full(hq.shape, float("nan"), dtype=torch.float32).pin_memory()
+    sage.attn_fwd_host(hq, hk, hv, out, "NHD", w.causal, scale, chunk_kv_heads=1, pv16=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref.cpu())
