@@ -548,7 +548,19 @@ cudaError_t host_runtime_init(HostRuntime& rt) {
                         &rt.computed[1], &rt.stored[0], &rt.stored[1]};
   for (cudaEvent_t* ev : evs)
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
-  if (e == cudaSuccess) rt.ready = true;
+  if (e == cudaSuccess) {
+    rt.ready = true;
+    return e;
+  }
+  // a partial set is released, so a later call starts from nothing
+  for (cudaEvent_t* ev : evs)
+    if (*ev != nullptr) {
+      cudaEventDestroy(*ev);
+      *ev = nullptr;
+    }
+  if (rt.in != nullptr) cudaStreamDestroy(rt.in);
+  if (rt.out != nullptr) cudaStreamDestroy(rt.out);
+  rt.in = rt.out = nullptr;
   return e;
 }
 
