@@ -21,8 +21,10 @@
  *
  * Conventions shared by every call:
  *  - All tensor pointers are DEVICE pointers of the current CUDA device and
- *    are owned by the caller.  The library allocates no memory, never
- *    synchronises the host and enqueues all work on the caller's stream.
+ *    are owned by the caller (the sage_attn_fwd_host* calls take host
+ *    buffers instead).  The library allocates no memory, never synchronises
+ *    the host and enqueues all work on the caller's stream (the host-buffer
+ *    calls add copies on two streams of their own, ordered by events).
  *  - Arguments are validated on the host before anything is enqueued; a bad
  *    argument returns an error and launches nothing.  The reason is kept in
  *    a thread-local string returned by sage_last_error().
