@@ -1,5 +1,7 @@
 // Quantized-attention oracle: a plain, slow, CPU restatement of the
-// SageAttention2-style forward pass (smoothed INT8 Q/K, FP8 P and V).
+// SageAttention2-style forward pass (smoothed INT8 Q/K, FP8 P and V), of its
+// FP16-PV variant (the same INT8 Q/K, fp16 P and V), and of exact fp64
+// attention to measure both against.
 //
 // TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
 // benchmark's CPU-baseline leg load this library.  The product path (the CUDA
