@@ -190,3 +190,19 @@ def test_host_buffer_call_sizes_and_refusals():
     assert call(q=None) == sage.ERR_INVALID_ARG
     assert call(dtype=7) == sage.ERR_INVALID_ARG
     assert call(Hq=3) == sage.ERR_INVALID_ARG
+
+
+def test_host_buffer_call_automatic_chunk():
+    """The automatic chunk holds one wave of query-tile pairs (one per SM; the
+    plan assumes GB300's 152 SMs when no device answers): at B=2 H=24 L=4096,
+    16 pairs per head, so 10 kv heads per chunk."""
+    import torch
+    L = sage.lib
+    if torch.cuda.is_available():
+        pytest.skip("the device's own SM count decides on a GPU")
+    auto = L.sage_workspace_bytes_host(2, 24, 24, 4096, 4096, 128, 0)
+    assert auto == L.sage_workspace_bytes_host(2, 24, 24, 4096, 4096, 128, 10)
+    assert auto != L.sage_workspace_bytes_host(2, 24, 24, 4096, 4096, 128, 9)
+    # a chunk never exceeds the kv heads there are
+    assert (L.sage_workspace_bytes_host(1, 8, 2, 128, 128, 64, 0) ==
+            L.sage_workspace_bytes_host(1, 8, 2, 128, 128, 64, 2))
