@@ -219,7 +219,11 @@ SAGE_API sage_status sage_attn_fwd_pv16(const void* q, const void* k, const void
  *   Host buffers should be page-locked for the copies to overlap; the call
  *   returns once everything is enqueued, and `stream` completes when every
  *   output row is in `out`.  Calls on one device enqueue one at a time.
- *   Lk = 0 is refused (use sage_attn_fwd); B = 0 or Lq = 0 does nothing. */
+ *   Lk = 0 is refused (use sage_attn_fwd); B = 0 or Lq = 0 does nothing.
+ *   Device-side failures of every chunk accumulate in the status word at
+ *   the start of ws (the first chunk clears it, later chunks keep it), so
+ *   sage_device_status(ws, stream) after the call reports a bounded wait
+ *   that ran out in any chunk. */
 SAGE_API size_t sage_workspace_bytes_host(int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq,
                                           int64_t Lk, int64_t D, int64_t chunk_kv_heads);
 SAGE_API sage_status sage_attn_fwd_host(const void* q, const void* k, const void* v,
@@ -263,6 +267,37 @@ SAGE_API sage_status sage_debug_qk_int32(const sage_quantized* qt, int64_t seg,
                                 int64_t hq, int64_t qtile, int64_t ktile,
                                 int32_t* out, sage_stream_t stream);
 
+/* Debug: the precision of the PV accumulator ([SD] kernel table: the FP8
+ * PV products accumulate into an fp32 buffer).  Computes
+ *   out[r][c] = sum over t < ntiles, j < 128 of P~_t[r][j] * V~_t[c][j]
+ * with the attention kernel's own PV instructions (tcgen05 kind::f8f6f4,
+ * e4m3 x e4m3, M=128, N=Dp, K=32 per instruction, accumulating in tensor
+ * memory; the first instruction overwrites), so that tests can compare the
+ * hardware's sums with exact ones.
+ *   p8    : device e4m3 codes [ntiles][128 rows][128 keys], 16-byte aligned;
+ *   v8    : device e4m3 codes [ntiles][Dp channels][128 keys] (the prologue's
+ *           channel-major V), 16-byte aligned;
+ *   ntiles: 1..4096 key tiles of 128 keys; Dp: 64 or 128;
+ *   out   : device fp32 [128][Dp];
+ *   status: a device word the call clears and the kernel sets if its bounded
+ *           wait runs out (read it with sage_device_status(status, stream)). */
+SAGE_API sage_status sage_debug_pv_accum(const uint8_t* p8, const uint8_t* v8, int64_t ntiles,
+                                         int64_t Dp, float* out, uint32_t* status,
+                                         sage_stream_t stream);
+
+/* Measurement: the tensor pipe's rate for the attention kernel's two MMA
+ * kinds, at the clock the GPU runs at the time (no counterpart on the
+ * pages; the benchmark reports its kernel against it).  Launches one CTA
+ * per SM, in which one thread issues n_mma back-to-back tcgen05 MMAs of
+ * shape M=128 N=128 into one tensor-memory accumulator: kind 0 = fp16
+ * operands, K=16 (2*128*128*16 flops each, the QK^T kind); kind 1 = e4m3
+ * operands, K=32 (twice that, the PV kind).  Operands are zeros; nothing is
+ * returned but the time the caller measures around the call (events on
+ * `stream`).  n_mma: 1..2^22.  status: a device word the call clears and
+ * the kernel sets if its bounded wait runs out (sage_device_status). */
+SAGE_API sage_status sage_debug_tc_rate(int kind, int64_t n_mma, uint32_t* status,
+                                        sage_stream_t stream);
+
 /* Debug: the attention kernel's fp32 -> e4m3 conversion (round to nearest
  * even, saturating to +-448) applied to n device floats. */
 SAGE_API sage_status sage_debug_e4m3(const float* in, uint8_t* out, int64_t n,
@@ -272,6 +307,11 @@ SAGE_API sage_status sage_debug_e4m3(const float* in, uint8_t* out, int64_t n,
  * loading key/value tile `skip_kv_tile` (-1: off) so that the consumer's
  * bounded wait runs out after `timeout_ns` (0: default of one second). */
 SAGE_API void sage_debug_set_fault(int skip_kv_tile, uint64_t timeout_ns);
+
+/* Debug hook: the fault set by sage_debug_set_fault applies to the next
+ * `launches` attention launches only (so that a test can fail one chunk of
+ * a host-buffer call); -1, the default, applies it to every launch. */
+SAGE_API void sage_debug_set_fault_launches(int launches);
 
 /* Test hook: the prologue entry points run as one launch (1), as two
  * launches (2: Q tiles and K/V statistics, then K/V tiles), or choose by
@@ -304,11 +344,22 @@ SAGE_API sage_status sage_device_status(const void* ws, sage_stream_t stream);
  * before any stream capture.  Every call clears and reuses the same array,
  * so calls that overlap on the GPU (other streams, other host threads)
  * race and must be serialised by the caller.  It calls no cudaMalloc or
- * cudaFree. */
+ * cudaFree.  Failures on the device (a bounded wait that ran out, for
+ * instance because an overlapping call took the array's counters) are
+ * recorded in a status word at the start of the array, which every call
+ * clears; sage_kv_stats_noalloc_status reads it. */
 SAGE_API sage_status sage_kv_stats_noalloc(const void* k, const void* v, int dtype,
                                            int layout, int64_t B, int64_t Hkv,
                                            int64_t Lk, int64_t D, float* k_mean,
                                            float* s_v, sage_stream_t stream);
+
+/* Reads (synchronising `stream`) the device status word of the last
+ * sage_kv_stats_noalloc call on the current device: SAGE_OK, or
+ * SAGE_ERR_DEVICE_TIMEOUT when a bounded wait ran out (k_mean and s_v may
+ * then be partial), or SAGE_ERR_UNSUPPORTED for an internal inconsistency.
+ * Like the statistics call, it allocates nothing; the pages have no
+ * counterpart. */
+SAGE_API sage_status sage_kv_stats_noalloc_status(sage_stream_t stream);
 
 /* Reason of the last failure on this thread ("" if none). */
 SAGE_API const char* sage_last_error(void);

@@ -33,6 +33,8 @@ thread_local std::string g_last_error;
 std::atomic<int> g_skip_kv_tile{-1};
 std::atomic<int> g_prologue_launches{0};
 std::atomic<unsigned long long> g_timeout_ns{0};
+// attention launches the failure-injection hook still applies to (-1: all)
+std::atomic<int> g_fault_launches{-1};
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;   // 1 s
 
 // Bound of every device-side wait of the next launches.
@@ -286,9 +288,12 @@ void fill_quantized(const SegGeo& g, const WsLayout& w, uint8_t* ws, sage_quanti
 }
 
 // Shared tail of both prologue entry points (arguments already validated).
+// keep_status: leave the device status word as it is (the host-buffer
+// pipeline's later chunks, so that a failure of an earlier chunk stays
+// visible to sage_device_status); otherwise it is cleared with the rest.
 sage_status run_prologue(const SegGeo& g, const void* q, const void* k, const void* v,
                          void* ws, size_t ws_bytes, sage_quantized* qt,
-                         cudaStream_t st, bool v16 = false) {
+                         cudaStream_t st, bool v16 = false, bool keep_status = false) {
   const WsLayout w = ws_layout(g);
   if (ws == nullptr || !aligned(ws, 256))
     return fail(SAGE_ERR_WORKSPACE, "workspace must be a 256-byte aligned device pointer");
@@ -303,7 +308,8 @@ sage_status run_prologue(const SegGeo& g, const void* q, const void* k, const vo
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   fill_quantized(g, w, wsb, qt);
   qt->v_fp16 = v16 ? 1 : 0;
-  cudaError_t e = cudaMemsetAsync(wsb, 0, w.zero_end, st);
+  const size_t zero_from = keep_status ? w.ksum : 0;   // the status word lies below ksum
+  cudaError_t e = cudaMemsetAsync(wsb + zero_from, 0, w.zero_end - zero_from, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
   PrologueBuffers b{};
   b.q = static_cast<const uint16_t*>(q);
@@ -368,6 +374,7 @@ sage_status launch_attn(const sage_quantized* qt, float* out, int layout, int is
     p.out_tok_stride = qt->Hq * qt->D;
   }
   p.scale_log2 = resolve_scale(sm_scale, qt->D) * 1.44269504088896340736f;
+  p.one = 1.0f;
   p.causal = is_causal ? 1 : 0;
   // the output as a tensor-store target (32-column boxes of 128 rows): rows
   // of a dense tile are clipped at Lq, columns at D; needs 16-byte rows
@@ -403,6 +410,16 @@ sage_status launch_attn(const sage_quantized* qt, float* out, int layout, int is
   }
   p.v16 = qt->v_fp16;
   p.skip_kv_tile = g_skip_kv_tile.load();
+  if (p.skip_kv_tile >= 0) {                  // a limited fault: count this launch
+    int left = g_fault_launches.load();
+    while (left >= 0) {
+      if (left == 0) {
+        p.skip_kv_tile = -1;
+        break;
+      }
+      if (g_fault_launches.compare_exchange_weak(left, left - 1)) break;
+    }
+  }
   p.timeout_ns = wait_timeout_ns();
   p.status = qt->status;
   cudaError_t e = launch_attention(maps, p, st);
@@ -443,7 +460,7 @@ sage_status dense_prologue(const void* q, const void* k, const void* v, int dtyp
 sage_status dense_fwd(const void* q, const void* k, const void* v, float* out, int64_t B,
                       int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk, int64_t D, int layout,
                       int is_causal, float sm_scale, int dtype, void* ws, size_t ws_bytes,
-                      sage_stream_t stream, bool v16) {
+                      sage_stream_t stream, bool v16, bool keep_status = false) {
   sage_status s = SAGE_OK;
   if (layout != SAGE_HND && layout != SAGE_NHD)
     return fail(SAGE_ERR_INVALID_ARG, "layout %d is neither SAGE_HND nor SAGE_NHD", layout);
@@ -464,7 +481,7 @@ sage_status dense_fwd(const void* q, const void* k, const void* v, float* out, i
   }
   sage_quantized qt;
   s = run_prologue(dense_geo(B, Hq, Hkv, Lq, Lk, D, dtype, layout), q, k, v, ws, ws_bytes,
-                   &qt, st, v16);
+                   &qt, st, v16, keep_status);
   if (s != SAGE_OK) return s;
   if (qt.nseg > 65535 || qt.Hq > 65535)
     return fail(SAGE_ERR_UNSUPPORTED, "more than 65535 segments or heads");
@@ -493,15 +510,15 @@ struct HostPlan {
 };
 
 int sm_count_of_current_device() {
-  static int sms[64] = {};
+  static std::atomic<int> sms[64] = {};          // per device, filled once
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (sms[dev] == 0) {
-    int n = 0;
+  int n = sms[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    sms[dev] = n;
+    sms[dev].store(n, std::memory_order_relaxed);
   }
-  return sms[dev];
+  return n;
 }
 
 // chunk_kv <= 0 picks enough kv heads for one wave of query-tile pairs per
@@ -652,8 +669,10 @@ sage_status host_fwd(const void* q, const void* k, const void* v, float* out, in
       if (e == cudaSuccess) e = cudaStreamWaitEvent(st, rt.loaded[sl], 0);
       if (e == cudaSuccess) e = cudaStreamWaitEvent(st, rt.stored[sl], 0);
       if (e != cudaSuccess) return cuda_fail(e, "pipeline copy-in");
+      // the first chunk clears the device status word, the others keep it,
+      // so a bounded wait that ran out in any chunk stays visible
       s = dense_fwd(dq, dk, dv, dout, 1, hn, gn, Lq, Lk, D, layout, is_causal, sm_scale,
-                    dtype, base, P.ws_bytes, stream, v16);
+                    dtype, base, P.ws_bytes, stream, v16, /*keep_status=*/i > 0);
       if (s != SAGE_OK) return s;
       e = cudaEventRecord(rt.computed[sl], st);
       // output: after the chunk was computed
@@ -871,6 +890,41 @@ sage_status sage_debug_qk_int32(const sage_quantized* qt, int64_t seg, int64_t h
   return ok();
 }
 
+sage_status sage_debug_pv_accum(const uint8_t* p8, const uint8_t* v8, int64_t ntiles,
+                                int64_t Dp, float* out, uint32_t* status,
+                                sage_stream_t stream) {
+  if (p8 == nullptr || v8 == nullptr || out == nullptr || status == nullptr)
+    return fail(SAGE_ERR_INVALID_ARG, "null argument");
+  if (Dp != 64 && Dp != 128) return fail(SAGE_ERR_INVALID_ARG, "Dp must be 64 or 128");
+  if (ntiles < 1 || ntiles > 4096)
+    return fail(SAGE_ERR_INVALID_ARG, "ntiles must be 1..4096 (got %lld)", (long long)ntiles);
+  if (!aligned(p8, 16) || !aligned(v8, 16) || !aligned(out, 4) || !aligned(status, 4))
+    return fail(SAGE_ERR_INVALID_ARG, "p8 and v8 must be 16-byte aligned, out and status 4");
+  sage_status s = check_device();
+  if (s != SAGE_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(status, 0, 4, st);
+  if (e == cudaSuccess) e = launch_debug_pv(p8, v8, ntiles, Dp, out, status, kDefaultTimeoutNs, st);
+  if (e != cudaSuccess) return cuda_fail(e, "debug pv launch");
+  return ok();
+}
+
+sage_status sage_debug_tc_rate(int kind, int64_t n_mma, uint32_t* status,
+                               sage_stream_t stream) {
+  if (kind != 0 && kind != 1) return fail(SAGE_ERR_INVALID_ARG, "kind must be 0 or 1");
+  if (n_mma < 1 || n_mma > (int64_t(1) << 22))
+    return fail(SAGE_ERR_INVALID_ARG, "n_mma must be 1..2^22");
+  if (status == nullptr || !aligned(status, 4))
+    return fail(SAGE_ERR_INVALID_ARG, "status must be a 4-byte aligned device pointer");
+  sage_status s = check_device();
+  if (s != SAGE_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(status, 0, 4, st);
+  if (e == cudaSuccess) e = launch_tc_rate(kind, n_mma, status, kDefaultTimeoutNs, st);
+  if (e != cudaSuccess) return cuda_fail(e, "tensor-core rate launch");
+  return ok();
+}
+
 sage_status sage_debug_e4m3(const float* in, uint8_t* out, int64_t n, sage_stream_t stream) {
   if (n < 0 || (n > 0 && (in == nullptr || out == nullptr)))
     return fail(SAGE_ERR_INVALID_ARG, "bad buffers");
@@ -886,17 +940,19 @@ void sage_debug_set_fault(int skip_kv_tile, uint64_t timeout_ns) {
   g_timeout_ns.store(timeout_ns);
 }
 
+void sage_debug_set_fault_launches(int launches) {
+  g_fault_launches.store(launches < 0 ? -1 : launches);
+}
+
 void sage_debug_set_prologue_launches(int launches) {
   g_prologue_launches.store(launches == 1 || launches == 2 ? launches : 0);
 }
 
-sage_status sage_device_status(const void* ws, sage_stream_t stream) {
-  if (ws == nullptr) return fail(SAGE_ERR_INVALID_ARG, "null workspace");
-  uint32_t word = 0;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(&word, ws, 4, cudaMemcpyDeviceToHost, st);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+}  // extern "C"
+
+namespace {
+// The sage_status a device status word stands for.
+sage_status status_of_word(uint32_t word) {
   if (word & kStatusTimeout)
     return fail(SAGE_ERR_DEVICE_TIMEOUT, "a device-side wait ran out (status 0x%x)", word);
   if (word & kStatusBadSeqlens)
@@ -905,6 +961,28 @@ sage_status sage_device_status(const void* ws, sage_stream_t stream) {
     return fail(SAGE_ERR_UNSUPPORTED, "internal error: a prologue work item fell outside "
                 "the call's plan and was skipped");
   return ok();
+}
+}  // namespace
+
+extern "C" {
+
+sage_status sage_device_status(const void* ws, sage_stream_t stream) {
+  if (ws == nullptr) return fail(SAGE_ERR_INVALID_ARG, "null workspace");
+  uint32_t word = 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&word, ws, 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+  return status_of_word(word);
+}
+
+sage_status sage_kv_stats_noalloc_status(sage_stream_t stream) {
+  sage_status s = check_device();
+  if (s != SAGE_OK) return s;
+  uint32_t word = 0;
+  cudaError_t e = read_kv_stats_static_status(&word, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "reading the static scratch's status word");
+  return status_of_word(word);
 }
 
 sage_status sage_kv_stats_noalloc(const void* k, const void* v, int dtype, int layout,

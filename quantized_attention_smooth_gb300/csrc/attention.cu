@@ -8,7 +8,7 @@
 //   m'  = max(m, rowmax x);  P = 2^(x - m');  l = l * 2^(m - m') + sum P
 //   O   = O * 2^(m - m') + e4m3(448 P) . v~
 // and finally out = O * s_v / (448 l) in fp32 for the caller's D channels.
-// The kernel carries 448 P directly (2^(x - m' + log2 448)) and 448 l.
+// The kernel carries 448 P and 448 l (the FP16-PV variant: P and l).
 //
 // GB300 mapping.  sm_103a has no INT8 tcgen05 MMA, so QK^T runs as
 // kind::f16 on operands that hold the int8 codes as exact fp16 integers;
@@ -42,6 +42,8 @@
 
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "sage_device.cuh"
 #include "sage_geom.h"
 #include "sage_kernels.h"
@@ -52,9 +54,9 @@ namespace {
 constexpr int kKStages = 2;   // K ring (released after the second QK^T)
 constexpr int kThreads = 512;
 constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2_448 = 8.80735492205760410750f;
 constexpr int kAtomBytes = 128 * 128;   // 128 rows x 128 bytes (swizzle atom column)
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr float kLog2_448 = 8.80735492205760410750f;
 // register split (launch: 512 threads x 128): 2 x 128 x 192 + 128 x 80 + 128 x 48
 constexpr int kSoftmaxRegs = 192;
 constexpr int kCorrRegs = 80;
@@ -655,26 +657,37 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
       alpha_s[(2 * t + (j & 1)) * kBlockM + r] = alpha;
       mbar_arrive(&alpha_ready[2 * t + (j & 1)]);        // correction may rescale O now
 
-      // 448 P = 2^(S c - m' + log2 448), quantised to e4m3; the FP16-PV
-      // variant takes P = 2^(S c - m') itself, rounded to fp16
-      const float bias = kV16 ? -m_new : kLog2_448 - m_new;
-      // packed fp32 pairs: the fused multiply-add rounds like fmaf, and the
-      // two packed sums keep the four chains (element i goes to chain i % 4)
-      const float2 c2 = make_float2(c, c), b2 = make_float2(bias, bias);
+      // The oracle's rounding order: the logit x = RN(S c), then
+      // d = RN(x - m'), then P = 2^d and P~ = e4m3(448 P) (the FP16-PV
+      // variant rounds P itself to fp16).  The subtraction is an FMA with
+      // the run-time multiplier `one` = 1, so it cannot be fused with the
+      // product: a fused S c - m' would skip the logit's own rounding, which
+      // at |x| ~ 1e4 is worth ~5e-4 in the exponent and flips e4m3 codes.
+      // 448 P is taken as 2^(RN(d + log2 448)): for the d that carry weight
+      // (|d| < 24) that rounding moves P by at most 2^-20 ln 2 relative, the
+      // size of the exp2 unit's own error, and it costs one packed add where
+      // a multiply after the exp2 would lengthen the chain to the e4m3
+      // conversion.  Packed fp32 pairs; the two packed sums keep four chains
+      // (element i goes to chain i % 4).
+      const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_new, -m_new);
+      const float2 one2 = make_float2(p.one, p.one);
+      const float2 kL448 = make_float2(kLog2_448, kLog2_448);
       float2 a01 = make_float2(0.0f, 0.0f), a23 = make_float2(0.0f, 0.0f);
       uint32_t w[kV16 ? 64 : 32];
 #pragma unroll
       for (int q4 = 0; q4 < 32; ++q4) {
         const int i = 4 * q4;
         const uint32_t* src = &sr[i >> 5][i & 31];
-        const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(src[0]), __uint_as_float(src[1])),
-                                      c2, b2);
-        const float2 x23 = __ffma2_rn(make_float2(__uint_as_float(src[2]), __uint_as_float(src[3])),
-                                      c2, b2);
-        const float2 p01 = make_float2(fast_exp2(x01.x), fast_exp2(x01.y));
-        const float2 p23 = make_float2(fast_exp2(x23.x), fast_exp2(x23.y));
-        a01 = __fadd2_rn(a01, p01);
-        a23 = __fadd2_rn(a23, p23);
+        const float2 x01 = __fmul2_rn(make_float2(__uint_as_float(src[0]), __uint_as_float(src[1])), c2);
+        const float2 x23 = __fmul2_rn(make_float2(__uint_as_float(src[2]), __uint_as_float(src[3])), c2);
+        float2 d01 = __ffma2_rn(x01, one2, nm2);
+        float2 d23 = __ffma2_rn(x23, one2, nm2);
+        if constexpr (!kV16) {                             // log2 of 448 P
+          d01 = __fadd2_rn(d01, kL448);
+          d23 = __fadd2_rn(d23, kL448);
+        }
+        const float2 p01 = make_float2(fast_exp2(d01.x), fast_exp2(d01.y));
+        const float2 p23 = make_float2(fast_exp2(d23.x), fast_exp2(d23.y));
         if constexpr (kV16) {
           const __half2 h01 = __floats2half2_rn(p01.x, p01.y);
           const __half2 h23 = __floats2half2_rn(p23.x, p23.y);
@@ -683,6 +696,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
         } else {
           w[q4] = pack_e4m3x2(p01.x, p01.y) | (pack_e4m3x2(p23.x, p23.y) << 16);
         }
+        a01 = __fadd2_rn(a01, p01);
+        a23 = __fadd2_rn(a23, p23);
       }
       const float a0 = a01.x, a1 = a01.y, a2 = a23.x, a3 = a23.y;
       // the P~ buffer is free once PV(j-1) has read it
@@ -788,6 +803,127 @@ debug_qk_kernel(const __grid_constant__ CUtensorMap tm_q,
   }
 }
 
+// ------------------------------------------------ debug: PV accumulation
+// O (128 x DP fp32 in TMEM) = sum over ntiles of P~_t . V~_t^T through the
+// attention kernel's own PV instructions (issue_pv: kind::f8f6f4, e4m3
+// operands in the 128-byte swizzled K-major shared-memory layout, K = 32
+// per MMA, the first MMA overwriting).  p8: [ntiles][128 rows][128 keys],
+// v8: [ntiles][DP channels][128 keys], e4m3 codes; 16-byte aligned rows.
+// One CTA of 128 threads: each tile is staged by plain loads with the
+// swizzle the softmax uses for P~, then one thread issues the MMAs and
+// waits (bounded) for them before the next tile overwrites the operands.
+template <int DP>
+__global__ void __launch_bounds__(128, 1)
+debug_pv_kernel(const uint8_t* p8, const uint8_t* v8, int64_t ntiles, float* out,
+                uint32_t* status, uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* ps = smem;                                  // 128 x 128 e4m3
+  uint8_t* vs = smem + kBlockM * kBlockN;              // DP x 128 e4m3
+  uint64_t* mma_done = reinterpret_cast<uint64_t*>(vs + DP * kBlockN);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  const int warp = threadIdx.x >> 5, r = threadIdx.x;
+  if (r == 0) {
+    mbar_init(mma_done, 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, 128);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  bool ok = true;
+  for (int64_t t = 0; ok && t < ntiles; ++t) {
+    const uint4* prow = reinterpret_cast<const uint4*>(p8 + (t * kBlockM + r) * kBlockN);
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<uint4*>(ps + r * 128 + ((c ^ (r & 7)) << 4)) = prow[c];
+    if (r < DP) {
+      const uint4* vrow = reinterpret_cast<const uint4*>(v8 + (t * DP + r) * kBlockN);
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(vs + r * 128 + ((c ^ (r & 7)) << 4)) = vrow[c];
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (r == 0) {
+      tc_fence_after();
+      issue_pv<DP>(tbase, sdesc_sw128_lo(smem_u32(ps)), sdesc_sw128_lo(smem_u32(vs)), t > 0);
+      tc_commit(mma_done);
+      ok = mbar_wait(mma_done, static_cast<uint32_t>(t & 1), nullptr, status, timeout_ns);
+    }
+    ok = __syncthreads_and(ok);                        // operands read before reuse
+  }
+  if (ok) {
+    tc_fence_after();
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+#pragma unroll 1
+    for (int cc = 0; cc < DP / 32; ++cc) {
+      uint32_t v[32];
+      tmem_ld32(tbase + lane_off + 32 * cc, v);
+      tmem_ld_wait();
+      reg_fence(v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) out[r * DP + 32 * cc + i] = __uint_as_float(v[i]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, 128);
+  }
+}
+
+// ------------------------------------------------ tensor-core rate
+// One CTA per SM; one thread issues n back-to-back M=128 N=128 MMAs of the
+// attention kernel's two kinds (kind 0: fp16 operands, K=16, as QK^T; kind
+// 1: e4m3 operands, K=32, as PV) from zeroed shared-memory operands into one
+// TMEM accumulator, commits once and waits (bounded).  Timed by the caller
+// around the launch, it gives the tensor pipe's rate at the clock the GPU
+// runs at that moment.
+template <int kKind>
+__global__ void __launch_bounds__(128, 1)
+tc_rate_kernel(int64_t n, uint32_t* status, uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* done = reinterpret_cast<uint64_t*>(smem + 2 * kAtomBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  for (int i = threadIdx.x; i < 2 * kAtomBytes / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  if (threadIdx.x == 0) {
+    mbar_init(done, 1);
+    mbar_fence_init();
+  }
+  if (threadIdx.x < 32) tmem_alloc(tmem_slot, 128);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  if (threadIdx.x == 0) {
+    const uint32_t a_lo = sdesc_sw128_lo(smem_u32(smem));
+    const uint32_t b_lo = sdesc_sw128_lo(smem_u32(smem + kAtomBytes));
+    constexpr uint32_t idesc = kKind == 0 ? make_idesc(kFmtF16, kFmtF16, kBlockM, kBlockN)
+                                          : make_idesc(kFmtE4M3, kFmtE4M3, kBlockM, kBlockN);
+    for (int64_t i = 0; i < n; ++i) {
+      const uint32_t off = static_cast<uint32_t>(i & 3) * 2;   // 32-byte K slices of the atom
+      if constexpr (kKind == 0) mma_f16_ss_lo(tbase, a_lo + off, b_lo + off, idesc, i > 0);
+      else mma_f8_ss_lo(tbase, a_lo + off, b_lo + off, idesc, i > 0);
+    }
+    tc_commit(done);
+    mbar_wait(done, 0, nullptr, status, timeout_ns);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 128);
+  }
+}
+
 __global__ void debug_e4m3_kernel(const float* in, uint8_t* out, int64_t n) {
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
        i < n; i += static_cast<int64_t>(gridDim.x) * blockDim.x)
@@ -798,17 +934,18 @@ template <int DP, bool kV16>
 cudaError_t launch_attention_t(const AttnMaps& maps, const AttnParams& p,
                                cudaStream_t st) {
   using L = Layout<DP, kV16>;
-  // the shared-memory limit is a per-device attribute of the kernel
-  static bool configured[64] = {};
+  // the shared-memory limit is a per-device attribute of the kernel (set
+  // once; concurrent first calls set the same value)
+  static std::atomic<bool> configured[64] = {};
   int cdev = 0;
   cudaError_t ce = cudaGetDevice(&cdev);
   if (ce != cudaSuccess) return ce;
   if (cdev < 0 || cdev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[cdev]) {
+  if (!configured[cdev].load(std::memory_order_relaxed)) {
     ce = cudaFuncSetAttribute(attn_kernel<DP, kV16>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (ce != cudaSuccess) return ce;
-    configured[cdev] = true;
+    configured[cdev].store(true, std::memory_order_relaxed);
   }
   const int64_t maxq = p.g.varlen ? p.g.max_q : p.g.Lq;
   const int64_t nqt = (maxq + kBlockM - 1) / kBlockM;      // query tiles, two per CTA
@@ -821,20 +958,20 @@ cudaError_t launch_attention_t(const AttnMaps& maps, const AttnParams& p,
     // Uniform pairs run in waves of one CTA per SM.  When the last wave is
     // at most half full, its pairs run as single tiles instead (launched
     // last), which shortens that wave to one tile's time.
-    static int sms[64] = {};
+    static std::atomic<int> sms[64] = {};       // resident CTAs per device, filled once
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && sms[dev] == 0) {
+    if (dev >= 0 && dev < 64 && sms[dev].load(std::memory_order_relaxed) == 0) {
       int n = 0, per = 0;
       e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
       if (e != cudaSuccess) return e;
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, attn_kernel<DP, kV16>, kThreads,
                                                         L::kAlloc);
       if (e != cudaSuccess) return e;
-      sms[dev] = n * (per > 0 ? per : 1);
+      sms[dev].store(n * (per > 0 ? per : 1), std::memory_order_relaxed);
     }
-    const int64_t wave = (dev >= 0 && dev < 64) ? sms[dev] : 0;
+    const int64_t wave = (dev >= 0 && dev < 64) ? sms[dev].load(std::memory_order_relaxed) : 0;
     const int64_t pairs = static_cast<int64_t>(grid.x) * grid.y * grid.z;
     const int64_t tail = wave > 0 ? pairs % wave : 0;
     if (tail > 0 && 2 * tail <= wave && pairs + tail < (int64_t(1) << 31)) {
@@ -852,19 +989,28 @@ template <int DP>
 cudaError_t launch_debug_qk_t(const AttnMaps& maps, const AttnParams& p,
                               int64_t q_row0, int64_t k_row0, int32_t* out,
                               cudaStream_t st) {
-  static bool configured[64] = {};            // per-device kernel attribute
+  static std::atomic<bool> configured[64] = {};   // per-device kernel attribute
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
+  if (!configured[dev].load(std::memory_order_relaxed)) {
     e = cudaFuncSetAttribute(debug_qk_kernel<DP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Layout<DP>::kAlloc);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[dev].store(true, std::memory_order_relaxed);
   }
   debug_qk_kernel<DP><<<1, 128, Layout<DP>::kAlloc, st>>>(maps.q, maps.k, q_row0, k_row0,
                                                           out, p.status, p.timeout_ns);
+  note_launch();
+  return cudaGetLastError();
+}
+
+template <int DP>
+cudaError_t launch_debug_pv_t(const uint8_t* p8, const uint8_t* v8, int64_t ntiles, float* out,
+                              uint32_t* status, uint64_t timeout_ns, cudaStream_t st) {
+  constexpr int kSmem = kBlockM * kBlockN + DP * kBlockN + 16 + 1024;
+  debug_pv_kernel<DP><<<1, 128, kSmem, st>>>(p8, v8, ntiles, out, status, timeout_ns);
   note_launch();
   return cudaGetLastError();
 }
@@ -894,6 +1040,37 @@ cudaError_t launch_debug_e4m3(const float* in, uint8_t* out, int64_t n,
   debug_e4m3_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(in, out, n);
   note_launch();
   return cudaGetLastError();
+}
+
+cudaError_t launch_tc_rate(int kind, int64_t n_mma, uint32_t* status, uint64_t timeout_ns,
+                           cudaStream_t st) {
+  // more shared memory than two CTAs can hold: exactly one CTA per SM
+  constexpr int kSmem = 120 * 1024;
+  static std::atomic<bool> configured[64] = {};
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev].load(std::memory_order_relaxed)) {
+    e = cudaFuncSetAttribute(tc_rate_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc_rate_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmem);
+    if (e != cudaSuccess) return e;
+    configured[dev].store(true, std::memory_order_relaxed);
+  }
+  if (kind == 0) tc_rate_kernel<0><<<sms, 128, kSmem, st>>>(n_mma, status, timeout_ns);
+  else tc_rate_kernel<1><<<sms, 128, kSmem, st>>>(n_mma, status, timeout_ns);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_pv(const uint8_t* p8, const uint8_t* v8, int64_t ntiles, int64_t Dp,
+                            float* out, uint32_t* status, uint64_t timeout_ns,
+                            cudaStream_t st) {
+  return Dp == 64 ? launch_debug_pv_t<64>(p8, v8, ntiles, out, status, timeout_ns, st)
+                  : launch_debug_pv_t<128>(p8, v8, ntiles, out, status, timeout_ns, st);
 }
 
 }  // namespace sage

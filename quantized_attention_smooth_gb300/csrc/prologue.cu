@@ -51,6 +51,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "sage_device.cuh"
@@ -1373,12 +1374,14 @@ bool view_map(CUtensorMap* map, const uint16_t* base, int64_t D, int64_t Dp, int
 
 template <bool kTma, bool kBf16, int DP>
 cudaError_t launch_t(ProParams& prm, int mode, cudaStream_t st) {
-  static int per_sm[64] = {};                  // resident CTAs per SM, per device
+  // resident CTAs per SM, per device (filled once; every thread computes
+  // the same value, so relaxed atomics suffice)
+  static std::atomic<int> per_sm[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (per_sm[dev] == 0) {
+  if (per_sm[dev].load(std::memory_order_relaxed) == 0) {
     e = cudaFuncSetAttribute(prologue_kernel<kTma, kBf16, DP>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes));
@@ -1387,7 +1390,7 @@ cudaError_t launch_t(ProParams& prm, int mode, cudaStream_t st) {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prologue_kernel<kTma, kBf16, DP>,
                                                       kThreads, kSmemBytes);
     if (e != cudaSuccess) return e;
-    per_sm[dev] = n > 0 ? n : 1;
+    per_sm[dev].store(n > 0 ? n : 1, std::memory_order_relaxed);
   }
   int sms = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1396,7 +1399,7 @@ cudaError_t launch_t(ProParams& prm, int mode, cudaStream_t st) {
   if (prm.plan.groups <= 0) return cudaSuccess;
   // every CTA is resident at once (the group barriers count them all): a
   // cooperative launch of exactly the resident CTAs
-  const unsigned grid = static_cast<unsigned>(sms * per_sm[dev]);
+  const unsigned grid = static_cast<unsigned>(sms * per_sm[dev].load(std::memory_order_relaxed));
   void* args[] = {&prm};
   e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(prologue_kernel<kTma, kBf16, DP>),
                                   dim3(grid), dim3(kThreads), args, kSmemBytes, st);
@@ -1467,18 +1470,20 @@ cudaError_t launch_prologue(const SegGeo& g, const PrologueBuffers& b,
   // statistics (counters of their own).
   const int64_t ntk = g.varlen ? g.total_k : g.nseg * g.Lk;
   const int64_t kv_bytes = 2 * ntk * g.Hkv * g.D * 2;
-  static int64_t l2_bytes[64] = {};
+  static std::atomic<int64_t> l2_bytes[64] = {};      // per device, filled once
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (l2_bytes[dev] == 0) {
+  int64_t l2b = l2_bytes[dev].load(std::memory_order_relaxed);
+  if (l2b == 0) {
     int l2 = 0;
     e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
     if (e != cudaSuccess) return e;
-    l2_bytes[dev] = l2 > 0 ? l2 : 1;
+    l2b = l2 > 0 ? l2 : 1;
+    l2_bytes[dev].store(l2b, std::memory_order_relaxed);
   }
-  const bool two = b.launches == 2 || (b.launches == 0 && 4 * kv_bytes > 5 * l2_bytes[dev]);
+  const bool two = b.launches == 2 || (b.launches == 0 && 4 * kv_bytes > 5 * l2b);
   if (!two) return launch_any(prm, vec, kPlanAll, st);
   e = launch_any(prm, vec, kPlanStatsQ, st);
   if (e != cudaSuccess) return e;
@@ -1505,6 +1510,13 @@ constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 }  // namespace
+
+cudaError_t read_kv_stats_static_status(uint32_t* word, cudaStream_t st) {
+  cudaError_t e = cudaMemcpyFromSymbolAsync(word, g_stats_scratch, sizeof(uint32_t), 0,
+                                            cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return e;
+}
 
 cudaError_t launch_kv_stats_static(const SegGeo& g, const uint16_t* k,
                                    const uint16_t* v, float* k_mean, float* s_v,

@@ -53,6 +53,10 @@ cudaError_t launch_kv_stats_static(const SegGeo& g, const uint16_t* k,
                                    const uint16_t* v, float* k_mean, float* s_v,
                                    bool vec, uint64_t timeout_ns, cudaStream_t st);
 
+// Reads (synchronising st) the status word at the start of that static
+// array on the current device.
+cudaError_t read_kv_stats_static_status(uint32_t* word, cudaStream_t st);
+
 struct AttnParams {
   SegGeo g;
   const float* s_q;
@@ -62,6 +66,9 @@ struct AttnParams {
   // output addressing in elements; varlen segments start at cu_q[s]*tok
   int64_t out_seg_stride, out_head_stride, out_tok_stride;
   float scale_log2;          // sm_scale * log2(e)
+  float one;                 // 1.0f: the multiplier of the FMA that subtracts the row
+                             // max from a rounded logit (a run-time value, so the
+                             // compiler cannot fuse that subtraction with the product)
   int32_t causal;
   int32_t skip_kv_tile;      // failure-injection hook, -1 = off
   int32_t v16;               // FP16-PV variant: V and P~ in fp16, single-stage K and V rings
@@ -84,6 +91,13 @@ cudaError_t launch_attention(const AttnMaps& maps, const AttnParams& p,
 cudaError_t launch_debug_qk(const AttnMaps& maps, const AttnParams& p,
                             int64_t q_row0, int64_t k_row0, int32_t* out,
                             cudaStream_t st);
+
+cudaError_t launch_debug_pv(const uint8_t* p8, const uint8_t* v8, int64_t ntiles, int64_t Dp,
+                            float* out, uint32_t* status, uint64_t timeout_ns,
+                            cudaStream_t st);
+
+cudaError_t launch_tc_rate(int kind, int64_t n_mma, uint32_t* status, uint64_t timeout_ns,
+                           cudaStream_t st);
 
 cudaError_t launch_debug_e4m3(const float* in, uint8_t* out, int64_t n,
                               cudaStream_t st);

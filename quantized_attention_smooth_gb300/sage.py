@@ -27,6 +27,8 @@ EXPORTS = (
     "sage_kv_stats_noalloc", "sage_launch_count", "sage_quant_prologue_strided",
     "sage_attn_fwd_strided", "sage_quant_prologue_pv16", "sage_attn_fwd_pv16",
     "sage_workspace_bytes_host", "sage_attn_fwd_host", "sage_attn_fwd_host_pv16",
+    "sage_debug_pv_accum", "sage_debug_set_fault_launches", "sage_kv_stats_noalloc_status",
+    "sage_debug_tc_rate",
 )
 
 
@@ -89,8 +91,12 @@ def _load():
                                   I, P, SZ, P], I),
         "sage_debug_qk_int32": ([QP, I64, I64, I64, I64, P, P], I),
         "sage_debug_e4m3": ([P, P, I64, P], I),
+        "sage_debug_pv_accum": ([P, P, I64, I64, P, P, P], I),
         "sage_debug_set_fault": ([I, ctypes.c_uint64], None),
         "sage_debug_set_prologue_launches": ([I], None),
+        "sage_debug_set_fault_launches": ([I], None),
+        "sage_debug_tc_rate": ([I, I64, P, P], I),
+        "sage_kv_stats_noalloc_status": ([P], I),
         "sage_device_status": ([P, P], I),
         "sage_last_error": ([], ctypes.c_char_p),
         "sage_kv_stats_noalloc": ([P, P, I, I, I64, I64, I64, I64, P, P, P], I),
@@ -420,22 +426,75 @@ def debug_e4m3(x, out=None, stream=None):
     return out
 
 
+def debug_pv_accum(p8, v8, status, out=None, stream=None):
+    """sum_t P~_t V~_t^T through the attention kernel's own FP8 PV instructions.
+    p8: uint8 CUDA tensor [ntiles, 128, 128] (e4m3 codes, key fastest);
+    v8: uint8 CUDA tensor [ntiles, Dp, 128] (channel-major); status: a 4-byte
+    CUDA tensor the call clears (read with device_status).  Returns fp32
+    [128, Dp]."""
+    import torch
+    for name, t in (("p8", p8), ("v8", v8)):
+        if not (t.is_cuda and t.is_contiguous() and t.dtype == torch.uint8):
+            raise ValueError(f"{name} must be a contiguous uint8 CUDA tensor")
+    ntiles, dp = v8.shape[0], v8.shape[1]
+    if tuple(p8.shape) != (ntiles, 128, 128) or tuple(v8.shape) != (ntiles, dp, 128):
+        raise ValueError("p8 must be [ntiles,128,128] and v8 [ntiles,Dp,128]")
+    if out is None:
+        out = torch.empty(128, dp, dtype=torch.float32, device=p8.device)
+    rc = _lib.sage_debug_pv_accum(_ptr(p8), _ptr(v8), ntiles, dp, _ptr(out), _ptr(status),
+                                  _stream(stream))
+    _check(rc, "sage_debug_pv_accum")
+    return out
+
+
 def kv_stats_noalloc(k, v, layout, k_mean, s_v, stream=None):
     """K channel means and V channel scales with no device allocation at all:
     the scratch is a static array inside the library (B*Hkv*Dp <= 16384).
-    k_mean and s_v are caller-owned fp32 tensors of B*Hkv*Dp elements."""
+    k_mean and s_v are caller-owned contiguous fp32 CUDA tensors of at least
+    B*Hkv*Dp elements (Dp = 64 if D <= 64 else 128).  kv_stats_noalloc_status
+    reports a failure on the device."""
+    import torch
+    if k.dim() != 4 or tuple(v.shape) != tuple(k.shape):
+        raise ValueError(f"kv_stats_noalloc: k {tuple(k.shape)} and v {tuple(v.shape)} must be "
+                         "4-D tensors of one shape")
     lay = _layout_code(layout)
     if lay == HND:
         B, Hkv, Lk, D = k.shape
     else:
         B, Lk, Hkv, D = k.shape
+    need = B * Hkv * (64 if D <= 64 else 128)
+    for name, t in (("k_mean", k_mean), ("s_v", s_v)):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError(f"kv_stats_noalloc: {name} must be a contiguous float32 tensor")
+        if t.numel() < need:
+            raise ValueError(f"kv_stats_noalloc: {name} has {t.numel()} elements, needs {need}")
+    _require_dense("kv_stats_noalloc", k, k, v)
+    for name, t in (("k_mean", k_mean), ("s_v", s_v)):
+        if not t.is_cuda:
+            raise ValueError(f"kv_stats_noalloc: {name} is not on a CUDA device")
     rc = _lib.sage_kv_stats_noalloc(_ptr(k), _ptr(v), _dtype_code(k), lay, B, Hkv, Lk, D,
                                     _ptr(k_mean), _ptr(s_v), _stream(stream))
     _check(rc, "sage_kv_stats_noalloc")
     return k_mean, s_v
 
 
-def set_fault(skip_kv_tile: int = -1, timeout_ns: int = 0):
+def debug_tc_rate(kind: int, n_mma: int, status, stream=None):
+    """Enqueues n_mma back-to-back M=128 N=128 tcgen05 MMAs per SM (kind 0:
+    fp16 K=16, kind 1: e4m3 K=32); time it with events on `stream`."""
+    _check(_lib.sage_debug_tc_rate(int(kind), int(n_mma), _ptr(status), _stream(stream)),
+           "sage_debug_tc_rate")
+
+
+def kv_stats_noalloc_status(stream=None) -> int:
+    """Device status of the last kv_stats_noalloc call on this device."""
+    return int(_lib.sage_kv_stats_noalloc_status(_stream(stream)))
+
+
+def set_fault(skip_kv_tile: int = -1, timeout_ns: int = 0, launches: int = -1):
+    """Failure injection: attention launches skip key/value tile skip_kv_tile
+    (-1: off) and give up waiting after timeout_ns; launches >= 0 limits the
+    fault to that many launches."""
+    _lib.sage_debug_set_fault_launches(int(launches))
     _lib.sage_debug_set_fault(int(skip_kv_tile), int(timeout_ns))
 
 

@@ -206,3 +206,31 @@ def test_host_buffer_call_automatic_chunk():
     # a chunk never exceeds the kv heads there are
     assert (L.sage_workspace_bytes_host(1, 8, 2, 128, 128, 64, 0) ==
             L.sage_workspace_bytes_host(1, 8, 2, 128, 128, 64, 2))
+
+
+@pytest.mark.parametrize("case,needle", [
+    ("v_shape", "one shape"),
+    ("mean_dtype", "contiguous float32"),
+    ("mean_view", "contiguous float32"),
+    ("mean_small", "needs"),
+    ("on_cpu", "not on a CUDA device"),
+])
+def test_noalloc_statistics_binding_refuses_bad_tensors(case, needle):
+    """The binding's own checks of the allocation-free statistics call, which
+    the C ABI cannot make (it sees plain pointers); every refusal is raised
+    before any call."""
+    import torch
+    k = torch.zeros(1, 2, 128, 64, dtype=torch.float16)
+    v = torch.zeros(1, 2, 128, 64, dtype=torch.float16)
+    k_mean = torch.zeros(2 * 64)
+    s_v = torch.zeros(2 * 64)
+    if case == "v_shape":
+        v = torch.zeros(1, 2, 100, 64, dtype=torch.float16)
+    elif case == "mean_dtype":
+        k_mean = torch.zeros(2 * 64, dtype=torch.float64)
+    elif case == "mean_view":
+        k_mean = torch.zeros(2 * 64 * 2)[::2]
+    elif case == "mean_small":
+        s_v = torch.zeros(2 * 64 - 1)
+    with pytest.raises(ValueError, match=needle):
+        sage.kv_stats_noalloc(k, v, "HND", k_mean, s_v)

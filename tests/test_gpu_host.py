@@ -78,3 +78,26 @@ def test_host_call_pv16_equals_device_call(sage):
     sage.attn_fwd_host(hq, hk, hv, out, "NHD", w.causal, scale, chunk_kv_heads=1, pv16=True)
     torch.cuda.synchronize()
     assert torch.equal(out, ref.cpu())
+
+
+def test_failure_in_an_early_chunk_stays_visible(sage):
+    """A bounded wait that runs out in the first of four chunks (the library's
+    failure-injection hook, limited to one attention launch) must still show
+    in the workspace's status word after the later chunks have run; the next
+    call clears it."""
+    w = _w("fault_chunks", B=2, Hq=4, Hkv=2, Lq=256, Lk=384, seed=905)
+    inp = wl.make_inputs(w)
+    d = H.device_inputs(w, inp)
+    hq, hk, hv = _host(d["q"]), _host(d["k"]), _host(d["v"])
+    out = torch.empty(hq.shape, dtype=torch.float32).pin_memory()
+    ws = sage.alloc_workspace(sage.workspace_bytes_host(w.B, w.Hq, w.Hkv, w.Lq, w.Lk, w.D, 1))
+    scale = wl.default_sm_scale(w)
+    try:
+        sage.set_fault(skip_kv_tile=1, timeout_ns=50_000_000, launches=1)
+        sage.attn_fwd_host(hq, hk, hv, out, "HND", False, scale, ws=ws, chunk_kv_heads=1)
+        status = sage.device_status(ws)                    # synchronises
+    finally:
+        sage.set_fault(-1, 0)
+    assert status == sage.ERR_DEVICE_TIMEOUT
+    sage.attn_fwd_host(hq, hk, hv, out, "HND", False, scale, ws=ws, chunk_kv_heads=1)
+    assert sage.device_status(ws) == sage.OK

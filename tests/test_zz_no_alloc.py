@@ -6,11 +6,14 @@ forbids its extensions to allocate, or a latency-critical loop that cannot
 pay for cudaMalloc's implicit device synchronisation.  This entry point keeps
 its scratch accumulators in a static device array inside the library.
 
-The test calls it twice in a row on different problems (a large one, then a
-smaller one, so stale accumulators from the first call would show) and
-compares both results, bit for bit, with the K channel means and V channel
-scales written by the workspace-based prologue.  This file is named so that
-pytest collects it last.
+The test calls it on several problems in a row (a large one, then smaller
+ones, so stale accumulators from an earlier call would show), one of them
+with a head dimension that forces element-wise loads (D=100) and one whose
+channels are padded (D=40, padded to 64), and compares every result, bit for
+bit, with the K channel means and V channel scales written by the
+workspace-based prologue; padded channels must be exactly zero and the
+call's device status word must read OK.  This file is named so that pytest
+collects it last.
 """
 import numpy as np
 import pytest
@@ -36,6 +39,8 @@ def _case(name, B, Hkv, Lk, D, dtype, layout, seed):
 CASES = [
     ("b2_h24_l4096_d128", 2, 24, 4096, 128, wl.F16, wl.HND, 1101),
     ("b3_h4_l1000_d80_nhd", 3, 4, 1000, 80, wl.BF16, wl.NHD, 1102),
+    ("b1_h3_l777_d100_nhd_elementwise", 1, 3, 777, 100, wl.F16, wl.NHD, 1103),
+    ("b2_h2_l300_d40_padded", 2, 2, 300, 40, wl.BF16, wl.HND, 1104),
 ]
 
 
@@ -54,9 +59,12 @@ def test_noalloc_statistics_match_the_prologue_on_two_calls_in_a_row():
         k_mean = torch.full((n,), float("nan"), device="cuda")
         s_v = torch.full((n,), float("nan"), device="cuda")
         sage.kv_stats_noalloc(k, v, lay, k_mean, s_v)
-        torch.cuda.synchronize()
+        assert sage.kv_stats_noalloc_status() == sage.OK, (name, sage.last_error())
         assert torch.equal(k_mean.view(torch.int32), ref_mean.view(torch.int32)), name
         assert torch.equal(s_v.view(torch.int32), ref_sv.view(torch.int32)), name
+        if Dp > D:                                          # padded channels
+            assert torch.all(k_mean.view(B * Hkv, Dp)[:, D:] == 0), name
+            assert torch.all(s_v.view(B * Hkv, Dp)[:, D:] == 0), name
 
 
 def test_noalloc_rejects_problems_beyond_the_static_scratch():
