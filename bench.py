@@ -35,11 +35,16 @@ L2_FLUSH_BYTES = 256 << 20
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # DRAM bytes (read + write) per attention-kernel launch on the default
-# workload, from the ncu capture summarised in
-# profiles/attn_kernel_b2_h24_l4096_d128.md (None for other workloads).
-ATTN_NCU_DRAM_BYTES = {"b2_h24_l4096_d128": 126.746624e6 + 60.900096e6}
+# workload, from the ncu capture of the attention kernel (None where no
+# capture of the current kernel exists).
+ATTN_NCU_DRAM_BYTES = {}
 # the same for the FP16-PV variant's attention kernel (fp16 V and P~)
-ATTN16_NCU_DRAM_BYTES = {"b2_h24_l4096_d128": 152.014336e6 + 63.817216e6}
+ATTN16_NCU_DRAM_BYTES = {}
+# (query row, key) pairs of attention in the oracle's bounded sample (one
+# head of the 4096 x 4096 workload; a whole small workload)
+ORACLE_PAIR_BUDGET = 4096 * 4096
+# flops of one M=128 N=128 tcgen05 MMA of each kind (sage_debug_tc_rate)
+TC_FLOP = {0: 2.0 * 128 * 128 * 16, 1: 2.0 * 128 * 128 * 32}
 
 
 def load_peaks():
@@ -248,14 +253,18 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int):
         e2e_ev.append((a, b))
     torch.cuda.synchronize()
     # query head 0 of segment 0 of the last output, for the parity sample
-    out_rows = np.array(wl.out_segment(w, out_host.numpy(), 0, inp.get("cu_q"))[0][:args.cpu_rows])
+    out_rows = np.array(wl.out_segment(w, out_host.numpy(), 0, inp.get("cu_q"))[0])
     e2e_ev = e2e_ev[-n_e2e:]
     e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
     h2d = sum(host[k].numel() * host[k].element_size() for k in ("q", "k", "v"))
     d2h = out_host.numel() * 4
 
+    # the tensor pipe's rate for the kernel's two MMA kinds, measured now, at
+    # the clock the GPU runs under this load (sage_debug_tc_rate)
+    tc = tensor_rates(torch, sage, stream, dev)
+
     Dp = 64 if w.D <= 64 else 128
-    r = dict(total_ms=total_ms, step_ms=step_ms, pro_ms=pro_ms, att_ms=att_ms,
+    r = dict(tc=tc, total_ms=total_ms, step_ms=step_ms, pro_ms=pro_ms, att_ms=att_ms,
              launches_per_step=launches_per_step, launches=launches,
              e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, ops=workload_ops(w), out_rows=out_rows,
              e2e_api=(("sage_attn_fwd_host_pv16" if pv16 else "sage_attn_fwd_host") +
@@ -266,6 +275,28 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int):
              ops_padded_effective=w.ops(dim=Dp, causal_effective=True),
              clocks=clock_info)
     return reduce_over_ranks(r, world, dev)
+
+
+def tensor_rates(torch, sage, stream, dev, n_mma: int = 1 << 15, reps: int = 5):
+    """TFLOP/s of back-to-back M=128 N=128 tcgen05 MMAs on every SM, per kind
+    (0: fp16 K=16, 1: e4m3 K=32): best of `reps` event-timed launches."""
+    status = torch.zeros(64, dtype=torch.int32, device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = {}
+    for kind in (0, 1):
+        sage.debug_tc_rate(kind, 1024, status, stream)          # warm-up
+        best = None
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            sage.debug_tc_rate(kind, n_mma, status, stream)
+            b.record(stream)
+            b.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        assert sage.device_status(status) == sage.OK, sage.last_error()
+        out[kind] = TC_FLOP[kind] * n_mma * sms / (best * 1e-3) / 1e12
+    return out
 
 
 # ---------------------------------------------------------- rank aggregation
@@ -308,18 +339,35 @@ def job_figures(r: dict, world: int, steps: int) -> dict:
 
 
 # ---------------------------------------------------------- CPU oracle arm
-def oracle_sample(w: wl.Workload, inp: dict, rows: int, heads: int = 1, pv16: bool = False):
-    """Times the oracle (prologue + attention; the FP16-PV variant's when pv16)
-    on `heads` query heads of segment 0 and its first `rows` query rows;
-    returns (ops, seconds, threads, output rows [rows, D] of query head 0)."""
-    import oracle
-    q, k, v = wl.segment(w, inp, 0)
-    # query head 0 reads kv head 0 for every GQA grouping
-    qs = np.ascontiguousarray(q[:1])
-    ks = np.ascontiguousarray(k[:1])
-    vs = np.ascontiguousarray(v[:1])
+def oracle_sample_plan(w: wl.Workload, budget: int = ORACLE_PAIR_BUDGET):
+    """The oracle's bounded sample of a workload, the same in both arms:
+    segment 0, query rows [0, rows) of query heads [0, heads), with
+    rows * Lk <= budget (row, key) pairs per head and as many heads as fit
+    the budget (whole groups of the heads that share a kv head).  Returns
+    (heads, kv_heads, rows)."""
     lq, lk = w.seg_lengths()[0]
-    rows = min(rows, lq)
+    rows = max(1, min(lq, budget // max(lk, 1)))
+    group = w.Hq // w.Hkv
+    fit = max(1, budget // max(rows * max(lk, 1), 1))
+    heads = min(w.Hq, fit)
+    if heads >= group:
+        heads = heads // group * group
+        return heads, heads // group, rows
+    return 1, 1, rows            # query head 0 alone reads kv head 0
+
+
+def oracle_sample(w: wl.Workload, inp: dict, pv16: bool = False,
+                  budget: int = ORACLE_PAIR_BUDGET):
+    """Times the oracle (prologue + attention; the FP16-PV variant's when pv16)
+    on the sample of oracle_sample_plan; returns (ops, seconds, threads,
+    output rows [rows, D] of query head 0, description)."""
+    import oracle
+    heads, kv_heads, rows = oracle_sample_plan(w, budget)
+    q, k, v = wl.segment(w, inp, 0)
+    qs = np.ascontiguousarray(q[:heads])
+    ks = np.ascontiguousarray(k[:kv_heads])
+    vs = np.ascontiguousarray(v[:kv_heads])
+    lq, lk = w.seg_lengths()[0]
     t0 = time.perf_counter()
     pro = oracle.prologue(qs, ks, vs, w.dtype)
     if pv16:
@@ -335,8 +383,12 @@ def oracle_sample(w: wl.Workload, inp: dict, rows: int, heads: int = 1, pv16: bo
         pairs *= w.ops() / w.ops(causal_effective=True)
     else:
         pairs = rows * lk
-    ops = 4.0 * qs.shape[0] * pairs * w.D
-    return ops, dt, os.cpu_count(), ref[0, :rows]
+    ops = 4.0 * heads * pairs * w.D
+    whole = heads == w.Hq and rows == lq and w.nseg == 1
+    desc = (f"segment 0, query heads [0,{heads}), rows [0,{rows}) of each"
+            f"{' (the whole workload)' if whole else ''}: the prologue of those heads plus "
+            f"attention, scaled to the workload's op count by the sample's (row, key) pairs")
+    return ops, dt, os.cpu_count(), ref[0, :rows], desc
 
 
 def reference_arm(args, w: wl.Workload, rank: int, world: int):
@@ -345,18 +397,15 @@ def reference_arm(args, w: wl.Workload, rank: int, world: int):
     import oracle
     oracle.build()
     inp = wl.make_inputs(w)
-    rows = args.ref_rows
     pv16 = args.variant == "pv16"
     for _ in range(args.warmup):
-        oracle_sample(w, inp, min(rows, 128), pv16=pv16)
-    tot_ops, tot_s = 0.0, 0.0
+        oracle_sample(w, inp, pv16=pv16, budget=max(args.oracle_pairs // 16, 1))
+    tot_ops, tot_s, desc = 0.0, 0.0, ""
     for _ in range(args.steps):
-        ops, dt, cores, _ = oracle_sample(w, inp, rows, pv16=pv16)
+        ops, dt, cores, _, desc = oracle_sample(w, inp, pv16=pv16, budget=args.oracle_pairs)
         tot_ops += ops
         tot_s += dt
     tops = tot_ops / tot_s / 1e12
-    sample = (f"segment 0, query head 0, rows [0,{rows}) of {w.name}: prologue of that "
-              f"head plus attention, per step")
     line = {
         "impl": "reference", "metric": METRIC, "value": tops, "unit": "TOPS",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -365,7 +414,7 @@ def reference_arm(args, w: wl.Workload, rank: int, world: int):
         "dtype": "int8+fp16 (fp32 softmax)" if pv16 else "int8+e4m3 (fp32 softmax)",
         "data": "synthetic", "config": dict(config_of(w), variant=args.variant),
         "cpu_baseline": {"value": tops, "unit": "TOPS", "cores": os.cpu_count(),
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": desc + ", per step"},
         "e2e": {"value": tops, "unit": "TOPS", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -391,8 +440,8 @@ def main():
     ap.add_argument("--variant", default="fp8", choices=["fp8", "pv16"],
                     help="fp8: INT8 QK^T + FP8 PV (default); pv16: INT8 QK^T + FP16 PV")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
-    ap.add_argument("--ref-rows", type=int, default=512)
-    ap.add_argument("--cpu-rows", type=int, default=4096)
+    ap.add_argument("--oracle-pairs", type=int, default=ORACLE_PAIR_BUDGET,
+                    help="(query row, key) pairs per head of the oracle's sample, both arms")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", 0))
@@ -424,9 +473,15 @@ def main():
     tops = fig["value"]
     pro_gbs = prologue_bytes(w, 2 if pv16 else 1) / (r["pro_ms"] * 1e-3) / 1e9
     inp = wl.make_inputs(w)
-    cpu_ops, cpu_s, cores, ref_rows = oracle_sample(w, inp, args.cpu_rows, pv16=pv16)
+    cpu_ops, cpu_s, cores, ref_rows, cpu_desc = oracle_sample(w, inp, pv16=pv16,
+                                                               budget=args.oracle_pairs)
     # the bench's own output on the oracle's sample (segment 0, query head 0)
     got_rows = r["out_rows"][:ref_rows.shape[0]]
+    # the tensor ceiling measured live (same clock as the timed region):
+    # QK^T at the fp16 rate and PV at the e4m3 rate, equal flops each, or
+    # both products at the fp16 rate for the FP16-PV variant
+    r16, r8 = r["tc"][0], r["tc"][1]
+    live_peak = r16 if pv16 else 2.0 / (1.0 / r16 + 1.0 / r8)
     parity = float(np.max(np.abs(got_rows.astype(np.float64) - ref_rows)))
     line = {
         "metric": METRIC, "value": tops, "unit": "TOPS", "n_gpus": world,
@@ -445,7 +500,13 @@ def main():
                                    "16-bit rate)" if pv16 else
                                    f"4/3 x {src} bf16 burst {bf16} (QK^T at the 16-bit "
                                    "rate, PV at the FP8 rate)"),
-                     "fp8_peak": fp8_peak, "frac_of_fp8_peak": att_tflops / fp8_peak},
+                     "fp8_peak": fp8_peak, "frac_of_fp8_peak": att_tflops / fp8_peak,
+                     "live_tensor_tflops": {"fp16_k16": r16, "e4m3_k32": r8},
+                     "live_peak": live_peak, "frac_of_live_peak": att_tflops / live_peak,
+                     "live_peak_note": ("back-to-back M=128 N=128 tcgen05 MMAs on every SM, "
+                                        "measured right after the timed region (sage_debug_"
+                                        "tc_rate); the mix ceiling at the clock the kernel "
+                                        "ran at")},
         "ops_per_step": {"literal": r["ops"], "padded_d": r["ops_padded"],
                          "causal_effective": r["ops_effective"],
                          "padded_d_causal_effective": r["ops_padded_effective"]},
@@ -465,9 +526,7 @@ def main():
         "launches_per_step": r["launches_per_step"],
         "clocks": r["clocks"],
         "cpu_baseline": {"value": cpu_ops / cpu_s / 1e12, "unit": "TOPS", "cores": cores,
-                         "kind": "oracle",
-                         "sample": f"segment 0, query head 0, rows [0,{args.cpu_rows}): "
-                                   "prologue of that head plus attention"},
+                         "kind": "oracle", "sample": cpu_desc},
     }
     print(json.dumps(line), flush=True)
 

@@ -7,6 +7,7 @@ from __future__ import annotations
 import os
 import socket
 import sys
+import json
 import types
 
 import pytest
@@ -86,6 +87,31 @@ def test_single_rank_needs_no_process_group():
 
 
 def test_reference_arm_is_rank_zero_only(capsys):
-    args = types.SimpleNamespace(ref_rows=8, warmup=3, steps=1, gpus=2)
+    args = types.SimpleNamespace(oracle_pairs=4096, warmup=3, steps=1, gpus=2, variant="fp8")
     bench.reference_arm(args, wl.WORKLOADS["small_d64"], rank=1, world=2)
     assert capsys.readouterr().out == ""
+
+
+def test_oracle_sample_is_bounded_and_covers_small_workloads():
+    """Both arms time the oracle on the same bounded sample: the whole small
+    workload, one head of the 4096 x 4096 one, and >= 512 rows of the
+    longest, so that attention (not the prologue) dominates the sample."""
+    plan = bench.oracle_sample_plan
+    assert plan(wl.WORKLOADS["small_d64"]) == (2, 2, 256)
+    assert plan(wl.WORKLOADS["b2_h24_l4096_d128"]) == (1, 1, 4096)
+    heads, kv, rows = plan(wl.WORKLOADS["dit_self_l32768"])
+    assert (heads, kv) == (1, 1) and rows == 512
+    heads, kv, rows = plan(wl.WORKLOADS["gqa_causal_b4_l8192"])
+    assert heads % (32 // 8) == 0 or (heads, kv) == (1, 1)
+    assert rows * 8192 <= bench.ORACLE_PAIR_BUDGET
+
+
+def test_reference_arm_line_on_rank_zero(capsys):
+    args = types.SimpleNamespace(oracle_pairs=256 * 64, warmup=3, steps=1, gpus=1,
+                                 variant="fp8")
+    bench.reference_arm(args, wl.WORKLOADS["small_d64"], rank=0, world=1)
+    line = json.loads(capsys.readouterr().out)
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
