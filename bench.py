@@ -37,7 +37,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per attention-kernel launch on the default
 # workload, from the ncu capture of the attention kernel (None where no
 # capture of the current kernel exists).
-ATTN_NCU_DRAM_BYTES = {}
+ATTN_NCU_DRAM_BYTES = {"b2_h24_l4096_d128": 126.745088e6 + 62.736640e6}
 # the same for the FP16-PV variant's attention kernel (fp16 V and P~)
 ATTN16_NCU_DRAM_BYTES = {}
 # (query row, key) pairs of attention in the oracle's bounded sample (one

@@ -77,6 +77,10 @@ enum { SAGE_F16 = 0, SAGE_BF16 = 1 };
  * counts padded to multiples of 128 per (segment, head), padding zeroed):
  *   q16  : [q_rows][Dp] fp16 holding the int8 codes of Q (exact integers)
  *   k16  : [k_rows][Dp] fp16 holding the int8 codes of smoothed K
+ *          (sm_103a has no 8-bit integer tensor-core MMA, so QK^T runs on
+ *          the 16-bit kind, whose operands these are: each int8 code n,
+ *          -127..127, is stored as the exact fp16 value n, so q16 and k16
+ *          are the quantised Q and K codes themselves, one-to-one)
  *   v8   : [v_rows][v_cols] e4m3 codes of V, channel-major ("permuted"):
  *          row = (segment base) + kv_head*Dp + channel, column = token
  *   s_q  : [q_rows] fp32, one scale per query token

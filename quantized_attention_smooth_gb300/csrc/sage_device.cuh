@@ -54,14 +54,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
                :: "r"(smem_u32(bar)) : "memory");
 }
 
-// Arrive once `after` is computed: the input operand keeps the compiler from
-// hoisting the arrive above the register arithmetic that produces it.
-__device__ __forceinline__ void mbar_arrive_after(uint64_t* bar, float after) {
-  asm volatile("{\n\t.reg .f32 dep;\n\tmov.f32 dep, %1;\n\t"
-               "mbarrier.arrive.shared::cta.b64 _, [%0];\n}"
-               :: "r"(smem_u32(bar)), "f"(after) : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -170,28 +162,6 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
       :: "r"(smem_u32(bar)) : "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, fp16 operands, fp32 accumulator.
-__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc,
-                                           uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
-      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]^T, e4m3 operands, fp32 accumulator.
-__device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem,
-                                          uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}"
-      :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // 32 consecutive 32-bit TMEM columns of this thread's lane (warp w of a
 // warpgroup reaches lanes 32w..32w+31).  Asynchronous: call tmem_ld_wait()
 // and pass the registers through reg_fence() before using them.
@@ -209,21 +179,6 @@ __device__ __forceinline__ void tmem_ld_wait() {
 // Orders later uses of r after the preceding tmem_ld_wait().
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
   asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
-}
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr,
-                                          const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
-      :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
-      :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-      : "memory");
 }
 
 // Register budget hand-off between warpgroups of a warp-specialised kernel.
@@ -257,21 +212,12 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
-// layout written by TMA (8-row x 128-byte atoms, 1024 bytes apart).
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address
-  d |= static_cast<uint64_t>(1) << 16;                   // LBO (unused)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;           // SBO: 8 rows
-  d |= static_cast<uint64_t>(1) << 46;                   // descriptor version
-  d |= static_cast<uint64_t>(2) << 61;                   // 128-byte swizzle
-  return d;
-}
-
-// The same descriptor split in two 32-bit words: the low word carries the
-// start address (and the unused LBO), the high word is constant, so an MMA
-// loop only adds (offset >> 4) to the low word.
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzle layout written by TMA (8-row x 128-byte atoms, 1024 bytes apart:
+// start address >> 4 in bits 0-13, LBO 1 (unused), SBO 1024 >> 4, version 1
+// at bit 46, swizzle mode 2 at bit 61), split in two 32-bit words: the low
+// word carries the start address (and the unused LBO), the high word is
+// constant, so an MMA loop only adds (offset >> 4) to the low word.
 __device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr) {
   return ((saddr & 0x3FFFFu) >> 4) | (1u << 16);
 }
@@ -287,20 +233,6 @@ __device__ __forceinline__ void mma_f16_ss_lo(uint32_t d_tmem, uint32_t a_lo,
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, p;\n}"
       :: "r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate),
-         "r"(kSdescSw128Hi)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]^T from a low descriptor word, e4m3 operands.
-__device__ __forceinline__ void mma_f8_ts_lo(uint32_t d_tmem, uint32_t a_tmem,
-                                             uint32_t b_lo, uint32_t idesc,
-                                             uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .b64 bd;\n\t.reg .pred p;\n\t"
-      "mov.b64 bd, {%2, %5};\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], bd, %3, p;\n}"
-      :: "r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate),
          "r"(kSdescSw128Hi)
       : "memory");
 }
