@@ -39,7 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture of the current kernel exists).
 ATTN_NCU_DRAM_BYTES = {"b2_h24_l4096_d128": 126.745088e6 + 62.736640e6}
 # the same for the FP16-PV variant's attention kernel (fp16 V and P~)
-ATTN16_NCU_DRAM_BYTES = {}
+ATTN16_NCU_DRAM_BYTES = {"b2_h24_l4096_d128": 152.318464e6 + 65.660928e6}
 # (query row, key) pairs of attention in the oracle's bounded sample (one
 # head of the 4096 x 4096 workload; a whole small workload)
 ORACLE_PAIR_BUDGET = 4096 * 4096
