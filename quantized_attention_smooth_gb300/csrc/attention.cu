@@ -664,11 +664,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
       // product: a fused S c - m' would skip the logit's own rounding, which
       // at |x| ~ 1e4 is worth ~5e-4 in the exponent and flips e4m3 codes.
       // 448 P is taken as 2^(RN(d + log2 448)): for the d that carry weight
-      // (|d| < 24) that rounding moves P by at most 2^-20 ln 2 relative, the
-      // size of the exp2 unit's own error, and it costs one packed add where
-      // a multiply after the exp2 would lengthen the chain to the e4m3
-      // conversion.  Packed fp32 pairs; the two packed sums keep four chains
-      // (element i goes to chain i % 4).
+      // (|d| < 24) that rounding moves P by at most 2^-20 ln 2 relative, a
+      // few times the exp2 unit's own error, and it costs one packed add
+      // where a multiply after the exp2 measured 2 % slower.  Packed fp32
+      // pairs; the two packed sums keep four chains (element i goes to
+      // chain i % 4).
       const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_new, -m_new);
       const float2 one2 = make_float2(p.one, p.one);
       const float2 kL448 = make_float2(kLog2_448, kLog2_448);
