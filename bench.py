@@ -228,11 +228,17 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int):
     att_ms = statistics.mean(b.elapsed_time(c) for a, b, c in ev)
     assert sage.device_status(ws) == sage.OK, sage.last_error()
 
-    # ---- end to end: host buffers, copies inside the timed region.  Dense
-    # problems go through the library's host-buffer call, which pipelines
-    # chunk copies with compute; packed sequences copy, compute, copy back.
-    host_call = not w.varlen
-    if host_call:
+    # ---- end to end: host buffers, copies inside the timed region, through
+    # the library's host-buffer calls, which pipeline chunk copies with
+    # compute (the FP16-PV variant has no packed-sequence call: there the
+    # step copies in, computes and copies back).
+    host_call = not (w.varlen and pv16)
+    cu_host = {}
+    if host_call and w.varlen:
+        cu_host = {k: torch.from_numpy(inp[k]) for k in ("cu_q", "cu_k")}
+        ws_host = sage.alloc_workspace(sage.workspace_bytes_varlen_host(
+            w.nseg, sum(w.seqlens_q), sum(w.seqlens_k), w.Hq, w.Hkv, w.D), dev)
+    elif host_call:
         ws_host = sage.alloc_workspace(sage.workspace_bytes_host(
             w.B, w.Hq, w.Hkv, w.Lq, w.Lk, w.D), dev)
     e2e_ev = []
@@ -241,7 +247,12 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        if host_call:
+        if host_call and w.varlen:
+            sage.attn_fwd_varlen_host(host["q"], host["k"], host["v"], out_host,
+                                      cu_host["cu_q"], cu_host["cu_k"], max(w.seqlens_q),
+                                      max(w.seqlens_k), w.causal, scale, ws=ws_host,
+                                      stream=stream)
+        elif host_call:
             sage.attn_fwd_host(host["q"], host["k"], host["v"], out_host, w.layout, w.causal,
                                scale, ws=ws_host, stream=stream, pv16=pv16)
         else:
@@ -256,7 +267,8 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int):
     out_rows = np.array(wl.out_segment(w, out_host.numpy(), 0, inp.get("cu_q"))[0])
     e2e_ev = e2e_ev[-n_e2e:]
     e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
-    h2d = sum(host[k].numel() * host[k].element_size() for k in ("q", "k", "v"))
+    h2d = (sum(host[k].numel() * host[k].element_size() for k in ("q", "k", "v")) +
+           sum(t.numel() * 4 for t in cu_host.values()))
     d2h = out_host.numel() * 4
 
     # the tensor pipe's rate for the kernel's two MMA kinds, measured now, at
@@ -267,7 +279,8 @@ def run_gpu(args, w: wl.Workload, rank: int, world: int):
     r = dict(tc=tc, total_ms=total_ms, step_ms=step_ms, pro_ms=pro_ms, att_ms=att_ms,
              launches_per_step=launches_per_step, launches=launches,
              e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, ops=workload_ops(w), out_rows=out_rows,
-             e2e_api=(("sage_attn_fwd_host_pv16" if pv16 else "sage_attn_fwd_host") +
+             e2e_api=(("sage_attn_fwd_varlen_host" if w.varlen else
+                       "sage_attn_fwd_host_pv16" if pv16 else "sage_attn_fwd_host") +
                       " (chunks of kv heads, copies pipelined with compute)"
                       if host_call else "copies, then the one-call entry point, then a copy back"),
              ops_padded=workload_ops(w, Dp),

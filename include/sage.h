@@ -21,7 +21,8 @@
  *
  * Conventions shared by every call:
  *  - All tensor pointers are DEVICE pointers of the current CUDA device and
- *    are owned by the caller (the sage_attn_fwd_host* calls take host
+ *    are owned by the caller (the host-buffer calls sage_attn_fwd_host,
+ *    sage_attn_fwd_host_pv16 and sage_attn_fwd_varlen_host take host
  *    buffers instead).  The library allocates no memory, never synchronises
  *    the host and enqueues all work on the caller's stream (the host-buffer
  *    calls add copies on two streams of their own, ordered by events).
@@ -245,6 +246,33 @@ SAGE_API sage_status sage_attn_fwd_host_pv16(const void* q, const void* k, const
                                              int is_causal, float sm_scale, int dtype,
                                              int64_t chunk_kv_heads, void* ws,
                                              size_t ws_bytes, sage_stream_t stream);
+
+/* Host-buffer call for packed sequences: sage_attn_fwd_varlen on q, k, v
+ * (packed (T,H,D)) and out (packed (total_q,Hq,D) fp32) in HOST memory, with
+ * cu_seqlens_q and cu_seqlens_k (nseq + 1 int32 each) in host memory too.
+ * The operation is sage_attn_fwd_varlen's ([OV] "variable-length sequences
+ * via sageattn_varlen"); the pipeline is sage_attn_fwd_host's, with chunks
+ * of chunk_kv_heads kv heads (and their query heads) of the whole packed
+ * tensor, every sequence at once; 0 picks enough kv heads for four waves
+ * of query-tile pairs per chunk (a chunk lasts at least as long as a pair of
+ * its longest sequence).  The offsets are checked on the host (start at
+ * 0, end at the totals, every length in 0..max) and copied once into the
+ * workspace, so they may live in ordinary host memory; a bad array returns
+ * SAGE_ERR_INVALID_ARG and enqueues nothing.  The output equals one
+ * sage_attn_fwd_varlen call's.
+ *   ws: device workspace of sage_workspace_bytes_varlen_host(...) bytes (0
+ *       for invalid sizes).
+ *   nseq = 0 or total_q = 0 does nothing; total_k = 0 is refused (use
+ *   sage_attn_fwd_varlen).  The status word behaves as for
+ *   sage_attn_fwd_host. */
+SAGE_API size_t sage_workspace_bytes_varlen_host(int64_t nseq, int64_t total_q,
+                                                 int64_t total_k, int64_t Hq, int64_t Hkv,
+                                                 int64_t D, int64_t chunk_kv_heads);
+SAGE_API sage_status sage_attn_fwd_varlen_host(
+    const void* q, const void* k, const void* v, float* out, const int32_t* cu_seqlens_q,
+    const int32_t* cu_seqlens_k, int64_t nseq, int64_t total_q, int64_t total_k, int max_q,
+    int max_k, int64_t Hq, int64_t Hkv, int64_t D, int is_causal, float sm_scale, int dtype,
+    int64_t chunk_kv_heads, void* ws, size_t ws_bytes, sage_stream_t stream);
 
 /* Prologue + attention in one call on strided views (see
  * sage_quant_prologue_strided); out is dense fp32 in `layout`. */

@@ -488,6 +488,59 @@ sage_status dense_fwd(const void* q, const void* k, const void* v, float* out, i
   return launch_attn(&qt, out, layout, is_causal, sm_scale, st);
 }
 
+// The varlen prologue; keep_status leaves the workspace's status word as it
+// is (the host-buffer pipeline's later chunks).
+sage_status varlen_prologue(const void* q, const void* k, const void* v, int dtype,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                            int64_t nseq, int64_t total_q, int64_t total_k, int max_q,
+                            int max_k, int64_t Hq, int64_t Hkv, int64_t D, void* ws,
+                            size_t ws_bytes, sage_quantized* qt, sage_stream_t stream,
+                            bool keep_status) {
+  if (qt == nullptr) return fail(SAGE_ERR_INVALID_ARG, "qt must not be null");
+  sage_status s = SAGE_OK;
+  if (!check_dims(Hq, Hkv, D, &s)) return s;
+  if ((s = check_common(q, k, v, dtype)) != SAGE_OK) return s;
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr || !aligned(cu_seqlens_q, 4) ||
+      !aligned(cu_seqlens_k, 4))
+    return fail(SAGE_ERR_INVALID_ARG, "cu_seqlens_q/k must be aligned device pointers");
+  if (nseq < 1 || total_q < 1 || total_k < 1 || max_q < 1 || max_k < 1)
+    return fail(SAGE_ERR_INVALID_ARG,
+                "varlen prologue needs nseq, totals and maxima > 0 (nseq=%lld)",
+                (long long)nseq);
+  if (nseq > 65535) return fail(SAGE_ERR_UNSUPPORTED, "nseq=%lld > 65535", (long long)nseq);
+  return run_prologue(varlen_geo(nseq, total_q, total_k, max_q, max_k, Hq, Hkv, D, dtype,
+                                 cu_seqlens_q, cu_seqlens_k),
+                      q, k, v, ws, ws_bytes, qt, reinterpret_cast<cudaStream_t>(stream),
+                      /*v16=*/false, keep_status);
+}
+
+// Packed varlen prologue and attention in one call; keep_status as above.
+sage_status varlen_fwd(const void* q, const void* k, const void* v, float* out,
+                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int64_t nseq,
+                       int64_t total_q, int64_t total_k, int max_q, int max_k, int64_t Hq,
+                       int64_t Hkv, int64_t D, int is_causal, float sm_scale, int dtype,
+                       void* ws, size_t ws_bytes, sage_stream_t stream, bool keep_status) {
+  sage_status s = SAGE_OK;
+  if (!check_dims(Hq, Hkv, D, &s)) return s;
+  if (nseq < 0 || total_q < 0 || total_k < 0)
+    return fail(SAGE_ERR_INVALID_ARG, "negative varlen size");
+  if (nseq == 0 || total_q == 0) return ok();
+  if (out == nullptr || !aligned(out, 4))
+    return fail(SAGE_ERR_INVALID_ARG, "out must be a 4-byte aligned device pointer");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (total_k == 0) {
+    if ((s = check_common(q, q, q, dtype)) != SAGE_OK) return s;
+    if ((s = check_device()) != SAGE_OK) return s;
+    cudaError_t e = cudaMemsetAsync(out, 0, total_q * Hq * D * 4, st);
+    return e == cudaSuccess ? ok() : cuda_fail(e, "cudaMemsetAsync");
+  }
+  sage_quantized qt;
+  s = varlen_prologue(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, nseq, total_q, total_k,
+                      max_q, max_k, Hq, Hkv, D, ws, ws_bytes, &qt, stream, keep_status);
+  if (s != SAGE_OK) return s;
+  return launch_attn(&qt, out, SAGE_NHD, is_causal, sm_scale, st);
+}
+
 }  // namespace
 
 
@@ -498,13 +551,30 @@ sage_status dense_fwd(const void* q, const void* k, const void* v, float* out, i
 // and chunk i-1's output is copied back on a third.  Two staging slots
 // alternate; events order every reuse.  Attention never mixes heads or
 // batches, so the result is the same as one sage_attn_fwd call.
+// sage_attn_fwd_varlen_host does the same for packed sequences: its chunks
+// are kv-head groups of the whole packed tensor (every sequence), and the
+// cumulative offsets are copied once into the workspace.
 namespace {
+
+// A host-buffer problem: dense (B entries of Lq query and Lk key rows) or
+// packed varlen (one entry of total_q and total_k rows, nseq sequences).
+struct HostShape {
+  int64_t B, Hq, Hkv, Lq, Lk, D;
+  bool varlen;
+  int64_t nseq;              // varlen only
+  int max_q, max_k;          // varlen only
+};
+
+HostShape dense_shape(int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk, int64_t D) {
+  return HostShape{B, Hq, Hkv, Lq, Lk, D, false, 0, 0, 0};
+}
 
 struct HostPlan {
   int64_t chunk_kv;          // kv heads per chunk
   int64_t group;             // query heads per kv head
   size_t ws_bytes;           // prologue workspace of one chunk (offset 0)
   size_t q_bytes, kv_bytes, out_bytes;   // one chunk's q, k (= v), out
+  size_t cu;                 // varlen: offset of the device copy of cu_seqlens_q, then _k
   size_t slot[2];            // offsets of the two staging slots
   size_t total;
 };
@@ -523,26 +593,57 @@ int sm_count_of_current_device() {
 
 // chunk_kv <= 0 picks enough kv heads for one wave of query-tile pairs per
 // chunk (one per SM), so that each chunk's attention still fills the GPU.
-HostPlan host_plan(int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk, int64_t D,
-                   int64_t chunk_kv) {
+// Packed sequences take four waves: a chunk's attention lasts at least as
+// long as a pair of its longest sequence, so a chunk of few heads leaves
+// most SMs idle behind that pair (measured on 8 sequences of 2k-16k tokens,
+// 16 heads: 4 or 2 kv heads per chunk 20-54 % faster than copying in,
+// computing and copying back; 1 head 11 % and 41 %).
+HostPlan host_plan(const HostShape& h, int64_t chunk_kv) {
   HostPlan P{};
-  P.group = Hq / Hkv;
+  P.group = h.Hq / h.Hkv;
   if (chunk_kv <= 0) {
-    const int64_t pairs = P.group * (((Lq + 127) / 128 + 1) / 2);
+    // query tiles per query head (packed sequences: at most one ragged tile each)
+    const int64_t qtiles = (h.Lq + 127) / 128 + (h.varlen ? h.nseq : 0);
+    const int64_t pairs = P.group * ((qtiles + 1) / 2);
     const int64_t sms = sm_count_of_current_device() > 0 ? sm_count_of_current_device() : 152;
-    chunk_kv = pairs > 0 ? (sms + pairs - 1) / pairs : Hkv;
+    const int64_t want = (h.varlen ? 4 : 1) * sms;
+    chunk_kv = pairs > 0 ? (want + pairs - 1) / pairs : h.Hkv;
   }
-  P.chunk_kv = chunk_kv < 1 ? 1 : (chunk_kv > Hkv ? Hkv : chunk_kv);
+  P.chunk_kv = chunk_kv < 1 ? 1 : (chunk_kv > h.Hkv ? h.Hkv : chunk_kv);
   const int64_t hq = P.chunk_kv * P.group;
-  P.q_bytes = static_cast<size_t>(hq * Lq * D * 2);
-  P.kv_bytes = static_cast<size_t>(P.chunk_kv * Lk * D * 2);
-  P.out_bytes = static_cast<size_t>(hq * Lq * D * 4);
-  P.ws_bytes = align256(sage_workspace_bytes(1, hq, P.chunk_kv, Lq, Lk, D));
+  P.q_bytes = static_cast<size_t>(hq * h.Lq * h.D * 2);
+  P.kv_bytes = static_cast<size_t>(P.chunk_kv * h.Lk * h.D * 2);
+  P.out_bytes = static_cast<size_t>(hq * h.Lq * h.D * 4);
+  P.ws_bytes = align256(
+      h.varlen ? sage_workspace_bytes_varlen(h.nseq, h.Lq, h.Lk, hq, P.chunk_kv, h.D)
+               : sage_workspace_bytes(1, hq, P.chunk_kv, h.Lq, h.Lk, h.D));
+  P.cu = P.ws_bytes;
+  const size_t cu_bytes = h.varlen ? 2 * align256(static_cast<size_t>(h.nseq + 1) * 4) : 0;
   const size_t per_slot = align256(P.q_bytes) + 2 * align256(P.kv_bytes) + align256(P.out_bytes);
-  P.slot[0] = P.ws_bytes;
-  P.slot[1] = P.ws_bytes + per_slot;
-  P.total = P.ws_bytes + 2 * per_slot;
+  P.slot[0] = P.ws_bytes + cu_bytes;
+  P.slot[1] = P.slot[0] + per_slot;
+  P.total = P.slot[1] + per_slot;
   return P;
+}
+
+// Host-side check of a host cu_seqlens array: starts at 0, ends at total,
+// and every length lies in 0..maxlen.
+bool check_cu_host(const int32_t* cu, int64_t nseq, int64_t total, int maxlen,
+                   const char* name, sage_status* st) {
+  if (cu[0] != 0 || cu[nseq] != total) {
+    *st = fail(SAGE_ERR_INVALID_ARG, "%s must start at 0 and end at %lld", name,
+               (long long)total);
+    return false;
+  }
+  for (int64_t i = 0; i < nseq; ++i) {
+    const int64_t len = static_cast<int64_t>(cu[i + 1]) - cu[i];
+    if (len < 0 || len > maxlen) {
+      *st = fail(SAGE_ERR_INVALID_ARG, "%s: sequence %lld has length %lld outside 0..%d", name,
+                 (long long)i, (long long)len, maxlen);
+      return false;
+    }
+  }
+  return true;
 }
 
 // Copy streams and events of the pipeline, created once per device and kept
@@ -608,27 +709,17 @@ cudaError_t copy_chunk(void* dst, const void* src, bool to_device, bool hnd, int
 
 namespace {
 
-// The host-buffer pipeline (see sage_attn_fwd_host); v16 runs the FP16-PV kernels.
-sage_status host_fwd(const void* q, const void* k, const void* v, float* out, int64_t B,
-                     int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk, int64_t D, int layout,
-                     int is_causal, float sm_scale, int dtype, int64_t chunk_kv_heads,
-                     void* ws, size_t ws_bytes, sage_stream_t stream, bool v16) {
+// The host-buffer pipeline (see sage_attn_fwd_host and
+// sage_attn_fwd_varlen_host); v16 runs the FP16-PV kernels (dense only).
+// Arguments are checked by the callers.
+sage_status host_pipeline(const void* q, const void* k, const void* v, float* out,
+                          const HostShape& h, const int32_t* cu_q, const int32_t* cu_k,
+                          int layout, int is_causal, float sm_scale, int dtype,
+                          int64_t chunk_kv_heads, void* ws, size_t ws_bytes,
+                          sage_stream_t stream, bool v16) {
   sage_status s = SAGE_OK;
-  if (layout != SAGE_HND && layout != SAGE_NHD)
-    return fail(SAGE_ERR_INVALID_ARG, "layout %d is neither SAGE_HND nor SAGE_NHD", layout);
-  if (B < 0 || Lq < 0 || Lk < 0)
-    return fail(SAGE_ERR_INVALID_ARG, "negative size (B=%lld Lq=%lld Lk=%lld)",
-                (long long)B, (long long)Lq, (long long)Lk);
-  if (!check_dims(Hq, Hkv, D, &s)) return s;
-  if (dtype != SAGE_F16 && dtype != SAGE_BF16)
-    return fail(SAGE_ERR_INVALID_ARG, "dtype %d is neither SAGE_F16 nor SAGE_BF16", dtype);
-  if (B == 0 || Lq == 0) return ok();                 // nothing to compute
-  if (Lk == 0)
-    return fail(SAGE_ERR_INVALID_ARG, "the host-buffer call needs Lk > 0");
-  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr)
-    return fail(SAGE_ERR_INVALID_ARG, "null host buffer");
   if ((s = check_device()) != SAGE_OK) return s;
-  const HostPlan P = host_plan(Hq, Hkv, Lq, Lk, D, chunk_kv_heads);
+  const HostPlan P = host_plan(h, chunk_kv_heads);
   if (ws == nullptr || !aligned(ws, 256))
     return fail(SAGE_ERR_WORKSPACE, "workspace must be a 256-byte aligned device pointer");
   if (ws_bytes < P.total)
@@ -649,10 +740,20 @@ sage_status host_fwd(const void* q, const void* k, const void* v, float* out, in
   e = cudaEventRecord(rt.start, st);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(rt.in, rt.start, 0);
   if (e != cudaSuccess) return cuda_fail(e, "pipeline start");
+  int32_t* dcu_q = reinterpret_cast<int32_t*>(base + P.cu);
+  int32_t* dcu_k = reinterpret_cast<int32_t*>(
+      base + P.cu + align256(static_cast<size_t>(h.nseq + 1) * 4));
+  if (h.varlen) {
+    // the offsets, once, ahead of the first chunk's inputs on the copy stream
+    const size_t n = static_cast<size_t>(h.nseq + 1) * 4;
+    e = cudaMemcpyAsync(dcu_q, cu_q, n, cudaMemcpyHostToDevice, rt.in);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dcu_k, cu_k, n, cudaMemcpyHostToDevice, rt.in);
+    if (e != cudaSuccess) return cuda_fail(e, "pipeline offsets");
+  }
   int64_t i = 0;
-  for (int64_t b = 0; b < B; ++b) {
-    for (int64_t g0 = 0; g0 < Hkv; g0 += P.chunk_kv, ++i) {
-      const int64_t gn = Hkv - g0 < P.chunk_kv ? Hkv - g0 : P.chunk_kv;
+  for (int64_t b = 0; b < h.B; ++b) {
+    for (int64_t g0 = 0; g0 < h.Hkv; g0 += P.chunk_kv, ++i) {
+      const int64_t gn = h.Hkv - g0 < P.chunk_kv ? h.Hkv - g0 : P.chunk_kv;
       const int64_t h0 = g0 * P.group, hn = gn * P.group;
       const int sl = static_cast<int>(i & 1);
       uint8_t* dq = base + P.slot[sl];
@@ -661,9 +762,12 @@ sage_status host_fwd(const void* q, const void* k, const void* v, float* out, in
       float* dout = reinterpret_cast<float*>(dv + align256(P.kv_bytes));
       // inputs: after the slot's previous chunk has been computed
       e = cudaStreamWaitEvent(rt.in, rt.computed[sl], 0);
-      if (e == cudaSuccess) e = copy_chunk(dq, q, true, hnd, b, h0, hn, Hq, Lq, D, 2, rt.in);
-      if (e == cudaSuccess) e = copy_chunk(dk, k, true, hnd, b, g0, gn, Hkv, Lk, D, 2, rt.in);
-      if (e == cudaSuccess) e = copy_chunk(dv, v, true, hnd, b, g0, gn, Hkv, Lk, D, 2, rt.in);
+      if (e == cudaSuccess)
+        e = copy_chunk(dq, q, true, hnd, b, h0, hn, h.Hq, h.Lq, h.D, 2, rt.in);
+      if (e == cudaSuccess)
+        e = copy_chunk(dk, k, true, hnd, b, g0, gn, h.Hkv, h.Lk, h.D, 2, rt.in);
+      if (e == cudaSuccess)
+        e = copy_chunk(dv, v, true, hnd, b, g0, gn, h.Hkv, h.Lk, h.D, 2, rt.in);
       if (e == cudaSuccess) e = cudaEventRecord(rt.loaded[sl], rt.in);
       // compute: after the inputs landed and the slot's previous output left
       if (e == cudaSuccess) e = cudaStreamWaitEvent(st, rt.loaded[sl], 0);
@@ -671,13 +775,19 @@ sage_status host_fwd(const void* q, const void* k, const void* v, float* out, in
       if (e != cudaSuccess) return cuda_fail(e, "pipeline copy-in");
       // the first chunk clears the device status word, the others keep it,
       // so a bounded wait that ran out in any chunk stays visible
-      s = dense_fwd(dq, dk, dv, dout, 1, hn, gn, Lq, Lk, D, layout, is_causal, sm_scale,
-                    dtype, base, P.ws_bytes, stream, v16, /*keep_status=*/i > 0);
+      if (h.varlen)
+        s = varlen_fwd(dq, dk, dv, dout, dcu_q, dcu_k, h.nseq, h.Lq, h.Lk, h.max_q, h.max_k,
+                       hn, gn, h.D, is_causal, sm_scale, dtype, base, P.ws_bytes, stream,
+                       /*keep_status=*/i > 0);
+      else
+        s = dense_fwd(dq, dk, dv, dout, 1, hn, gn, h.Lq, h.Lk, h.D, layout, is_causal,
+                      sm_scale, dtype, base, P.ws_bytes, stream, v16, /*keep_status=*/i > 0);
       if (s != SAGE_OK) return s;
       e = cudaEventRecord(rt.computed[sl], st);
       // output: after the chunk was computed
       if (e == cudaSuccess) e = cudaStreamWaitEvent(rt.out, rt.computed[sl], 0);
-      if (e == cudaSuccess) e = copy_chunk(out, dout, false, hnd, b, h0, hn, Hq, Lq, D, 4, rt.out);
+      if (e == cudaSuccess)
+        e = copy_chunk(out, dout, false, hnd, b, h0, hn, h.Hq, h.Lq, h.D, 4, rt.out);
       if (e == cudaSuccess) e = cudaEventRecord(rt.stored[sl], rt.out);
       if (e != cudaSuccess) return cuda_fail(e, "pipeline copy-out");
     }
@@ -686,6 +796,60 @@ sage_status host_fwd(const void* q, const void* k, const void* v, float* out, in
   e = cudaStreamWaitEvent(st, rt.stored[0], 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(st, rt.stored[1], 0);
   return e == cudaSuccess ? ok() : cuda_fail(e, "pipeline end");
+}
+
+// Dense host-buffer call: argument checks, then the pipeline.
+sage_status host_fwd(const void* q, const void* k, const void* v, float* out, int64_t B,
+                     int64_t Hq, int64_t Hkv, int64_t Lq, int64_t Lk, int64_t D, int layout,
+                     int is_causal, float sm_scale, int dtype, int64_t chunk_kv_heads,
+                     void* ws, size_t ws_bytes, sage_stream_t stream, bool v16) {
+  sage_status s = SAGE_OK;
+  if (layout != SAGE_HND && layout != SAGE_NHD)
+    return fail(SAGE_ERR_INVALID_ARG, "layout %d is neither SAGE_HND nor SAGE_NHD", layout);
+  if (B < 0 || Lq < 0 || Lk < 0)
+    return fail(SAGE_ERR_INVALID_ARG, "negative size (B=%lld Lq=%lld Lk=%lld)",
+                (long long)B, (long long)Lq, (long long)Lk);
+  if (!check_dims(Hq, Hkv, D, &s)) return s;
+  if (dtype != SAGE_F16 && dtype != SAGE_BF16)
+    return fail(SAGE_ERR_INVALID_ARG, "dtype %d is neither SAGE_F16 nor SAGE_BF16", dtype);
+  if (B == 0 || Lq == 0) return ok();                 // nothing to compute
+  if (Lk == 0)
+    return fail(SAGE_ERR_INVALID_ARG, "the host-buffer call needs Lk > 0");
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr)
+    return fail(SAGE_ERR_INVALID_ARG, "null host buffer");
+  return host_pipeline(q, k, v, out, dense_shape(B, Hq, Hkv, Lq, Lk, D), nullptr, nullptr,
+                       layout, is_causal, sm_scale, dtype, chunk_kv_heads, ws, ws_bytes,
+                       stream, v16);
+}
+
+// Packed varlen host-buffer call: argument and offset checks, then the pipeline.
+sage_status varlen_host_fwd(const void* q, const void* k, const void* v, float* out,
+                            const int32_t* cu_q, const int32_t* cu_k, int64_t nseq,
+                            int64_t total_q, int64_t total_k, int max_q, int max_k,
+                            int64_t Hq, int64_t Hkv, int64_t D, int is_causal, float sm_scale,
+                            int dtype, int64_t chunk_kv_heads, void* ws, size_t ws_bytes,
+                            sage_stream_t stream) {
+  sage_status s = SAGE_OK;
+  if (!check_dims(Hq, Hkv, D, &s)) return s;
+  if (dtype != SAGE_F16 && dtype != SAGE_BF16)
+    return fail(SAGE_ERR_INVALID_ARG, "dtype %d is neither SAGE_F16 nor SAGE_BF16", dtype);
+  if (nseq < 0 || total_q < 0 || total_k < 0)
+    return fail(SAGE_ERR_INVALID_ARG, "negative varlen size");
+  if (nseq == 0 || total_q == 0) return ok();         // nothing to compute
+  if (total_k == 0)
+    return fail(SAGE_ERR_INVALID_ARG, "the host-buffer call needs total_k > 0");
+  if (nseq > 65535) return fail(SAGE_ERR_UNSUPPORTED, "nseq=%lld > 65535", (long long)nseq);
+  if (max_q < 1 || max_k < 1)
+    return fail(SAGE_ERR_INVALID_ARG, "max_q and max_k must be positive");
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || cu_q == nullptr ||
+      cu_k == nullptr)
+    return fail(SAGE_ERR_INVALID_ARG, "null host buffer");
+  if (!check_cu_host(cu_q, nseq, total_q, max_q, "cu_seqlens_q", &s) ||
+      !check_cu_host(cu_k, nseq, total_k, max_k, "cu_seqlens_k", &s))
+    return s;
+  const HostShape h{1, Hq, Hkv, total_q, total_k, D, true, nseq, max_q, max_k};
+  return host_pipeline(q, k, v, out, h, cu_q, cu_k, SAGE_NHD, is_causal, sm_scale, dtype,
+                       chunk_kv_heads, ws, ws_bytes, stream, false);
 }
 
 }  // namespace
@@ -733,21 +897,8 @@ sage_status sage_quant_prologue_varlen(const void* q, const void* k, const void*
                                        int max_k, int64_t Hq, int64_t Hkv, int64_t D,
                                        void* ws, size_t ws_bytes, sage_quantized* qt,
                                        sage_stream_t stream) {
-  if (qt == nullptr) return fail(SAGE_ERR_INVALID_ARG, "qt must not be null");
-  sage_status s = SAGE_OK;
-  if (!check_dims(Hq, Hkv, D, &s)) return s;
-  if ((s = check_common(q, k, v, dtype)) != SAGE_OK) return s;
-  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr || !aligned(cu_seqlens_q, 4) ||
-      !aligned(cu_seqlens_k, 4))
-    return fail(SAGE_ERR_INVALID_ARG, "cu_seqlens_q/k must be aligned device pointers");
-  if (nseq < 1 || total_q < 1 || total_k < 1 || max_q < 1 || max_k < 1)
-    return fail(SAGE_ERR_INVALID_ARG,
-                "varlen prologue needs nseq, totals and maxima > 0 (nseq=%lld)",
-                (long long)nseq);
-  if (nseq > 65535) return fail(SAGE_ERR_UNSUPPORTED, "nseq=%lld > 65535", (long long)nseq);
-  return run_prologue(varlen_geo(nseq, total_q, total_k, max_q, max_k, Hq, Hkv, D, dtype,
-                                 cu_seqlens_q, cu_seqlens_k),
-                      q, k, v, ws, ws_bytes, qt, reinterpret_cast<cudaStream_t>(stream));
+  return varlen_prologue(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, nseq, total_q, total_k,
+                         max_q, max_k, Hq, Hkv, D, ws, ws_bytes, qt, stream, false);
 }
 
 sage_status sage_quant_prologue_strided(const void* q, const void* k, const void* v,
@@ -842,26 +993,8 @@ sage_status sage_attn_fwd_varlen(const void* q, const void* k, const void* v, fl
                                  int max_k, int64_t Hq, int64_t Hkv, int64_t D,
                                  int is_causal, float sm_scale, int dtype, void* ws,
                                  size_t ws_bytes, sage_stream_t stream) {
-  sage_status s = SAGE_OK;
-  if (!check_dims(Hq, Hkv, D, &s)) return s;
-  if (nseq < 0 || total_q < 0 || total_k < 0)
-    return fail(SAGE_ERR_INVALID_ARG, "negative varlen size");
-  if (nseq == 0 || total_q == 0) return ok();
-  if (out == nullptr || !aligned(out, 4))
-    return fail(SAGE_ERR_INVALID_ARG, "out must be a 4-byte aligned device pointer");
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (total_k == 0) {
-    if ((s = check_common(q, q, q, dtype)) != SAGE_OK) return s;
-    if ((s = check_device()) != SAGE_OK) return s;
-    cudaError_t e = cudaMemsetAsync(out, 0, total_q * Hq * D * 4, st);
-    return e == cudaSuccess ? ok() : cuda_fail(e, "cudaMemsetAsync");
-  }
-  sage_quantized qt;
-  s = sage_quant_prologue_varlen(q, k, v, dtype, cu_seqlens_q, cu_seqlens_k, nseq, total_q,
-                                 total_k, max_q, max_k, Hq, Hkv, D, ws, ws_bytes, &qt,
-                                 stream);
-  if (s != SAGE_OK) return s;
-  return launch_attn(&qt, out, SAGE_NHD, is_causal, sm_scale, st);
+  return varlen_fwd(q, k, v, out, cu_seqlens_q, cu_seqlens_k, nseq, total_q, total_k, max_q,
+                    max_k, Hq, Hkv, D, is_causal, sm_scale, dtype, ws, ws_bytes, stream, false);
 }
 
 sage_status sage_debug_qk_int32(const sage_quantized* qt, int64_t seg, int64_t hq,
@@ -1019,7 +1152,29 @@ size_t sage_workspace_bytes_host(int64_t B, int64_t Hq, int64_t Hkv, int64_t Lq,
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lk <= 0 || D < 1 || D > 128 ||
       Hq % Hkv != 0)
     return 0;
-  return host_plan(Hq, Hkv, Lq, Lk, D, chunk_kv_heads).total;
+  return host_plan(dense_shape(B, Hq, Hkv, Lq, Lk, D), chunk_kv_heads).total;
+}
+
+size_t sage_workspace_bytes_varlen_host(int64_t nseq, int64_t total_q, int64_t total_k,
+                                        int64_t Hq, int64_t Hkv, int64_t D,
+                                        int64_t chunk_kv_heads) {
+  if (nseq <= 0 || nseq > 65535 || total_q <= 0 || total_k <= 0 || D < 1 || D > 128 ||
+      Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0)
+    return 0;
+  const HostShape h{1, Hq, Hkv, total_q, total_k, D, true, nseq, 0, 0};
+  return host_plan(h, chunk_kv_heads).total;
+}
+
+sage_status sage_attn_fwd_varlen_host(const void* q, const void* k, const void* v, float* out,
+                                      const int32_t* cu_seqlens_q,
+                                      const int32_t* cu_seqlens_k, int64_t nseq,
+                                      int64_t total_q, int64_t total_k, int max_q, int max_k,
+                                      int64_t Hq, int64_t Hkv, int64_t D, int is_causal,
+                                      float sm_scale, int dtype, int64_t chunk_kv_heads,
+                                      void* ws, size_t ws_bytes, sage_stream_t stream) {
+  return varlen_host_fwd(q, k, v, out, cu_seqlens_q, cu_seqlens_k, nseq, total_q, total_k,
+                         max_q, max_k, Hq, Hkv, D, is_causal, sm_scale, dtype, chunk_kv_heads,
+                         ws, ws_bytes, stream);
 }
 
 sage_status sage_attn_fwd_host(const void* q, const void* k, const void* v, float* out,

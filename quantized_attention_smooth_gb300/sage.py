@@ -28,7 +28,7 @@ EXPORTS = (
     "sage_attn_fwd_strided", "sage_quant_prologue_pv16", "sage_attn_fwd_pv16",
     "sage_workspace_bytes_host", "sage_attn_fwd_host", "sage_attn_fwd_host_pv16",
     "sage_debug_pv_accum", "sage_debug_set_fault_launches", "sage_kv_stats_noalloc_status",
-    "sage_debug_tc_rate",
+    "sage_debug_tc_rate", "sage_workspace_bytes_varlen_host", "sage_attn_fwd_varlen_host",
 )
 
 
@@ -74,6 +74,9 @@ def _load():
         "sage_attn_fwd_host_pv16": ([P, P, P, P, I64, I64, I64, I64, I64, I64, I, I, F, I, I64, P,
                                      SZ, P], I),
         "sage_workspace_bytes_varlen": ([I64] * 6, SZ),
+        "sage_workspace_bytes_varlen_host": ([I64] * 7, SZ),
+        "sage_attn_fwd_varlen_host": ([P, P, P, P, P, P, I64, I64, I64, I, I, I64, I64, I64, I,
+                                       F, I, I64, P, SZ, P], I),
         "sage_quant_prologue": ([P, P, P, I, I, I64, I64, I64, I64, I64, I64, P, SZ, QP, P], I),
         "sage_quant_prologue_varlen": ([P, P, P, I, P, P, I64, I64, I64, I, I, I64, I64, I64,
                                         P, SZ, QP, P], I),
@@ -476,6 +479,49 @@ def kv_stats_noalloc(k, v, layout, k_mean, s_v, stream=None):
                                     _ptr(k_mean), _ptr(s_v), _stream(stream))
     _check(rc, "sage_kv_stats_noalloc")
     return k_mean, s_v
+
+
+def workspace_bytes_varlen_host(nseq, total_q, total_k, Hq, Hkv, D, chunk_kv_heads=0) -> int:
+    return int(_lib.sage_workspace_bytes_varlen_host(nseq, total_q, total_k, Hq, Hkv, D,
+                                                     int(chunk_kv_heads)))
+
+
+def attn_fwd_varlen_host(q, k, v, out, cu_q, cu_k, max_q, max_k, is_causal=False,
+                         sm_scale=None, chunk_kv_heads=0, ws=None, stream=None):
+    """Packed-sequence attention on host tensors (q, k, v packed (T, H, D),
+    page-locked for overlap; out float32 of q's shape; cu_q and cu_k int32
+    host tensors of nseq + 1 offsets): the library copies chunks of kv heads
+    in, computes them and copies the output back, pipelined.  `stream`
+    completes when `out` is filled."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out), ("cu_q", cu_q),
+                    ("cu_k", cu_k)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"attn_fwd_varlen_host: {name} must be a contiguous host tensor")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("attn_fwd_varlen_host: q, k and v must share one dtype")
+    if cu_q.dtype != torch.int32 or cu_k.dtype != torch.int32:
+        raise TypeError("attn_fwd_varlen_host: cu_q and cu_k must be int32")
+    if q.dim() != 3 or k.dim() != 3 or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("attn_fwd_varlen_host: q, k, v must be packed (T, H, D), v like k")
+    if out.dtype != torch.float32 or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("attn_fwd_varlen_host: out must be float32 with q's shape")
+    if cu_q.numel() != cu_k.numel() or cu_q.numel() < 2:
+        raise ValueError("attn_fwd_varlen_host: cu_q and cu_k need the same nseq + 1 >= 2 entries")
+    total_q, Hq, D = q.shape
+    total_k, Hkv, _ = k.shape
+    nseq = cu_q.numel() - 1
+    if ws is None:
+        ws = alloc_workspace(workspace_bytes_varlen_host(nseq, total_q, total_k, Hq, Hkv, D,
+                                                         chunk_kv_heads))
+    rc = _lib.sage_attn_fwd_varlen_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(cu_q),
+                                        _ptr(cu_k), nseq, total_q, total_k, int(max_q),
+                                        int(max_k), Hq, Hkv, D, int(bool(is_causal)),
+                                        float(sm_scale or 0.0), _dtype_code(q),
+                                        int(chunk_kv_heads), _ptr(ws), ws.numel(),
+                                        _stream(stream))
+    _check(rc, "sage_attn_fwd_varlen_host")
+    return out
 
 
 def debug_tc_rate(kind: int, n_mma: int, status, stream=None):

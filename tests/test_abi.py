@@ -208,6 +208,80 @@ def test_host_buffer_call_automatic_chunk():
             L.sage_workspace_bytes_host(1, 8, 2, 128, 128, 64, 2))
 
 
+def test_varlen_host_call_sizes_and_refusals():
+    """sage_workspace_bytes_varlen_host: the chunk's varlen prologue
+    workspace, the device copy of both offset arrays and two staging slots;
+    sage_attn_fwd_varlen_host checks its host offset arrays (start 0, end at
+    the total, lengths within the maxima) before touching a device."""
+    import ctypes
+    L = sage.lib
+    one = L.sage_workspace_bytes_varlen_host(3, 700, 900, 4, 2, 64, 1)
+    two = L.sage_workspace_bytes_varlen_host(3, 700, 900, 4, 2, 64, 2)
+    chunk1 = 2 * 700 * 64 * 2 + 2 * (900 * 64 * 2) + 2 * 700 * 64 * 4     # q, k, v, out
+    assert one >= 2 * chunk1 + L.sage_workspace_bytes_varlen(3, 700, 900, 2, 1, 64)
+    assert two > one
+    assert L.sage_workspace_bytes_varlen_host(0, 700, 900, 4, 2, 64, 0) == 0     # nseq
+    assert L.sage_workspace_bytes_varlen_host(3, 700, 900, 3, 2, 64, 0) == 0     # Hq % Hkv
+    assert L.sage_workspace_bytes_varlen_host(3, 700, 900, 4, 2, 129, 0) == 0    # D > 128
+
+    def cu(*xs):
+        return (ctypes.c_int32 * len(xs))(*xs)
+
+    def call(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, cu_q=cu(0, 300, 700), cu_k=cu(0, 400, 900),
+                 nseq=2, total_q=700, total_k=900, max_q=400, max_k=500, Hq=2, Hkv=2, D=64,
+                 causal=0, scale=0.0, dtype=0, chunk=0, ws=FAKE, ws_bytes=1 << 30)
+        a.update(kw)
+        return L.sage_attn_fwd_varlen_host(
+            a["q"], a["k"], a["v"], a["out"], ctypes.cast(a["cu_q"], ctypes.c_void_p),
+            ctypes.cast(a["cu_k"], ctypes.c_void_p), a["nseq"], a["total_q"], a["total_k"],
+            a["max_q"], a["max_k"], a["Hq"], a["Hkv"], a["D"], a["causal"], a["scale"],
+            a["dtype"], a["chunk"], a["ws"], a["ws_bytes"], None)
+    assert call(nseq=0) == sage.OK
+    assert call(total_q=0) == sage.OK
+    assert call(total_k=0) == sage.ERR_INVALID_ARG
+    assert call(q=None) == sage.ERR_INVALID_ARG
+    assert call(dtype=7) == sage.ERR_INVALID_ARG
+    assert call(Hq=3) == sage.ERR_INVALID_ARG
+    assert call(cu_q=cu(1, 300, 700)) == sage.ERR_INVALID_ARG        # does not start at 0
+    assert "cu_seqlens_q" in sage.last_error()
+    assert call(cu_k=cu(0, 400, 901)) == sage.ERR_INVALID_ARG        # does not end at total_k
+    assert "cu_seqlens_k" in sage.last_error()
+    assert call(cu_q=cu(0, 301, 300)) == sage.ERR_INVALID_ARG        # negative length
+    assert call(max_k=450) == sage.ERR_INVALID_ARG                   # a length above max_k
+    assert "length 500" in sage.last_error()
+    assert call(nseq=70000) == sage.ERR_UNSUPPORTED
+
+
+def test_varlen_host_call_automatic_chunk():
+    """Packed sequences: the automatic chunk holds four waves of query-tile
+    pairs (152 SMs assumed without a device).  8 sequences, 73514 tokens:
+    at most 575 + 8 query tiles per head, 292 pairs, so 3 kv heads."""
+    import torch
+    L = sage.lib
+    if torch.cuda.is_available():
+        pytest.skip("the device's own SM count decides on a GPU")
+    auto = L.sage_workspace_bytes_varlen_host(8, 73514, 73514, 16, 16, 40, 0)
+    assert auto == L.sage_workspace_bytes_varlen_host(8, 73514, 73514, 16, 16, 40, 3)
+    assert auto != L.sage_workspace_bytes_varlen_host(8, 73514, 73514, 16, 16, 40, 2)
+
+
+def test_varlen_host_binding_refuses_device_or_misshaped_tensors():
+    import torch
+    q = torch.zeros(10, 2, 64, dtype=torch.float16)
+    out = torch.zeros(10, 2, 64, dtype=torch.float32)
+    cu = torch.tensor([0, 10], dtype=torch.int32)
+    with pytest.raises(TypeError, match="int32"):
+        sage.attn_fwd_varlen_host(q, q, q, out, cu.long(), cu, 10, 10)
+    with pytest.raises(ValueError, match="float32"):
+        sage.attn_fwd_varlen_host(q, q, q, out.half(), cu, cu, 10, 10)
+    with pytest.raises(ValueError, match="same nseq"):
+        sage.attn_fwd_varlen_host(q, q, q, out, cu, torch.tensor([0, 5, 10], dtype=torch.int32),
+                                  10, 10)
+    with pytest.raises(ValueError, match="packed"):
+        sage.attn_fwd_varlen_host(q, q[None], q[None], out, cu, cu, 10, 10)
+
+
 @pytest.mark.parametrize("case,needle", [
     ("v_shape", "one shape"),
     ("mean_dtype", "contiguous float32"),

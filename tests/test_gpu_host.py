@@ -101,3 +101,44 @@ def test_failure_in_an_early_chunk_stays_visible(sage):
     assert status == sage.ERR_DEVICE_TIMEOUT
     sage.attn_fwd_host(hq, hk, hv, out, "HND", False, scale, ws=ws, chunk_kv_heads=1)
     assert sage.device_status(ws) == sage.OK
+
+
+def _vw(name, lq, lk, **kw):
+    base = dict(B=0, Hq=4, Hkv=2, Lq=0, Lk=0, D=64, dtype=wl.F16, layout=wl.NHD,
+                causal=False, seed=910, k_offset_sigma=1.5, seqlens_q=lq, seqlens_k=lk)
+    base.update(kw)
+    return wl.Workload(name, **base)
+
+
+VARLEN_CASES = [
+    (_vw("varlen_d40_ragged", (1, 130, 257, 128), (5, 128, 300, 1), D=40), 1),
+    (_vw("varlen_bf16_gqa_causal", (200, 64, 333), (200, 64, 333), Hq=6, Hkv=3, D=128,
+         dtype=wl.BF16, causal=True, seed=911), 2),            # 2 does not divide 3
+    (_vw("varlen_empty_key_sequence", (130, 7, 256), (140, 0, 129), D=80, seed=912), 0),
+]
+
+
+def _compare_varlen(sage, w, chunk):
+    """sage_attn_fwd_varlen_host against sage_attn_fwd_varlen on the same
+    packed inputs: equal bit for bit, and nothing left in the status word."""
+    inp = wl.make_inputs(w)
+    d = H.device_inputs(w, inp)
+    ref = H.run_attention(sage, w, d)
+    hq, hk, hv = _host(d["q"]), _host(d["k"]), _host(d["v"])
+    out = torch.full(hq.shape, float("nan"), dtype=torch.float32).pin_memory()
+    cu_q, cu_k = torch.from_numpy(inp["cu_q"]), torch.from_numpy(inp["cu_k"])
+    ws = sage.alloc_workspace(sage.workspace_bytes_varlen_host(
+        w.nseg, sum(w.seqlens_q), sum(w.seqlens_k), w.Hq, w.Hkv, w.D, chunk))
+    sage.attn_fwd_varlen_host(hq, hk, hv, out, cu_q, cu_k, max(w.seqlens_q), max(w.seqlens_k),
+                              w.causal, wl.default_sm_scale(w), chunk_kv_heads=chunk, ws=ws)
+    assert sage.device_status(ws) == sage.OK                # synchronises
+    assert torch.equal(out, ref.cpu())
+
+
+@pytest.mark.parametrize("w,chunk", VARLEN_CASES, ids=[w.name for w, _ in VARLEN_CASES])
+def test_varlen_host_call_equals_device_call(sage, w, chunk):
+    _compare_varlen(sage, w, chunk)
+
+
+def test_varlen_host_call_at_full_size(sage):
+    _compare_varlen(sage, wl.WORKLOADS["varlen_d80"], 0)
