@@ -142,3 +142,28 @@ def test_varlen_host_call_equals_device_call(sage, w, chunk):
 
 def test_varlen_host_call_at_full_size(sage):
     _compare_varlen(sage, wl.WORKLOADS["varlen_d80"], 0)
+
+
+def test_varlen_failure_in_an_early_chunk_stays_visible(sage):
+    """The packed call keeps the status word across chunks as the dense one
+    does: a bounded wait that runs out in the first of two chunks shows after
+    the call, and the next call clears it."""
+    w = _vw("varlen_fault_chunks", (300, 200), (400, 260), Hq=2, Hkv=2, seed=913)
+    inp = wl.make_inputs(w)
+    d = H.device_inputs(w, inp)
+    hq, hk, hv = _host(d["q"]), _host(d["k"]), _host(d["v"])
+    out = torch.empty(hq.shape, dtype=torch.float32).pin_memory()
+    cu_q, cu_k = torch.from_numpy(inp["cu_q"]), torch.from_numpy(inp["cu_k"])
+    ws = sage.alloc_workspace(sage.workspace_bytes_varlen_host(2, 500, 660, 2, 2, w.D, 1))
+    scale = wl.default_sm_scale(w)
+    try:
+        sage.set_fault(skip_kv_tile=1, timeout_ns=50_000_000, launches=1)
+        sage.attn_fwd_varlen_host(hq, hk, hv, out, cu_q, cu_k, 300, 400, False, scale,
+                                  chunk_kv_heads=1, ws=ws)
+        status = sage.device_status(ws)                    # synchronises
+    finally:
+        sage.set_fault(-1, 0)
+    assert status == sage.ERR_DEVICE_TIMEOUT
+    sage.attn_fwd_varlen_host(hq, hk, hv, out, cu_q, cu_k, 300, 400, False, scale,
+                              chunk_kv_heads=1, ws=ws)
+    assert sage.device_status(ws) == sage.OK
