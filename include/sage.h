@@ -346,10 +346,10 @@ SAGE_API void sage_debug_set_fault(int skip_kv_tile, uint64_t timeout_ns);
 SAGE_API void sage_debug_set_fault_launches(int launches);
 
 /* Test hook: the prologue entry points run as one launch (1), as two
- * launches (2: Q tiles and K/V statistics, then K/V tiles), or choose by
- * size (0, the default: two launches when the K and V inputs exceed 5/4 of
- * the device's L2).  Other values mean 0.  The results are identical either
- * way; the hook lets tests cover both plans at any size. */
+ * launches (2: Q tiles and K/V statistics, then K/V tiles), or choose (0,
+ * the default: one launch, measured as fast or faster at every size).  Other
+ * values mean 0.  The results are identical either way; the hook lets tests
+ * cover both plans at any size. */
 SAGE_API void sage_debug_set_prologue_launches(int launches);
 
 /* Reads (synchronising `stream`) the device status word of workspace ws:

@@ -6,9 +6,9 @@
 // overview's Core features (INT8 Q/K, smoothing) and the SageAttention-RDNA4
 // v0.4.0 notes (key mean summed in fp64, 64-bit offsets).
 //
-// One persistent kernel, two CTAs per SM, launched cooperatively (every CTA
+// One persistent kernel, three CTAs per SM, launched cooperatively (every CTA
 // resident).  A CTA has eight consumer warps, a producer warp and a helper
-// warp around a ring of three 32 KB shared-memory stages.  The producer takes
+// warp around a ring of two 32 KB shared-memory stages.  The producer takes
 // work items from a counter in the workspace and copies each item's 128-token
 // input tile into a free stage with a tensor copy (TMA), zero-padded to Dp
 // channels; the consumers quantise the tile in the stage and release it.  A
@@ -66,7 +66,7 @@ constexpr int kConsumers = 256;              // eight consumer warps
 constexpr int kProducerWarp = 8;
 constexpr int kHelperWarp = 9;
 constexpr int kThreads = kConsumers + 64;
-constexpr int kStages = 3;
+constexpr int kStages = 2;                   // three CTAs per SM: more tiles in work at once
 constexpr int kQueue = 8;                    // finished stats tiles awaiting the helper
 constexpr int kMaxGroups = 64;               // counters per list in the workspace
 constexpr int64_t kGroupBytes = 100ll << 20; // K and V bytes of a group (target)
@@ -1226,7 +1226,7 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
 
 // --------------------------------------------------------------- kernel
 template <bool kTma, bool kBf16, int DP>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
 prologue_kernel(const __grid_constant__ ProParams p) {
   extern __shared__ uint8_t smem_raw[];
   PSmem& sm = *reinterpret_cast<PSmem*>(align1024(smem_raw));
@@ -1463,29 +1463,15 @@ cudaError_t launch_prologue(const SegGeo& g, const PrologueBuffers& b,
   prm.v16 = b.v16;
   prm.one = 1.0f;
   // One launch keeps a few groups of K and V in L2 between their two reads
-  // (the A list runs ahead of the B list).  When the K and V inputs exceed
-  // 5/4 of L2 (measured crossover: 134 MB one launch faster, 188 MB two
-  // launches), two launches stream better: the Q tiles, the K and V
-  // statistics and the final items; then the K and V tiles from the final
-  // statistics (counters of their own).
-  const int64_t ntk = g.varlen ? g.total_k : g.nseg * g.Lk;
-  const int64_t kv_bytes = 2 * ntk * g.Hkv * g.D * 2;
-  static std::atomic<int64_t> l2_bytes[64] = {};      // per device, filled once
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  int64_t l2b = l2_bytes[dev].load(std::memory_order_relaxed);
-  if (l2b == 0) {
-    int l2 = 0;
-    e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
-    if (e != cudaSuccess) return e;
-    l2b = l2 > 0 ? l2 : 1;
-    l2_bytes[dev].store(l2b, std::memory_order_relaxed);
-  }
-  const bool two = b.launches == 2 || (b.launches == 0 && 4 * kv_bytes > 5 * l2b);
+  // (the A list runs ahead of the B list).  Two launches (the Q tiles, the K
+  // and V statistics and the final items; then the K and V tiles from the
+  // final statistics, with counters of their own) re-read K and V from DRAM.
+  // With three CTAs per SM one launch measured as fast or faster at every
+  // size tried (134 MB to 402 MB of K and V), so two launches run only when
+  // a test asks for them.
+  const bool two = b.launches == 2;
   if (!two) return launch_any(prm, vec, kPlanAll, st);
-  e = launch_any(prm, vec, kPlanStatsQ, st);
+  cudaError_t e = launch_any(prm, vec, kPlanStatsQ, st);
   if (e != cudaSuccess) return e;
   if ((g.varlen ? g.max_k : g.Lk) <= 0) return cudaSuccess;    // no keys to quantise
   ProParams kv = prm;

@@ -320,8 +320,9 @@ def test_inconsistent_cu_seqlens_reported(sage):
 
 
 # ------------------------------------------------- the prologue's two-launch plan
-# Inputs whose K and V exceed 5/4 of L2 take two prologue launches (Q tiles
-# and K/V statistics, then K/V tiles).  A test hook forces either plan, so the
+# The prologue can also run as two launches (Q tiles and K/V statistics,
+# then K/V tiles); the automatic plan is one launch.  A test hook forces either
+# plan, so the
 # small shapes check the two-launch plan bit-exactly against the oracle and
 # the bench shape checks that both plans write identical workspaces.
 TWO_LAUNCH = ["d1", "d128_ragged", "d80", "causal_lq_gt_lk", "gqa_nhd", "varlen_small",
