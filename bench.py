@@ -37,9 +37,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per attention-kernel launch on the default
 # workload, from the ncu capture of the attention kernel (None where no
 # capture of the current kernel exists).
-ATTN_NCU_DRAM_BYTES = {"b2_h24_l4096_d128": 126.745088e6 + 62.736640e6}
+ATTN_NCU_DRAM_BYTES = {"b2_h24_l4096_d128": 126.744320e6 + 63.198208e6}
 # the same for the FP16-PV variant's attention kernel (fp16 V and P~)
-ATTN16_NCU_DRAM_BYTES = {"b2_h24_l4096_d128": 152.318464e6 + 65.660928e6}
+ATTN16_NCU_DRAM_BYTES = {"b2_h24_l4096_d128": 152.014592e6 + 63.843584e6}
 # (query row, key) pairs of attention in the oracle's bounded sample (one
 # head of the 4096 x 4096 workload; a whole small workload)
 ORACLE_PAIR_BUDGET = 4096 * 4096

@@ -688,45 +688,61 @@ attn_kernel(const __grid_constant__ CUtensorMap tm_q,
       const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_new, -m_new);
       const float2 one2 = make_float2(p.one, p.one);
       const float2 kL448 = make_float2(kLog2_448, kLog2_448);
+      // The row is encoded and stored in parts (64 keys at Dp = 128, 32 at
+      // Dp = 64), so only a part of it is live in registers: fewer spills, 1-4 %
+      // faster than the whole row at once.  The wait for the previous PV comes
+      // before the first part's store; at Dp = 64 the shorter PV is done by
+      // the end of the first quarter, at Dp = 128 only by mid-row.
       float2 a01 = make_float2(0.0f, 0.0f), a23 = make_float2(0.0f, 0.0f);
-      uint32_t w[kV16 ? 64 : 32];
+      constexpr int kParts = DP == 64 ? 4 : 2;
+      constexpr int kPartQ = 32 / kParts;                    // groups of 4 keys per part
+      constexpr int kPartW = (kV16 ? 64 : 32) / kParts;      // packed words per part
+      constexpr int kPartC = (kV16 ? 16 : 8) / kParts;       // 16-byte chunks per part
 #pragma unroll
-      for (int q4 = 0; q4 < 32; ++q4) {
-        const int i = 4 * q4;
-        const uint32_t* src = &sr[i >> 5][i & 31];
-        const float2 x01 = __fmul2_rn(make_float2(__uint_as_float(src[0]), __uint_as_float(src[1])), c2);
-        const float2 x23 = __fmul2_rn(make_float2(__uint_as_float(src[2]), __uint_as_float(src[3])), c2);
-        float2 d01 = __ffma2_rn(x01, one2, nm2);
-        float2 d23 = __ffma2_rn(x23, one2, nm2);
-        if constexpr (!kV16) {                             // log2 of 448 P
-          d01 = __fadd2_rn(d01, kL448);
-          d23 = __fadd2_rn(d23, kL448);
+      for (int part = 0; part < kParts; ++part) {
+        uint32_t w[kPartW];
+#pragma unroll
+        for (int qq = 0; qq < kPartQ; ++qq) {
+          const int q4 = kPartQ * part + qq;
+          const int i = 4 * q4;
+          const uint32_t* src = &sr[i >> 5][i & 31];
+          const float2 x01 = __fmul2_rn(make_float2(__uint_as_float(src[0]), __uint_as_float(src[1])), c2);
+          const float2 x23 = __fmul2_rn(make_float2(__uint_as_float(src[2]), __uint_as_float(src[3])), c2);
+          float2 d01 = __ffma2_rn(x01, one2, nm2);
+          float2 d23 = __ffma2_rn(x23, one2, nm2);
+          if constexpr (!kV16) {                             // log2 of 448 P
+            d01 = __fadd2_rn(d01, kL448);
+            d23 = __fadd2_rn(d23, kL448);
+          }
+          const float2 p01 = make_float2(fast_exp2(d01.x), fast_exp2(d01.y));
+          const float2 p23 = make_float2(fast_exp2(d23.x), fast_exp2(d23.y));
+          if constexpr (kV16) {
+            const __half2 h01 = __floats2half2_rn(p01.x, p01.y);
+            const __half2 h23 = __floats2half2_rn(p23.x, p23.y);
+            w[2 * qq] = *reinterpret_cast<const uint32_t*>(&h01);
+            w[2 * qq + 1] = *reinterpret_cast<const uint32_t*>(&h23);
+          } else {
+            w[qq] = pack_e4m3x2(p01.x, p01.y) | (pack_e4m3x2(p23.x, p23.y) << 16);
+          }
+          a01 = __fadd2_rn(a01, p01);
+          a23 = __fadd2_rn(a23, p23);
         }
-        const float2 p01 = make_float2(fast_exp2(d01.x), fast_exp2(d01.y));
-        const float2 p23 = make_float2(fast_exp2(d23.x), fast_exp2(d23.y));
-        if constexpr (kV16) {
-          const __half2 h01 = __floats2half2_rn(p01.x, p01.y);
-          const __half2 h23 = __floats2half2_rn(p23.x, p23.y);
-          w[2 * q4] = *reinterpret_cast<const uint32_t*>(&h01);
-          w[2 * q4 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
-        } else {
-          w[q4] = pack_e4m3x2(p01.x, p01.y) | (pack_e4m3x2(p23.x, p23.y) << 16);
+        // the P~ buffer is free once PV(j-1) has read it
+        if (part == 0 && j > 0) {
+          ok = wait_all(&o_done[t], (j - 1) & 1, abort_flag, p.status, p.timeout_ns);
+          if (!ok) break;
         }
-        a01 = __fadd2_rn(a01, p01);
-        a23 = __fadd2_rn(a23, p23);
+        // 16-byte chunks of the row, swizzled by row % 8 within each 64-key
+        // (fp16) or 128-key (e4m3) atom
+#pragma unroll
+        for (int cc = 0; cc < kPartC; ++cc) {
+          const int c16 = kPartC * part + cc;
+          *reinterpret_cast<uint4*>(prow + (c16 / 8) * kAtomBytes + (((c16 % 8) ^ rsw) << 4)) =
+              make_uint4(w[4 * cc], w[4 * cc + 1], w[4 * cc + 2], w[4 * cc + 3]);
+        }
       }
+      if (!ok) break;
       const float a0 = a01.x, a1 = a01.y, a2 = a23.x, a3 = a23.y;
-      // the P~ buffer is free once PV(j-1) has read it
-      if (j > 0) {
-        ok = wait_all(&o_done[t], (j - 1) & 1, abort_flag, p.status, p.timeout_ns);
-        if (!ok) break;
-      }
-      // 16-byte chunks of the row, swizzled by row % 8 within each 64-key
-      // (fp16) or 128-key (e4m3) atom
-#pragma unroll
-      for (int c16 = 0; c16 < (kV16 ? 16 : 8); ++c16)
-        *reinterpret_cast<uint4*>(prow + (c16 / 8) * kAtomBytes + (((c16 % 8) ^ rsw) << 4)) =
-            make_uint4(w[4 * c16], w[4 * c16 + 1], w[4 * c16 + 2], w[4 * c16 + 3]);
       fence_proxy_async_smem();
       l448 = l448 * alpha + ((a0 + a1) + (a2 + a3));
       m = m_new;
