@@ -35,8 +35,8 @@
 // arrived, so they find the group's sums complete and their K and V, read
 // by the A list with an evict-last hint, still in L2.  Few large groups
 // measured faster than many small ones (fewer barrier rounds; the Q list
-// fills the waits).  Inputs whose K and V exceed 5/4 of L2 are re-read from
-// HBM anyway and take two launches instead (launch_prologue).  The Q tiles depend on nothing: they form one more
+// fills the waits).  Beyond L2, the part of K and V that does not stay there
+// is read again from HBM.  The Q tiles depend on nothing: they form one more
 // list, taken only when neither of the others has an item ready, so they
 // fill the barrier waits and the end.  Nothing waits inside a list, and
 // every wait is bounded (timeout -> status bit).  Every 128-token
