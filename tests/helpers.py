@@ -9,6 +9,13 @@ from quantized_attention_smooth_gb300 import workloads as wl
 
 ATOL_ORACLE = 2e-3      # max-abs difference to the oracle (fp32 outputs)
 COS_EXACT = 0.999       # cosine similarity to fp64 exact attention
+# An element beyond ATOL_ORACLE is accepted only in a row where the oracle's
+# own 448 P of some key lies within NEAR_TIE of an e4m3 rounding boundary: the
+# kernel's exp2 (a few ulp from the oracle's) may round that P~ code the other
+# way.  Such a flip moves the output by at most one e4m3 step of that key's
+# weight times |v - o|; FLIP_CAP bounds what the tests accept.
+NEAR_TIE = 2.0 ** -19
+FLIP_CAP = 2e-2
 
 
 def torch_dtype(dtype):
@@ -145,6 +152,39 @@ def compare_prologue(orc_seg: dict, gpu_seg: dict, D: int):
         else:
             res[name] = int(np.sum(a != b))
     return res
+
+
+def near_tie_rows(orc, pro, h, rows, causal, sm_scale):
+    """For query head h of one segment: which of `rows` have a key whose 448 P,
+    in the oracle's arithmetic (fp32 dequantised logits, running maximum per
+    128-key block, exp2), lies within NEAR_TIE of an e4m3 rounding boundary."""
+    f32 = np.float32
+    Hq, Hkv, Lk = pro["Hq"], pro["Hkv"], pro["Lk"]
+    hk = h // (Hq // Hkv)
+    scale_log2 = f32(f32(sm_scale) * f32(1.4426950408889634))
+    k8 = pro["k8"][hk].astype(np.int64)
+    out = []
+    for i in rows:
+        S = k8 @ pro["q8"][h, i].astype(np.int64)
+        m = f32(-np.inf)
+        tie = False
+        for b in range((Lk + 127) // 128):
+            j0, j1 = 128 * b, min(Lk, 128 * b + 128)
+            c = f32(f32(pro["s_q"][h, i] * pro["s_k"][hk, b]) * scale_log2)
+            x = (S[j0:j1].astype(f32) * c).astype(f32)
+            if causal:
+                x[np.arange(j0, j1) > i] = -np.inf
+            if not np.isfinite(x).any():
+                continue
+            m_new = f32(max(m, x.max()))
+            d = (x - m_new).astype(f32)
+            v448 = (f32(448.0) * np.exp2(d.astype(np.float64)).astype(f32)).astype(f32)
+            lo = orc.e4m3_encode((v448 * (1.0 - NEAR_TIE)).astype(f32))
+            hi = orc.e4m3_encode((v448 * (1.0 + NEAR_TIE)).astype(f32))
+            tie |= bool(np.any(lo != hi))
+            m = m_new
+        out.append(tie)
+    return out
 
 
 def cosine(a, b):

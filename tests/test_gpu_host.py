@@ -115,6 +115,9 @@ VARLEN_CASES = [
     (_vw("varlen_bf16_gqa_causal", (200, 64, 333), (200, 64, 333), Hq=6, Hkv=3, D=128,
          dtype=wl.BF16, causal=True, seed=911), 2),            # 2 does not divide 3
     (_vw("varlen_empty_key_sequence", (130, 7, 256), (140, 0, 129), D=80, seed=912), 0),
+    (_vw("varlen_many_sequences", tuple(int(x) for x in np.random.default_rng(914).integers(1, 300, 80)),
+         tuple(int(x) for x in np.random.default_rng(915).integers(0, 300, 80)), Hq=6, Hkv=3,
+         seed=914), 0),
 ]
 
 

@@ -33,6 +33,16 @@ def _small(name, **kw):
     return wl.Workload(name, **base)
 
 
+def _lengths(n, lo, hi, seed, zeros=0):
+    """n sequence lengths drawn uniformly from [lo, hi] (seeded), `zeros` of
+    them, chosen at random, set to 0."""
+    rng = np.random.default_rng(seed)
+    x = rng.integers(lo, hi + 1, size=n)
+    if zeros:
+        x[rng.choice(n, size=zeros, replace=False)] = 0
+    return tuple(int(v) for v in x)
+
+
 SMALL = [
     wl.WORKLOADS["small_d64"],
     _small("d128_ragged", Lq=300, Lk=333, D=128, seed=1),
@@ -60,7 +70,21 @@ SMALL = [
            causal=True, seqlens_q=(200, 64, 333), seqlens_k=(200, 64, 333)),
     _small("varlen_empty_keys", B=0, Hq=4, Hkv=2, Lq=0, Lk=0, D=64, layout=wl.NHD, seed=20,
            seqlens_q=(130, 7, 256), seqlens_k=(140, 0, 129)),
+    # many short packed sequences: every segment's offsets, ragged tiles and
+    # (for some) an empty key set
+    _small("varlen_many", B=0, Hq=4, Hkv=2, Lq=0, Lk=0, D=64, layout=wl.NHD, seed=21,
+           seqlens_q=_lengths(96, 1, 300, 210), seqlens_k=_lengths(96, 0, 300, 211, zeros=8)),
+    _small("varlen_many_causal_bf16", B=0, Hq=2, Hkv=2, Lq=0, Lk=0, D=128, layout=wl.NHD,
+           seed=22, dtype=wl.BF16, causal=True,
+           seqlens_q=_lengths(64, 1, 400, 212), seqlens_k=_lengths(64, 1, 400, 212)),
 ]
+
+
+# Stress shapes (many short packed sequences, 14k rows each): their rows span
+# millions of P~ codes, so a near-tie that the kernel's exp2 rounds the other
+# way (H.near_tie_rows) lands on a heavily weighted key now and then; one such
+# row measured 2.8e-3.  Everything else stays within H.ATOL_ORACLE.
+STRESS = {"varlen_many", "varlen_many_causal_bf16"}
 
 
 def _check_prologue(sage, orc, w, inp, d):
@@ -83,8 +107,12 @@ def _check_prologue(sage, orc, w, inp, d):
     return qt, ws
 
 
-def _check_rows(orc, w, inp, out_np, samples, pros=None):
-    """samples: list of (segment, (h0, h1), (r0, r1))."""
+def _check_rows(orc, w, inp, out_np, samples, pros=None, allow_ties=False):
+    """samples: list of (segment, (h0, h1), (r0, r1)).  Returns the largest
+    difference to the oracle and the smallest cosine to fp64 attention.  With
+    allow_ties, rows beyond H.ATOL_ORACLE whose excess a P~ near-tie explains
+    are checked against H.FLIP_CAP here and left out of the largest
+    difference; anything else still counts."""
     worst, cos_min = 0.0, 1.0
     pros = {} if pros is None else pros
     for s, heads, rows in samples:
@@ -98,7 +126,14 @@ def _check_rows(orc, w, inp, out_np, samples, pros=None):
         sl = (slice(*heads), slice(*rows))
         g, r, e = got[sl], ref[sl], ex[sl]
         assert np.all(np.isfinite(g)), f"non-finite output in segment {s}"
-        worst = max(worst, float(np.max(np.abs(g.astype(np.float64) - r))))
+        err = np.max(np.abs(g.astype(np.float64) - r), axis=-1)        # [heads, rows]
+        for hh, ii in zip(*np.nonzero(err > H.ATOL_ORACLE) if allow_ties else ([], [])):
+            h, i = heads[0] + int(hh), rows[0] + int(ii)
+            assert err[hh, ii] <= H.FLIP_CAP, (s, h, i, float(err[hh, ii]))
+            assert H.near_tie_rows(orc, pros[s], h, [i], w.causal, scale)[0], \
+                f"segment {s} head {h} row {i}: {float(err[hh, ii])} with no P~ near-tie"
+            err[hh, ii] = 0.0
+        worst = max(worst, float(err.max()) if err.size else 0.0)
         if np.linalg.norm(e) > 0:
             cos_min = min(cos_min, H.cosine(g, e))
     return worst, cos_min
@@ -114,7 +149,8 @@ def test_small_shapes_bit_exact_and_all_rows(sage, orc, w):
     for s, (lq, lk) in enumerate(w.seg_lengths()):
         if lq > 0:
             samples.append((s, (0, w.Hq), (0, lq)))
-    worst, cmin = _check_rows(orc, w, inp, out, samples, ws.oracle)
+    worst, cmin = _check_rows(orc, w, inp, out, samples, ws.oracle,
+                              allow_ties=w.name in STRESS)
     assert worst <= H.ATOL_ORACLE, worst
     assert cmin >= H.COS_EXACT, cmin
 
