@@ -72,6 +72,10 @@ SMALL = [
            seqlens_q=(130, 7, 256), seqlens_k=(140, 0, 129)),
     # many short packed sequences: every segment's offsets, ragged tiles and
     # (for some) an empty key set
+    _small("dense_many_batches", B=32, Hq=2, Hkv=1, Lq=70, Lk=90, D=128, layout=wl.NHD,
+           seed=23),
+    _small("gqa8_causal_bf16", B=1, Hq=16, Hkv=2, Lq=256, Lk=384, D=64, causal=True,
+           dtype=wl.BF16, seed=24),
     _small("varlen_many", B=0, Hq=4, Hkv=2, Lq=0, Lk=0, D=64, layout=wl.NHD, seed=21,
            seqlens_q=_lengths(96, 1, 300, 210), seqlens_k=_lengths(96, 0, 300, 211, zeros=8)),
     _small("varlen_many_causal_bf16", B=0, Hq=2, Hkv=2, Lq=0, Lk=0, D=128, layout=wl.NHD,
