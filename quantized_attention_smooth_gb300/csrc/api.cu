@@ -592,7 +592,8 @@ int sm_count_of_current_device() {
 }
 
 // chunk_kv <= 0 picks enough kv heads for one wave of query-tile pairs per
-// chunk (one per SM), so that each chunk's attention still fills the GPU.
+// chunk (one per SM), so that each chunk's attention still fills the GPU, or
+// one fewer when that still fills 90 % of the wave.
 // Packed sequences take four waves: a chunk's attention lasts at least as
 // long as a pair of its longest sequence, so a chunk of few heads leaves
 // most SMs idle behind that pair (measured on 8 sequences of 2k-16k tokens,
@@ -608,6 +609,10 @@ HostPlan host_plan(const HostShape& h, int64_t chunk_kv) {
     const int64_t sms = sm_count_of_current_device() > 0 ? sm_count_of_current_device() : 152;
     const int64_t want = (h.varlen ? 4 : 1) * sms;
     chunk_kv = pairs > 0 ? (want + pairs - 1) / pairs : h.Hkv;
+    // A dense chunk one kv head smaller that still fills 90 % of the wave
+    // keeps its pairs out of a second, nearly empty wave (B=2 H=24 L=4096:
+    // 9 kv heads, 144 pairs, 1.047 ms per call against 1.111 ms for 10).
+    if (!h.varlen && chunk_kv > 1 && 10 * (chunk_kv - 1) * pairs >= 9 * want) --chunk_kv;
   }
   P.chunk_kv = chunk_kv < 1 ? 1 : (chunk_kv > h.Hkv ? h.Hkv : chunk_kv);
   const int64_t hq = P.chunk_kv * P.group;

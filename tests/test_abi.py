@@ -194,15 +194,20 @@ def test_host_buffer_call_sizes_and_refusals():
 
 def test_host_buffer_call_automatic_chunk():
     """The automatic chunk holds one wave of query-tile pairs (one per SM; the
-    plan assumes GB300's 152 SMs when no device answers): at B=2 H=24 L=4096,
-    16 pairs per head, so 10 kv heads per chunk."""
+    plan assumes GB300's 152 SMs when no device answers), or one kv head fewer
+    when that still fills 90 % of the wave: at B=2 H=24 L=4096, 16 pairs per
+    head, 10 heads would spill 8 pairs into a second wave and 9 heads (144
+    pairs) fill 95 % of one.  At L=32768 (128 pairs per head) one head fills
+    only 84 %, so two stay."""
     import torch
     L = sage.lib
     if torch.cuda.is_available():
         pytest.skip("the device's own SM count decides on a GPU")
     auto = L.sage_workspace_bytes_host(2, 24, 24, 4096, 4096, 128, 0)
-    assert auto == L.sage_workspace_bytes_host(2, 24, 24, 4096, 4096, 128, 10)
-    assert auto != L.sage_workspace_bytes_host(2, 24, 24, 4096, 4096, 128, 9)
+    assert auto == L.sage_workspace_bytes_host(2, 24, 24, 4096, 4096, 128, 9)
+    assert auto != L.sage_workspace_bytes_host(2, 24, 24, 4096, 4096, 128, 10)
+    long = L.sage_workspace_bytes_host(1, 24, 24, 32768, 32768, 128, 0)
+    assert long == L.sage_workspace_bytes_host(1, 24, 24, 32768, 32768, 128, 2)
     # a chunk never exceeds the kv heads there are
     assert (L.sage_workspace_bytes_host(1, 8, 2, 128, 128, 64, 0) ==
             L.sage_workspace_bytes_host(1, 8, 2, 128, 128, 64, 2))
