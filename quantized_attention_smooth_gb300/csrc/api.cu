@@ -593,7 +593,8 @@ int sm_count_of_current_device() {
 
 // chunk_kv <= 0 picks enough kv heads for one wave of query-tile pairs per
 // chunk (one per SM), so that each chunk's attention still fills the GPU, or
-// one fewer when that still fills 90 % of the wave.
+// one fewer when that still fills 90 % of the wave; chunks whose attention
+// outlasts their copies are sized for whole waves instead.
 // Packed sequences take four waves: a chunk's attention lasts at least as
 // long as a pair of its longest sequence, so a chunk of few heads leaves
 // most SMs idle behind that pair (measured on 8 sequences of 2k-16k tokens,
@@ -613,6 +614,22 @@ HostPlan host_plan(const HostShape& h, int64_t chunk_kv) {
     // keeps its pairs out of a second, nearly empty wave (B=2 H=24 L=4096:
     // 9 kv heads, 144 pairs, 1.047 ms per call against 1.111 ms for 10).
     if (!h.varlen && chunk_kv > 1 && 10 * (chunk_kv - 1) * pairs >= 9 * want) --chunk_kv;
+    // A dense chunk whose attention outlasts its copies (long key spans: more
+    // than ~7000 flops per copied byte, about 1.4 PFLOP/s of attention over a
+    // 200 GB/s link) is sized for whole waves of pairs instead, the smallest
+    // that wastes at most 5 % of its last wave (L=32768: 7 kv heads, 896 pairs
+    // in 6 waves, 14.06 ms per call against 15.45 ms for 2 heads).
+    const double flops = 4.0 * P.group * h.Lq * h.Lk;              // per kv head, / D
+    const double bytes = 6.0 * P.group * h.Lq + 4.0 * h.Lk;        // q, k, v in, out; / D
+    if (!h.varlen && pairs > 0 && flops > 7000.0 * bytes) {
+      for (int64_t c = chunk_kv; c <= h.Hkv; ++c) {
+        const int64_t n = c * pairs, waves = (n + sms - 1) / sms;
+        if (20 * (waves * sms - n) <= n) {                         // waste <= 5 %
+          chunk_kv = c;
+          break;
+        }
+      }
+    }
   }
   P.chunk_kv = chunk_kv < 1 ? 1 : (chunk_kv > h.Hkv ? h.Hkv : chunk_kv);
   const int64_t hq = P.chunk_kv * P.group;

@@ -197,8 +197,7 @@ def test_host_buffer_call_automatic_chunk():
     plan assumes GB300's 152 SMs when no device answers), or one kv head fewer
     when that still fills 90 % of the wave: at B=2 H=24 L=4096, 16 pairs per
     head, 10 heads would spill 8 pairs into a second wave and 9 heads (144
-    pairs) fill 95 % of one.  At L=32768 (128 pairs per head) one head fills
-    only 84 %, so two stay."""
+    pairs) fill 95 % of one."""
     import torch
     L = sage.lib
     if torch.cuda.is_available():
@@ -206,8 +205,15 @@ def test_host_buffer_call_automatic_chunk():
     auto = L.sage_workspace_bytes_host(2, 24, 24, 4096, 4096, 128, 0)
     assert auto == L.sage_workspace_bytes_host(2, 24, 24, 4096, 4096, 128, 9)
     assert auto != L.sage_workspace_bytes_host(2, 24, 24, 4096, 4096, 128, 10)
+    # B=1 H=24 L=32768: attention outlasts the copies (13107 flops per copied
+    # byte over D), so the chunk fills whole waves: 7 kv heads, 896 pairs in
+    # 6 waves of 152 (1.8 % idle)
     long = L.sage_workspace_bytes_host(1, 24, 24, 32768, 32768, 128, 0)
-    assert long == L.sage_workspace_bytes_host(1, 24, 24, 32768, 32768, 128, 2)
+    assert long == L.sage_workspace_bytes_host(1, 24, 24, 32768, 32768, 128, 7)
+    # B=4 L=8192 with 4 query heads per kv head stays copy-bound (4681): two
+    # kv heads, the one-wave rule
+    gqa = L.sage_workspace_bytes_host(4, 32, 8, 8192, 8192, 128, 0)
+    assert gqa == L.sage_workspace_bytes_host(4, 32, 8, 8192, 8192, 128, 2)
     # a chunk never exceeds the kv heads there are
     assert (L.sage_workspace_bytes_host(1, 8, 2, 128, 128, 64, 0) ==
             L.sage_workspace_bytes_host(1, 8, 2, 128, 128, 64, 2))
