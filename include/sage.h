@@ -352,6 +352,14 @@ SAGE_API void sage_debug_set_fault_launches(int launches);
  * cover both plans at any size. */
 SAGE_API void sage_debug_set_prologue_launches(int launches);
 
+/* Test hook: the host-buffer calls (sage_attn_fwd_host, _host_pv16,
+ * sage_attn_fwd_varlen_host) treat chunk `chunk` (0-based, in order) as if
+ * its launch had failed: they enqueue nothing for it or after it and return
+ * SAGE_ERR_INVALID_ARG, after making the caller's stream wait for the
+ * copies of the earlier chunks, as they do on any failure.  -1, the
+ * default, turns it off. */
+SAGE_API void sage_debug_set_host_fail_chunk(int chunk);
+
 /* Reads (synchronising `stream`) the device status word of workspace ws:
  * SAGE_OK, SAGE_ERR_DEVICE_TIMEOUT, SAGE_ERR_INVALID_ARG, or
  * SAGE_ERR_UNSUPPORTED for an internal inconsistency the prologue caught

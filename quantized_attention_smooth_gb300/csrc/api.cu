@@ -35,6 +35,7 @@ std::atomic<int> g_prologue_launches{0};
 std::atomic<unsigned long long> g_timeout_ns{0};
 // attention launches the failure-injection hook still applies to (-1: all)
 std::atomic<int> g_fault_launches{-1};
+std::atomic<int> g_host_fail_chunk{-1};
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;   // 1 s
 
 // Bound of every device-side wait of the next launches.
@@ -762,6 +763,10 @@ sage_status host_pipeline(const void* q, const void* k, const void* v, float* ou
   e = cudaEventRecord(rt.start, st);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(rt.in, rt.start, 0);
   if (e != cudaSuccess) return cuda_fail(e, "pipeline start");
+  // Every exit from here on first makes the caller's stream wait for the copies
+  // already enqueued, so that it never completes while one of them still
+  // reads the staging or writes the caller's host output.
+  const char* where = nullptr;
   int32_t* dcu_q = reinterpret_cast<int32_t*>(base + P.cu);
   int32_t* dcu_k = reinterpret_cast<int32_t*>(
       base + P.cu + align256(static_cast<size_t>(h.nseq + 1) * 4));
@@ -770,10 +775,10 @@ sage_status host_pipeline(const void* q, const void* k, const void* v, float* ou
     const size_t n = static_cast<size_t>(h.nseq + 1) * 4;
     e = cudaMemcpyAsync(dcu_q, cu_q, n, cudaMemcpyHostToDevice, rt.in);
     if (e == cudaSuccess) e = cudaMemcpyAsync(dcu_k, cu_k, n, cudaMemcpyHostToDevice, rt.in);
-    if (e != cudaSuccess) return cuda_fail(e, "pipeline offsets");
+    if (e != cudaSuccess) where = "pipeline offsets";
   }
   int64_t i = 0;
-  for (int64_t b = 0; b < h.B; ++b) {
+  for (int64_t b = 0; b < h.B && where == nullptr && s == SAGE_OK; ++b) {
     for (int64_t g0 = 0; g0 < h.Hkv; g0 += P.chunk_kv, ++i) {
       const int64_t gn = h.Hkv - g0 < P.chunk_kv ? h.Hkv - g0 : P.chunk_kv;
       const int64_t h0 = g0 * P.group, hn = gn * P.group;
@@ -794,9 +799,16 @@ sage_status host_pipeline(const void* q, const void* k, const void* v, float* ou
       // compute: after the inputs landed and the slot's previous output left
       if (e == cudaSuccess) e = cudaStreamWaitEvent(st, rt.loaded[sl], 0);
       if (e == cudaSuccess) e = cudaStreamWaitEvent(st, rt.stored[sl], 0);
-      if (e != cudaSuccess) return cuda_fail(e, "pipeline copy-in");
+      if (e != cudaSuccess) {
+        where = "pipeline copy-in";
+        break;
+      }
       // the first chunk clears the device status word, the others keep it,
       // so a bounded wait that ran out in any chunk stays visible
+      if (i == g_host_fail_chunk.load()) {
+        s = fail(SAGE_ERR_INVALID_ARG, "chunk %lld failed (test hook)", (long long)i);
+        break;
+      }
       if (h.varlen)
         s = varlen_fwd(dq, dk, dv, dout, dcu_q, dcu_k, h.nseq, h.Lq, h.Lk, h.max_q, h.max_k,
                        hn, gn, h.D, is_causal, sm_scale, dtype, base, P.ws_bytes, stream,
@@ -804,20 +816,30 @@ sage_status host_pipeline(const void* q, const void* k, const void* v, float* ou
       else
         s = dense_fwd(dq, dk, dv, dout, 1, hn, gn, h.Lq, h.Lk, h.D, layout, is_causal,
                       sm_scale, dtype, base, P.ws_bytes, stream, v16, /*keep_status=*/i > 0);
-      if (s != SAGE_OK) return s;
+      if (s != SAGE_OK) break;
       e = cudaEventRecord(rt.computed[sl], st);
       // output: after the chunk was computed
       if (e == cudaSuccess) e = cudaStreamWaitEvent(rt.out, rt.computed[sl], 0);
       if (e == cudaSuccess)
         e = copy_chunk(out, dout, false, hnd, b, h0, hn, h.Hq, h.Lq, h.D, 4, rt.out);
       if (e == cudaSuccess) e = cudaEventRecord(rt.stored[sl], rt.out);
-      if (e != cudaSuccess) return cuda_fail(e, "pipeline copy-out");
+      if (e != cudaSuccess) {
+        where = "pipeline copy-out";
+        break;
+      }
     }
   }
-  // the caller's stream completes once every output is in host memory
-  e = cudaStreamWaitEvent(st, rt.stored[0], 0);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, rt.stored[1], 0);
-  return e == cudaSuccess ? ok() : cuda_fail(e, "pipeline end");
+  // the caller's stream completes once every output is in host memory (and,
+  // after a failure, once every copy enqueued so far has finished; rt.start,
+  // whose first record the copy stream has already waited for, marks the end
+  // of the copy-in stream)
+  cudaError_t ej = cudaEventRecord(rt.start, rt.in);
+  if (ej == cudaSuccess) ej = cudaStreamWaitEvent(st, rt.start, 0);
+  if (ej == cudaSuccess) ej = cudaStreamWaitEvent(st, rt.stored[0], 0);
+  if (ej == cudaSuccess) ej = cudaStreamWaitEvent(st, rt.stored[1], 0);
+  if (where != nullptr) return cuda_fail(e, where);
+  if (s != SAGE_OK) return s;
+  return ej == cudaSuccess ? ok() : cuda_fail(ej, "pipeline end");
 }
 
 // Dense host-buffer call: argument checks, then the pipeline.
@@ -1101,6 +1123,10 @@ void sage_debug_set_fault_launches(int launches) {
 
 void sage_debug_set_prologue_launches(int launches) {
   g_prologue_launches.store(launches == 1 || launches == 2 ? launches : 0);
+}
+
+void sage_debug_set_host_fail_chunk(int chunk) {
+  g_host_fail_chunk.store(chunk < 0 ? -1 : chunk);
 }
 
 }  // extern "C"

@@ -29,6 +29,7 @@ EXPORTS = (
     "sage_workspace_bytes_host", "sage_attn_fwd_host", "sage_attn_fwd_host_pv16",
     "sage_debug_pv_accum", "sage_debug_set_fault_launches", "sage_kv_stats_noalloc_status",
     "sage_debug_tc_rate", "sage_workspace_bytes_varlen_host", "sage_attn_fwd_varlen_host",
+    "sage_debug_set_host_fail_chunk",
 )
 
 
@@ -98,6 +99,7 @@ def _load():
         "sage_debug_set_fault": ([I, ctypes.c_uint64], None),
         "sage_debug_set_prologue_launches": ([I], None),
         "sage_debug_set_fault_launches": ([I], None),
+        "sage_debug_set_host_fail_chunk": ([I], None),
         "sage_debug_tc_rate": ([I, I64, P, P], I),
         "sage_kv_stats_noalloc_status": ([P], I),
         "sage_device_status": ([P, P], I),
@@ -547,6 +549,11 @@ def set_fault(skip_kv_tile: int = -1, timeout_ns: int = 0, launches: int = -1):
 def set_prologue_launches(launches: int = 0):
     """Test hook: 1 or 2 prologue launches, 0 to choose by size."""
     _lib.sage_debug_set_prologue_launches(int(launches))
+
+
+def set_host_fail_chunk(chunk: int = -1):
+    """Test hook: the host-buffer calls fail at chunk `chunk` (-1: off)."""
+    _lib.sage_debug_set_host_fail_chunk(int(chunk))
 
 
 def device_status(ws, stream=None) -> int:

@@ -103,6 +103,43 @@ def test_failure_in_an_early_chunk_stays_visible(sage):
     assert sage.device_status(ws) == sage.OK
 
 
+@pytest.mark.parametrize("fail_at", [0, 1, 3])
+def test_failed_chunk_leaves_earlier_chunks_complete(sage, fail_at):
+    """A chunk that fails (the library's test hook) ends the host-buffer call
+    with an error.  The caller's stream still waits for the earlier chunks'
+    copies: once it is synchronised their rows are in host memory, equal to
+    the device call's, and no later row was written; the next call runs
+    normally.  Chunk c of B=2, Hkv=2 at one kv head per chunk is batch entry
+    c // 2, query heads 2 (c % 2) and 2 (c % 2) + 1."""
+    w = _w("fail_chunk", Lq=256, Lk=384, seed=906)
+    inp = wl.make_inputs(w)
+    d = H.device_inputs(w, inp)
+    scale = wl.default_sm_scale(w)
+    ref = torch.empty(d["q"].shape, dtype=torch.float32, device="cuda")
+    sage.attn_fwd(d["q"], d["k"], d["v"], ref, "HND", False, scale)
+    ref = ref.cpu()
+    hq, hk, hv = _host(d["q"]), _host(d["k"]), _host(d["v"])
+    out = torch.full(hq.shape, float("nan"), dtype=torch.float32).pin_memory()
+    try:
+        sage.set_host_fail_chunk(fail_at)
+        with pytest.raises(sage.SageError) as err:
+            sage.attn_fwd_host(hq, hk, hv, out, "HND", False, scale, chunk_kv_heads=1)
+    finally:
+        sage.set_host_fail_chunk(-1)
+    assert err.value.status == sage.ERR_INVALID_ARG
+    torch.cuda.current_stream().synchronize()
+    for c in range(4):
+        b, h0 = c // 2, 2 * (c % 2)
+        rows = out[b, h0:h0 + 2]
+        if c < fail_at:
+            assert torch.equal(rows, ref[b, h0:h0 + 2]), c
+        else:
+            assert torch.isnan(rows).all(), c
+    sage.attn_fwd_host(hq, hk, hv, out, "HND", False, scale, chunk_kv_heads=1)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+
+
 def _vw(name, lq, lk, **kw):
     base = dict(B=0, Hq=4, Hkv=2, Lq=0, Lk=0, D=64, dtype=wl.F16, layout=wl.NHD,
                 causal=False, seed=910, k_offset_sigma=1.5, seqlens_q=lq, seqlens_k=lk)
