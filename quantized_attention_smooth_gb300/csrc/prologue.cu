@@ -73,6 +73,7 @@ constexpr int64_t kGroupBytes = 100ll << 20; // K and V bytes of a group (target
 constexpr int64_t kL2Hold = 128ll << 20;     // K and V bytes held in L2 between reads
 constexpr int kTileBytes = 128 * 128 * 2;    // 128 rows of up to 128 16-bit values
 constexpr uint32_t kSleepNs = 20000;         // suspend hint of barrier waits
+constexpr int kCuSmem = 256;                 // packed sequences: offsets held in shared memory
 // fp32 2^23 + 2^22 + 0x6600: adding it rounds to an integer n (ties to even)
 // and leaves 0x6600 + n, the fp16 bits of 1536 + n, in the low 16 bits.
 constexpr float kCodeMagic = 12609024.0f;
@@ -158,6 +159,11 @@ struct alignas(1024) PSmem {
   Slot slot[kStages];
   float red[8];
   int abort;
+  // packed instances (at most kCuSmem sequences): cu_seqlens_k and _q,
+  // copied at the start (every item looks up its sequence's offsets; from
+  // global memory each lookup is an L2 round trip on the producer's path)
+  int32_t cu_k[kCuSmem + 1];
+  int32_t cu_q[kCuSmem + 1];
 };
 
 __device__ __forceinline__ int group_units(const Plan& P, int g) {
@@ -190,6 +196,67 @@ __device__ __forceinline__ void decode_b(const Plan& P, int g, int i, int* kind,
   *unit = g * P.group + u;
   *kind = P.n_kv == 0 ? kFinal : (off & 1) ? kV : kK;
   *sub = P.n_kv == 0 ? 0 : off >> 1;
+}
+
+// Packed sequences.  Lists sized by the longest sequence would carry every
+// shorter sequence's missing tiles as empty items (41 % of them for 8
+// sequences of 2k-16k tokens), each still claimed and decoded.  The packed
+// lists run over virtual tiles instead: sequence s owns tiles vt(s) ..
+// vt(s + 1) - 1, vt(s) = s + floor(cu[s] / 128), which is its workspace base
+// over 128 (ws_seg_base).  That is at least its real tile count and at most
+// one more, so a list carries at most one or two empty items per sequence.
+// Units stay sequence-major (unit = s Hkv + h); a list holds m items per
+// virtual tile and unit (K and V: 2; Q: the kv head's query heads).  The
+// entries are clamped to [0, total] and vt(nseg) comes from the host's
+// total, so every list stays within the sizes the host checked even for
+// inconsistent offsets (which check_offsets reports).
+__device__ __forceinline__ int vtile(const int32_t* cu, int s, int nseg, int64_t total) {
+  if (s <= 0) return 0;
+  int64_t c = s >= nseg ? total : static_cast<int64_t>(cu[s]);
+  c = c < 0 ? 0 : (c > total ? total : c);
+  return s + static_cast<int>(c >> 7);
+}
+
+// First item of unit u in a packed list (u = nseg Hkv: the list's end).
+__device__ __forceinline__ int vstart(const int32_t* cu, int nseg, int64_t total, int Hkv,
+                                      int m, int u) {
+  const int s = u / Hkv, h = u - s * Hkv;
+  const int v0 = vtile(cu, s, nseg, total);
+  const int w = s < nseg ? vtile(cu, s + 1, nseg, total) - v0 : 0;
+  return m * (Hkv * v0 + h * w);
+}
+
+// The sequence of the last item a producer decoded from a list: its
+// virtual tiles v0 .. v0 + w - 1.  A producer's claims from a list increase
+// by about one item per CTA, so the next item is mostly in the same
+// sequence and needs no search (each search step is a dependent load).
+struct SeqCache {
+  int s = 0, v0 = 0, w = 0;
+};
+
+// Item i of a packed list: its unit, virtual tile t within the unit's
+// sequence and place j in [0, m).  False for inconsistent offsets.
+__device__ __forceinline__ bool vdecode(const int32_t* cu, int nseg, int64_t total, int Hkv,
+                                        int m, int i, SeqCache& c, int* unit, int* t, int* j) {
+  const int q = i / m;                 // (virtual tile, kv head) slot
+  *j = i - q * m;
+  if (q < Hkv * c.v0 || q >= Hkv * (c.v0 + c.w)) {
+    int lo = 0, hi = nseg;             // the last sequence s with Hkv vt(s) <= q
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (Hkv * vtile(cu, mid, nseg, total) <= q) lo = mid;
+      else hi = mid;
+    }
+    c.s = lo;
+    c.v0 = vtile(cu, lo, nseg, total);
+    c.w = vtile(cu, lo + 1, nseg, total) - c.v0;
+  }
+  const int r = q - Hkv * c.v0;
+  if (c.w <= 0 || r < 0 || r >= Hkv * c.w) return false;
+  const int h = r / c.w;
+  *unit = c.s * Hkv + h;
+  *t = r - h * c.w;
+  return true;
 }
 
 // ------------------------------------------------------------ memory ops
@@ -344,18 +411,19 @@ __device__ __forceinline__ uint32_t row_max_transposed(uint32_t (&a)[P], int lan
   return max(a[0], __shfl_xor_sync(0xFFFFFFFFu, a[0], 1));
 }
 
-// Segment bounds (dense: the whole sequence); false on bad cu_seqlens.
-__device__ __forceinline__ bool key_range(const SegGeo& g, int64_t s, int64_t* start,
-                                          int64_t* len) {
+// Segment bounds (dense: the whole sequence) from offsets cu (g.cu_k or
+// g.cu_q, or their shared-memory copies); false on bad cu_seqlens.
+__device__ __forceinline__ bool key_range(const SegGeo& g, const int32_t* cu, int64_t s,
+                                          int64_t* start, int64_t* len) {
   *start = 0;
   *len = g.Lk;
-  return !g.varlen || seg_range(g.cu_k, s, g.total_k, g.max_k, start, len);
+  return !g.varlen || seg_range(cu, s, g.total_k, g.max_k, start, len);
 }
-__device__ __forceinline__ bool query_range(const SegGeo& g, int64_t s, int64_t* start,
-                                            int64_t* len) {
+__device__ __forceinline__ bool query_range(const SegGeo& g, const int32_t* cu, int64_t s,
+                                            int64_t* start, int64_t* len) {
   *start = 0;
   *len = g.Lq;
-  return !g.varlen || seg_range(g.cu_q, s, g.total_q, g.max_q, start, len);
+  return !g.varlen || seg_range(cu, s, g.total_q, g.max_q, start, len);
 }
 
 // Rows of the current 128-token tile for one thread: row r + R * i as
@@ -811,11 +879,13 @@ __device__ __forceinline__ float v_mul_of(uint32_t m) {
 }
 
 // ------------------------------------------------------------- consumers
-template <bool kTma, bool kBf16, int DP>
+template <bool kTma, bool kBf16, int DP, bool kPacked>
 __device__ __forceinline__ void consume(const ProParams& p, const Slot& it, int stage,
                                         PSmem& sm) {
   constexpr int G = DP / 8;
   const SegGeo& g = p.g;
+  const int32_t* cuk = kPacked ? sm.cu_k : g.cu_k;   // packed: the shared copies
+  const int32_t* cuq = kPacked ? sm.cu_q : g.cu_q;
   const int64_t s = it.unit / g.Hkv, h = it.unit % g.Hkv;
   const int lc = threadIdx.x % G, r = threadIdx.x / G, c0 = lc * 8;
   TileRows<kTma, DP> rows;
@@ -826,7 +896,7 @@ __device__ __forceinline__ void consume(const ProParams& p, const Slot& it, int 
   if (it.kind == kQ) {
     const int64_t hq = h * (g.Hq / g.Hkv) + it.sub / p.plan.nqt;
     const int64_t t0 = static_cast<int64_t>(it.sub % p.plan.nqt) * kBlockM;
-    query_range(g, s, &start, &len);
+    query_range(g, cuq, s, &start, &len);
     if constexpr (!kTma) {
       rows.row0 = p.q + (g.varlen ? start * g.q_tok_stride : s * g.q_seg_stride) +
                   hq * g.q_head_stride + (t0 + r) * g.q_tok_stride;
@@ -837,7 +907,7 @@ __device__ __forceinline__ void consume(const ProParams& p, const Slot& it, int 
     q_tile<kBf16, DP>(p, it.nvalid, rows, p.q16 + (row0 + r) * DP + c0, p.s_q + row0);
     return;
   }
-  const bool seg_ok = key_range(g, s, &start, &len);
+  const bool seg_ok = key_range(g, cuk, s, &start, &len);
   const int64_t t0 = static_cast<int64_t>(it.sub) * kBlockN;
   if constexpr (!kTma) {
     const uint16_t* src = (it.kind == kStatsK || it.kind == kK) ? p.k : p.v;
@@ -1007,8 +1077,30 @@ __device__ __forceinline__ bool hand_over(const ProParams& p, PSmem& sm, int uni
   return true;
 }
 
+// Packed sequences: each CTA's helper warp checks its share of the offsets
+// (the lists over virtual tiles cover every tile only for consistent ones)
+// and reports an inconsistent entry in the status word.
+__device__ __forceinline__ void check_offsets(const ProParams& p) {
+  const SegGeo& g = p.g;
+  const int64_t per = (g.nseg + gridDim.x - 1) / gridDim.x;
+  const int64_t s0 = static_cast<int64_t>(blockIdx.x) * per;
+  const int64_t s1 = s0 + per < g.nseg ? s0 + per : g.nseg;
+  bool bad = false;
+  for (int64_t s = s0 + (threadIdx.x & 31); s < s1; s += 32) {
+    int64_t start, len;
+    bad |= !seg_range(g.cu_k, s, g.total_k, g.max_k, &start, &len) ||
+           !seg_range(g.cu_q, s, g.total_q, g.max_q, &start, &len);
+  }
+  if (__any_sync(0xFFFFFFFFu, bad) && (threadIdx.x & 31) == 0)
+    atomicOr(p.status, kStatusBadSeqlens);
+}
+
 // -------------------------------------------------------------- producer
-template <bool kTma, bool kBf16, int DP>
+// kPacked: packed sequences, whose lists run over virtual tiles (vdecode).
+// It is a template parameter so that the other instances keep the plain
+// per-unit lists with no trace of it (the extra live state alone made the
+// dense prologue 8 % slower).
+template <bool kTma, bool kBf16, int DP, bool kPacked>
 __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
   const SegGeo& g = p.g;
   const Plan& P = p.plan;
@@ -1028,6 +1120,44 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
   bool q_left = P.n_q > 0;   // the Q list may still have items
   const uint32_t grid = gridDim.x;
   uint64_t idle0 = 0;
+  // packed lists: the first item and size of groups ga and gb (over
+  // virtual tiles), the Q list's size, and the sequence of the last A, B and
+  // Q item decoded (B holds one final item per unit without K/V items)
+  const bool pk_b = kPacked && P.n_kv > 0;
+  const int nseg = static_cast<int>(g.nseg), hkv = static_cast<int>(g.Hkv);
+  const int32_t* cuk = kPacked ? sm.cu_k : g.cu_k;   // packed: the shared copies
+  const int32_t* cuq = kPacked ? sm.cu_q : g.cu_q;
+  const int gq = static_cast<int>(g.Hq / g.Hkv);
+  int a_first = 0, a_size = 0, b_first = 0, b_size = 0, q_size = 0;
+  SeqCache ca, cb, cq;
+  auto kv_first = [&](int gi) {
+    return vstart(cuk, nseg, g.total_k, hkv, 2, min(gi * P.group, P.units));
+  };
+  auto set_a = [&]() {
+    if constexpr (kPacked) {
+      if (ga < P.groups) {
+        a_first = kv_first(ga);
+        a_size = kv_first(ga + 1) - a_first;
+      }
+    }
+  };
+  auto set_b = [&]() {
+    if constexpr (kPacked) {
+      if (gb < P.groups) {
+        b_first = pk_b ? kv_first(gb) : 0;
+        b_size = pk_b ? kv_first(gb + 1) - b_first : group_units(P, gb) * P.n_b;
+      }
+    }
+  };
+  if constexpr (kPacked) {
+    set_a();
+    set_b();
+    q_size = P.n_q > 0 ? vstart(cuq, nseg, g.total_q, hkv, gq, P.units) : 0;
+  }
+  // a packed item outside its sequence's tiles (inconsistent offsets)
+  auto bad_offsets = [&]() {
+    if (lane == 0) atomicOr(p.status, kStatusBadSeqlens);
+  };
   while (ok) {
     // ---- choose the next item: a B item if its group is final, else an A
     // item (at most `lead` groups ahead of the B list), else a Q item, else
@@ -1054,8 +1184,19 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
       if (!b_pend && lane == 0) b_idx = static_cast<int>(atomicAdd(p.cnt_b + gb, 1u));
       const int idx = __shfl_sync(0xFFFFFFFFu, b_idx, 0);
       b_pend = false;
-      if (idx < group_units(P, gb) * P.n_b) {
-        decode_b(P, gb, idx, &it.kind, &it.unit, &it.sub);
+      if (idx < (kPacked ? b_size : group_units(P, gb) * P.n_b)) {
+        if (pk_b) {
+          int u, t, j;
+          if (vdecode(cuk, nseg, g.total_k, hkv, 2, b_first + idx, cb, &u, &t, &j)) {
+            it.kind = j ? kV : kK;
+            it.unit = u;
+            it.sub = t;
+          } else {
+            bad_offsets();
+          }
+        } else {
+          decode_b(P, gb, idx, &it.kind, &it.unit, &it.sub);
+        }
         // claim the group's next B item now; it is used on the next turn
         if (lane == 0) b_idx = static_cast<int>(atomicAdd(p.cnt_b + gb, 1u));
         b_pend = true;
@@ -1063,6 +1204,7 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
       }
       ++gb;
       b_open = P.open != 0;
+      set_b();
     }
     // the Q list: a lambda, taken before or after the A list
     auto take_q = [&]() {
@@ -1070,8 +1212,19 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
         if (!q_pend && lane == 0) q_idx = static_cast<int>(atomicAdd(p.cnt_q, 1u));
         const int idx = __shfl_sync(0xFFFFFFFFu, q_idx, 0);
         q_pend = false;
-        if (idx < P.units * P.n_q) {
-          decode_q(P, idx, &it.kind, &it.unit, &it.sub);
+        if (idx < (kPacked ? q_size : P.units * P.n_q)) {
+          if constexpr (kPacked) {
+            int u, t, j;
+            if (!vdecode(cuq, nseg, g.total_q, hkv, gq, idx, cq, &u, &t, &j)) {
+              bad_offsets();
+            } else if (t < P.nqt) {      // else the sequence's spare virtual tile
+              it.kind = kQ;
+              it.unit = u;
+              it.sub = j * P.nqt + t;
+            }
+          } else {
+            decode_q(P, idx, &it.kind, &it.unit, &it.sub);
+          }
           if (lane == 0) q_idx = static_cast<int>(atomicAdd(p.cnt_q, 1u));
           q_pend = true;
         } else {
@@ -1084,8 +1237,19 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
       if (!a_pend && lane == 0) a_idx = static_cast<int>(atomicAdd(p.cnt_a + ga, 1u));
       const int idx = __shfl_sync(0xFFFFFFFFu, a_idx, 0);
       a_pend = false;
-      if (idx < group_units(P, ga) * P.n_stats) {
-        decode_a(P, ga, idx, &it.kind, &it.unit, &it.sub);
+      if (idx < (kPacked ? a_size : group_units(P, ga) * P.n_stats)) {
+        if constexpr (kPacked) {
+          int u, t, j;
+          if (vdecode(cuk, nseg, g.total_k, hkv, 2, a_first + idx, ca, &u, &t, &j)) {
+            it.kind = j ? kStatsV : kStatsK;
+            it.unit = u;
+            it.sub = t;
+          } else {
+            bad_offsets();
+          }
+        } else {
+          decode_a(P, ga, idx, &it.kind, &it.unit, &it.sub);
+        }
         // claim the group's next A item now (A items never wait, so holding
         // the claim cannot hold up a barrier)
         if (lane == 0) a_idx = static_cast<int>(atomicAdd(p.cnt_a + ga, 1u));
@@ -1095,6 +1259,7 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
         it.unit = ga;
         marker = true;
         ++ga;
+        set_a();
       }
     }
     if (!P.q_first) take_q();
@@ -1144,11 +1309,11 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
       h = it.unit % g.Hkv;
       bool seg_ok;
       if (it.kind == kQ) {
-        seg_ok = query_range(g, s, &start, &len);
+        seg_ok = query_range(g, cuq, s, &start, &len);
         h = h * (g.Hq / g.Hkv) + it.sub / P.nqt;        // query head
         t0 = static_cast<int64_t>(it.sub % P.nqt) * kBlockM;
       } else {
-        seg_ok = key_range(g, s, &start, &len);
+        seg_ok = key_range(g, cuk, s, &start, &len);
         t0 = static_cast<int64_t>(it.sub) * kBlockN;
       }
       if (!seg_ok) {
@@ -1225,7 +1390,7 @@ __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
 }
 
 // --------------------------------------------------------------- kernel
-template <bool kTma, bool kBf16, int DP>
+template <bool kTma, bool kBf16, int DP, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 3)
 prologue_kernel(const __grid_constant__ ProParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -1242,6 +1407,12 @@ prologue_kernel(const __grid_constant__ ProParams p) {
     sm.abort = 0;
     mbar_fence_init();
   }
+  if constexpr (kPacked) {          // at most kCuSmem sequences (launch_any)
+    for (int i = threadIdx.x; i <= p.g.nseg; i += kThreads) {
+      sm.cu_k[i] = p.g.cu_k[i];
+      sm.cu_q[i] = p.g.cu_q[i];
+    }
+  }
   __syncthreads();
   const int warp = threadIdx.x >> 5;
   if (warp == kProducerWarp) {
@@ -1252,10 +1423,11 @@ prologue_kernel(const __grid_constant__ ProParams p) {
         tma_prefetch_desc(&p.mv);
       }
     }
-    produce<kTma, kBf16, DP>(p, sm);
+    produce<kTma, kBf16, DP, kPacked>(p, sm);
     return;
   }
   if (warp == kHelperWarp) {
+    if constexpr (kPacked) check_offsets(p);
     helper<kBf16, DP>(p, sm);
     return;
   }
@@ -1265,7 +1437,7 @@ prologue_kernel(const __grid_constant__ ProParams p) {
     if (!mbar_sleep_wait(&sm.full[stage], phase, &sm.abort, p.status, p.timeout_ns)) break;
     const Slot it = sm.slot[stage];
     if (it.kind == kEnd) break;
-    if (it.kind != kGroupEnd) consume<kTma, kBf16, DP>(p, it, stage, sm);
+    if (it.kind != kGroupEnd) consume<kTma, kBf16, DP, kPacked>(p, it, stage, sm);
     csync();                                    // every consumer is done with the stage
     if (threadIdx.x == 0) {
       if (it.kind <= kStatsV) {
@@ -1302,6 +1474,12 @@ bool make_plan(const SegGeo& g, int mode, Plan* out) {
   const int64_t n_kv = (mode == kPlanAll || mode == kPlanKV) ? 2 * nkb : 0;
   const int64_t per = n_stats + n_q + (n_kv > 0 ? n_kv : 1);
   if (units * per >= (int64_t(1) << 31)) return false;
+  if (g.varlen) {
+    // packed lists: 2 (K and V) or Hq / Hkv (Q) items per virtual tile and
+    // kv head, nseg + total / 128 virtual tiles
+    const int64_t vk = g.nseg + g.total_k / kBlockN + 1, vq = g.nseg + g.total_q / kBlockM + 1;
+    if (2 * g.Hkv * vk >= (int64_t(1) << 31) || g.Hq * vq >= (int64_t(1) << 31)) return false;
+  }
   int64_t group = units, lead = 1;
   if (n_kv > 0 && stats) {
     // a group's K and V are read by its A list and again (from L2) by its B
@@ -1372,7 +1550,7 @@ bool view_map(CUtensorMap* map, const uint16_t* base, int64_t D, int64_t Dp, int
                       dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-template <bool kTma, bool kBf16, int DP>
+template <bool kTma, bool kBf16, int DP, bool kPacked>
 cudaError_t launch_t(ProParams& prm, int mode, cudaStream_t st) {
   // resident CTAs per SM, per device (filled once; every thread computes
   // the same value, so relaxed atomics suffice)
@@ -1382,12 +1560,12 @@ cudaError_t launch_t(ProParams& prm, int mode, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (per_sm[dev].load(std::memory_order_relaxed) == 0) {
-    e = cudaFuncSetAttribute(prologue_kernel<kTma, kBf16, DP>,
+    e = cudaFuncSetAttribute(prologue_kernel<kTma, kBf16, DP, kPacked>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prologue_kernel<kTma, kBf16, DP>,
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prologue_kernel<kTma, kBf16, DP, kPacked>,
                                                       kThreads, kSmemBytes);
     if (e != cudaSuccess) return e;
     per_sm[dev].store(n > 0 ? n : 1, std::memory_order_relaxed);
@@ -1401,11 +1579,26 @@ cudaError_t launch_t(ProParams& prm, int mode, cudaStream_t st) {
   // cooperative launch of exactly the resident CTAs
   const unsigned grid = static_cast<unsigned>(sms * per_sm[dev].load(std::memory_order_relaxed));
   void* args[] = {&prm};
-  e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(prologue_kernel<kTma, kBf16, DP>),
+  e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(prologue_kernel<kTma, kBf16, DP, kPacked>),
                                   dim3(grid), dim3(kThreads), args, kSmemBytes, st);
   if (e != cudaSuccess) return e;
   note_launch();
   return cudaGetLastError();
+}
+
+// Packed sequences take the lists over virtual tiles (vdecode) when at least
+// a quarter of the items in lists sized by the longest sequence would be
+// empty, judged from the host's sizes: the listed tiles are nseq
+// ceil(max_k / 128) and the real ones at most total_k / 128 + nseq.  Each
+// packed item costs the producer a little more (5-7 % with equal lengths,
+// no empty items to save); with 8 sequences of 2k-16k tokens (41 % empty)
+// the packed lists were 9 % faster at Dp = 64 and as fast at Dp = 128.
+// The offsets then sit in shared memory, which bounds the sequences.
+bool packed_lists(const SegGeo& g) {
+  if (!g.varlen || g.nseg > kCuSmem) return false;
+  const int64_t listed = g.nseg * ((g.max_k + kBlockN - 1) / kBlockN);
+  const int64_t real_max = g.total_k / kBlockN + g.nseg;
+  return 4 * real_max <= 3 * listed;
 }
 
 cudaError_t launch_any(ProParams& prm, bool vec, int mode, cudaStream_t st) {
@@ -1435,15 +1628,21 @@ cudaError_t launch_any(ProParams& prm, bool vec, int mode, cudaStream_t st) {
                       !input_map(&prm.mv, prm.v, g.D, g.Dp, g.Hkv, g.Lk, ntk, prm.k_hnd)))
         return cudaErrorInvalidValue;
     }
-    if (bf16) return d64 ? launch_t<true, true, 64>(prm, mode, st)
-                         : launch_t<true, true, 128>(prm, mode, st);
-    return d64 ? launch_t<true, false, 64>(prm, mode, st)
-               : launch_t<true, false, 128>(prm, mode, st);
+    if (packed_lists(g)) {
+      if (bf16) return d64 ? launch_t<true, true, 64, true>(prm, mode, st)
+                           : launch_t<true, true, 128, true>(prm, mode, st);
+      return d64 ? launch_t<true, false, 64, true>(prm, mode, st)
+                 : launch_t<true, false, 128, true>(prm, mode, st);
+    }
+    if (bf16) return d64 ? launch_t<true, true, 64, false>(prm, mode, st)
+                         : launch_t<true, true, 128, false>(prm, mode, st);
+    return d64 ? launch_t<true, false, 64, false>(prm, mode, st)
+               : launch_t<true, false, 128, false>(prm, mode, st);
   }
-  if (bf16) return d64 ? launch_t<false, true, 64>(prm, mode, st)
-                       : launch_t<false, true, 128>(prm, mode, st);
-  return d64 ? launch_t<false, false, 64>(prm, mode, st)
-             : launch_t<false, false, 128>(prm, mode, st);
+  if (bf16) return d64 ? launch_t<false, true, 64, false>(prm, mode, st)
+                       : launch_t<false, true, 128, false>(prm, mode, st);
+  return d64 ? launch_t<false, false, 64, false>(prm, mode, st)
+             : launch_t<false, false, 128, false>(prm, mode, st);
 }
 
 }  // namespace

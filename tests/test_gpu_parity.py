@@ -81,6 +81,12 @@ SMALL = [
     _small("varlen_many_causal_bf16", B=0, Hq=2, Hkv=2, Lq=0, Lk=0, D=128, layout=wl.NHD,
            seed=22, dtype=wl.BF16, causal=True,
            seqlens_q=_lengths(64, 1, 400, 212), seqlens_k=_lengths(64, 1, 400, 212)),
+    # more sequences than the prologue holds offsets for in shared memory:
+    # the work lists sized by the longest sequence (D = 64: at D = 32 a
+    # sequence of 4 queries over 52 keys has cosine 0.99897 to exact
+    # attention in the oracle itself, below the bar)
+    _small("varlen_300_sequences", B=0, Hq=2, Hkv=1, Lq=0, Lk=0, D=64, layout=wl.NHD, seed=23,
+           seqlens_q=_lengths(300, 1, 60, 213), seqlens_k=_lengths(300, 0, 60, 214, zeros=12)),
 ]
 
 
@@ -88,7 +94,7 @@ SMALL = [
 # millions of P~ codes, so a near-tie that the kernel's exp2 rounds the other
 # way (H.near_tie_rows) lands on a heavily weighted key now and then; one such
 # row measured 2.8e-3.  Everything else stays within H.ATOL_ORACLE.
-STRESS = {"varlen_many", "varlen_many_causal_bf16"}
+STRESS = {"varlen_many", "varlen_many_causal_bf16", "varlen_300_sequences"}
 
 
 def _check_prologue(sage, orc, w, inp, d):
@@ -356,6 +362,18 @@ def test_inconsistent_cu_seqlens_reported(sage):
     out = torch.zeros(300, 2, 64, device="cuda")
     ws = sage.alloc_workspace(sage.workspace_bytes_varlen(2, 300, 300, 2, 2, 64))
     sage.attn_fwd_varlen(q, q, q, out, cu, cu, 200, 200, ws=ws)
+    assert sage.device_status(ws) == sage.ERR_INVALID_ARG
+
+
+def test_inconsistent_cu_seqlens_reported_packed_lists(sage):
+    """The same with sizes for which the prologue's work lists run over the
+    sequences' own tiles (a declared maximum far above the mean length): the
+    offsets are checked on the device and the call reports them."""
+    q = torch.randn(300, 2, 64, dtype=torch.float16, device="cuda")
+    cu = torch.tensor([0, 100, 50, 150, 300], dtype=torch.int32, device="cuda")  # 100 > 50
+    out = torch.zeros(300, 2, 64, device="cuda")
+    ws = sage.alloc_workspace(sage.workspace_bytes_varlen(4, 300, 300, 2, 2, 64))
+    sage.attn_fwd_varlen(q, q, q, out, cu, cu, 1000, 1000, ws=ws)
     assert sage.device_status(ws) == sage.ERR_INVALID_ARG
 
 
