@@ -38,7 +38,10 @@
 // fills the waits).  Beyond L2, the part of K and V that does not stay there
 // is read again from HBM.  The Q tiles depend on nothing: they form one more
 // list, taken only when neither of the others has an item ready, so they
-// fill the barrier waits and the end.  Nothing waits inside a list, and
+// fill the barrier waits and the end.  A unit's items are its tiles up to
+// the longest sequence's count; packed sequences whose lists would then be
+// a quarter empty or more take lists over each sequence's own tiles instead
+// (packed_lists, vdecode).  Nothing waits inside a list, and
 // every wait is bounded (timeout -> status bit).  Every 128-token
 // tile of the workspace is written in full (zeros past the sequence end and
 // past D), so the attention kernel never reads stale bytes.
@@ -1096,10 +1099,11 @@ __device__ __forceinline__ void check_offsets(const ProParams& p) {
 }
 
 // -------------------------------------------------------------- producer
-// kPacked: packed sequences, whose lists run over virtual tiles (vdecode).
-// It is a template parameter so that the other instances keep the plain
-// per-unit lists with no trace of it (the extra live state alone made the
-// dense prologue 8 % slower).
+// kPacked: packed sequences, whose lists run over virtual tiles (vdecode;
+// packed_lists chooses).  It is a template parameter so that the other
+// instances keep the plain per-unit lists with no trace of it: with the
+// packed code in a shared instance the dense prologue ran 8 % slower
+// without executing any of it.
 template <bool kTma, bool kBf16, int DP, bool kPacked>
 __device__ __forceinline__ void produce(const ProParams& p, PSmem& sm) {
   const SegGeo& g = p.g;
