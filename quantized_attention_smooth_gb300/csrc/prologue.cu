@@ -1592,7 +1592,7 @@ cudaError_t launch_t(ProParams& prm, int mode, cudaStream_t st) {
 
 // Packed sequences take the lists over virtual tiles (vdecode) when at least
 // a quarter of the items in lists sized by the longest sequence would be
-// empty, judged from the host's sizes: the listed tiles are nseq
+// empty, estimated from the host's sizes: the listed tiles are nseq
 // ceil(max_k / 128) and the real ones at most total_k / 128 + nseq.  Each
 // packed item costs the producer a little more (5-7 % with equal lengths,
 // no empty items to save); with 8 sequences of 2k-16k tokens (41 % empty)
